@@ -1,0 +1,198 @@
+/*
+ * moe_cache.h — C ABI of the routed Mixture-of-Experts layer over a
+ * GPU-resident expert-slot cache (one GB300 GPU, sm_103a).
+ *
+ * What one layer call computes (sources, by page title and section):
+ *  1. Router: the top-k experts of each token and their weights
+ *     ("llama.cpp + MoE expert cache", "The idea: cache the hot experts on the
+ *     GPU", step 1).  Top-k of the raw fp32 logits, descending, ties to the lower
+ *     expert id; weight = softmax probability over all E experts
+ *     (weight_mode 0) or renormalised over the chosen k (weight_mode 1).
+ *  2. Slot table, -1 = not cached (same section, step 2), kept per layer with
+ *     least-recently-used replacement under a fixed budget of slots
+ *     ("Longhaul MoE loading", opening paragraph).  The call's experts are
+ *     planned as one batch: experts it needs are never evicted by it, and each
+ *     distinct expert is loaded at most once (same page, the paragraph on
+ *     expert IDs planned as a batch).
+ *  3. Missing experts are copied from the host store into their slots
+ *     ("llama.cpp + MoE expert cache", "Keeping the cache fresh": a slot is
+ *     published only after its copy completes).
+ *  4. Each (token, expert) pair is computed exactly once from its slot
+ *     (same page, "The idea", step 3): Q4_0 SwiGLU FFN, h = silu(W_gate x) *
+ *     (W_up x), y = W_down h ("Limitations": merged gate/up, SiLU).
+ *  5. Weighted sum out_t = sum_k w[t,k] y[t,k], ascending k ("The idea", step 4).
+ *  If one call needs more distinct experts than there are slots, the call runs
+ *  in stages and the partial results are summed ("Longhaul MoE loading", the
+ *  paragraph on --ubatch-size and stages).
+ *
+ * Weights: Q4_0, 18 bytes per 32 values ("Multi-GPU LLM Calculator: VRAM Split
+ * and RAM Offload", "Memory placement"): fp16 scale d (little-endian), then 16
+ * bytes whose low nibbles are values 0..15 and high nibbles values 16..31,
+ * w = (q - 8) * d.  One expert block = [gate: F rows x H/32 blocks]
+ * [up: F rows x H/32 blocks][down: H rows x F/32 blocks], rows row-major
+ * (row r = output feature r, blocks along the input dimension).
+ *
+ * Conventions for every entry point:
+ *  - Return value: MOE_OK (0) or one of the MOE_ERR_* codes; nothing else
+ *    crosses the ABI (no exceptions, no aborts).
+ *  - "device" pointers are CUDA device memory owned by the caller; "host"
+ *    pointers are ordinary host memory owned by the caller.
+ *  - Work is stream-ordered on the caller's stream; results are valid when that
+ *    stream reaches the end of the call.  A handle serves one stream/thread at a
+ *    time (not re-entrant).
+ *  - After an error detected during a call (a CUDA error, a non-finite logit, a
+ *    timeout) the handle is poisoned: later forward calls return
+ *    MOE_ERR_POISONED; stats remain readable; destroy still frees everything.
+ */
+#ifndef MOE_CACHE_H
+#define MOE_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG 1   /* bad argument or config; non-finite logit      */
+#define MOE_ERR_CUDA 2          /* a CUDA runtime call failed                     */
+#define MOE_ERR_OOM 3           /* device or pinned allocation failed             */
+#define MOE_ERR_TIMEOUT 4       /* a bounded host wait gave up                    */
+#define MOE_ERR_HOST_STORE 5    /* host store invalid or could not be registered  */
+#define MOE_ERR_POISONED 6      /* an earlier call on this handle failed          */
+#define MOE_ERR_UNSUPPORTED 7   /* shape outside what the kernels implement       */
+
+/* How misses reach their slots. */
+#define MOE_FILL_MEMCPY 0  /* cudaMemcpyAsync per missed block on a side stream into a
+                              staging area, overlapped with hit compute; then a device
+                              repack into the slot */
+#define MOE_FILL_PULL 1    /* a kernel reads the missed blocks straight from the pinned,
+                              mapped host store and writes the slot (no host round trip) */
+
+typedef struct moe_cache moe_cache;
+
+typedef struct {
+    int32_t n_layers;        /* L >= 1                                             */
+    int32_t n_experts;       /* E, 1..1024                                         */
+    int32_t top_k;           /* k, 1..min(E, 32)                                   */
+    int32_t hidden;          /* H, multiple of 256                                 */
+    int32_t ffn;             /* F, multiple of 32 with F*H a multiple of 256       */
+    int32_t slots_per_layer; /* S, 1..E: the per-layer budget of device slots      */
+    int32_t max_tokens;      /* largest n_tokens of any call, >= 1                 */
+    int32_t weight_mode;     /* 0: softmax over all E (default); 1: over chosen k  */
+    int32_t act_dtype;       /* 0: x is fp32 [T,H]; 1: x is bf16 [T,H]             */
+    int32_t fill_mode;       /* MOE_FILL_MEMCPY or MOE_FILL_PULL                   */
+    int32_t gemm_min_tokens; /* calls with n_tokens >= this use the tensor-core
+                                grouped GEMM (bf16 activations only); 0 = never    */
+    int32_t reserved;        /* must be 0                                          */
+    int64_t timeout_us;      /* limit of every bounded host wait, > 0              */
+} moe_cache_config;
+
+typedef struct {
+    const void *base;        /* host memory holding canonical Q4_0 expert blocks   */
+    uint64_t bytes;          /* size of the region at base                         */
+    uint64_t layer_stride;   /* bytes between layer l and l+1                      */
+    uint64_t expert_stride;  /* bytes between expert e and e+1 of one layer        */
+} moe_host_store;
+
+typedef struct {
+    uint64_t calls;          /* forward calls that reached planning                */
+    uint64_t pick_hits;      /* (token, pick) pairs whose expert was cached before */
+    uint64_t pick_misses;
+    uint64_t unique_hits;    /* distinct experts of a call already cached          */
+    uint64_t unique_misses;  /* distinct experts uploaded (= uploads)              */
+    uint64_t evictions;      /* uploads that replaced a cached expert              */
+    uint64_t bytes_uploaded; /* unique_misses x expert block bytes                 */
+    uint64_t stages;         /* sum over calls of the number of stages             */
+    uint64_t staged_calls;   /* calls that needed more than one stage              */
+    int32_t poisoned;        /* 1 once a call on the handle has failed             */
+    int32_t last_error;      /* the code that poisoned it (or MOE_OK)              */
+} moe_cache_stats_t;
+
+/*
+ * Create a cache.  cfg and store are read during the call only.
+ * The host store must stay valid and unchanged until moe_cache_destroy.  If it
+ * is not page-locked already, it is registered (cudaHostRegister, mapped) here
+ * and unregistered at destroy; failure -> MOE_ERR_HOST_STORE.  Every (layer,
+ * expert) block [base + l*layer_stride + e*expert_stride, + block bytes) must
+ * lie inside [base, base + bytes).
+ * The library allocates the slots (L x S blocks, repacked), the per-layer
+ * state, the per-call scratch for max_tokens, a side stream and events.
+ * cuda_stream: stream for the initial state set-up (NULL = legacy default).
+ * *out receives the handle (NULL on error).
+ */
+int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *store,
+                   void *cuda_stream, moe_cache **out);
+
+/*
+ * One routed-MoE layer call (steps 1-5 above, staged when needed).
+ * d_logits: device fp32 [n_tokens, E] row-major.
+ * d_x:      device [n_tokens, H] row-major, fp32 or bf16 per cfg.act_dtype.
+ * d_out:    device fp32 [n_tokens, H] row-major, overwritten.
+ * n_tokens == 0: no-op, MOE_OK.  n_tokens > max_tokens or layer out of range:
+ * MOE_ERR_INVALID_ARG.  A non-finite logit: MOE_ERR_INVALID_ARG, the layer's
+ * state is left as it was and the handle is poisoned (with MOE_FILL_PULL the
+ * check completes on the device; it is reported by the next call, by
+ * moe_cache_sync or by moe_cache_stats).
+ * Buffers must not alias each other.
+ */
+int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits, const void *d_x,
+                      int32_t n_tokens, float *d_out, void *cuda_stream);
+
+/*
+ * Wait (bounded by cfg.timeout_us) for the handle's outstanding work on
+ * cuda_stream and its side stream, then report any error raised on the device.
+ */
+int moe_cache_sync(moe_cache *c, void *cuda_stream);
+
+/* Counters of one layer, or the sum over all layers for layer == -1 (host out;
+ * synchronises with the device). */
+int moe_cache_stats(const moe_cache *c, int32_t layer, moe_cache_stats_t *out);
+
+/*
+ * Test hook: the plan of the most recent forward call, which must have been on
+ * `layer` (else MOE_ERR_INVALID_ARG).  All outputs are host arrays, any may be
+ * NULL: ids/gpu_slot/stage [n_tokens*k], w [n_tokens*k] (fp32 router weights),
+ * miss_* [n_miss] in ascending expert order (evicted = -1 for an empty slot),
+ * n_miss, n_stages.  Synchronises with the device.
+ */
+int moe_layer_last_plan(const moe_cache *c, int32_t layer, int32_t *ids, float *w,
+                        int32_t *gpu_slot, int32_t *stage, int32_t *miss_expert,
+                        int32_t *miss_slot, int32_t *miss_evicted, int32_t *miss_stage,
+                        int32_t *n_miss, int32_t *n_stages);
+
+/*
+ * Per-kernel timing with CUDA events on the streams the kernels run on.
+ * enable = 1 starts recording (resets the totals), 0 stops.  moe_cache_timing
+ * fills, for up to `cap` kernel kinds, the name (static string), the number of
+ * launches and the summed device milliseconds; returns the number of kinds in
+ * *n.  Synchronises with the device.
+ */
+int moe_cache_set_timing(moe_cache *c, int32_t enable);
+int moe_cache_timing(moe_cache *c, const char **names, uint64_t *launches, double *ms,
+                     int32_t cap, int32_t *n);
+
+/*
+ * Measured host->device bandwidth of one expert block: `iters` cudaMemcpyAsync
+ * of one block from the pinned store into the staging area on the side stream,
+ * each timed with events; *gbps receives the median in GB/s (1e9 B/s).
+ */
+int moe_cache_probe_h2d(moe_cache *c, int32_t iters, double *gbps);
+
+/* Bytes of one expert block (3 * F * H / 32 * 18) and of one device slot. */
+uint64_t moe_expert_bytes(int32_t hidden, int32_t ffn);
+
+/* Number of kernel launches the library issued since init (all streams). */
+uint64_t moe_cache_launch_count(const moe_cache *c);
+
+/* Free everything the handle owns (waits for its outstanding work first). */
+void moe_cache_destroy(moe_cache *c);
+
+/* Static description of a return code. */
+const char *moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_CACHE_H */

@@ -1,0 +1,178 @@
+// Internal declarations shared by the library's translation units (not part
+// of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+// ---------------------------------------------------------------- limits
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+constexpr int kPlanThreads = 1024;
+constexpr int kNStat = 9;  // calls, pick_hits, pick_misses, unique_hits, unique_misses,
+                           // evictions, bytes_uploaded, stages, staged_calls
+constexpr int kTokPerUnit = 8;  // tokens of one expert handled by one GEMV work unit
+
+// ------------------------------------------------------------ plan records
+// Header of one call's plan, written by the plan kernel into device scratch and
+// mirrored into the host mailbox.
+struct PlanHdr {
+  int32_t error;      // 0 ok, 1 non-finite logit (state untouched)
+  int32_t n_unique;   // |U|
+  int32_t n_hits;     // cached before the call
+  int32_t n_miss;     // uploads
+  int32_t n_stage0_miss;
+  int32_t n_stages;
+  int32_t n_units;    // GEMV work units (all stages)
+  int32_t n_evict;
+  int32_t pick_hits;
+  int32_t pick_misses;
+  int32_t hit_units;  // GEMV units of the stage-0 hits: [0, hit_units)
+  int32_t pad[5];
+};
+
+// A work item = one distinct expert of the call.  Items are ordered: stage-0
+// hits (ascending expert), then misses (ascending expert, which is stage order).
+struct WorkItem {
+  int32_t expert;
+  int32_t slot;
+  int32_t stage;
+  int32_t is_miss;
+  int32_t pair_begin;  // into perm
+  int32_t pair_count;
+};
+
+// A GEMV work unit = up to kTokPerUnit pairs of one work item.  Units follow
+// the item order, so each stage's units (and stage 0's hit units) are a range.
+struct WorkUnit {
+  int32_t item;
+  int32_t pair_begin;  // into perm
+  int32_t pair_count;
+  int32_t stage;
+};
+
+struct MissItem {
+  int32_t expert;
+  int32_t slot;
+  int32_t evicted;
+  int32_t stage;
+};
+
+// Host-visible mailbox (pinned, mapped) filled by the plan kernel at its end.
+// Followed in memory by int32 unit_begin[stage_cap] (units of stage j are
+// [unit_begin[j], unit_begin[j+1])) and MissItem miss[max distinct experts].
+struct Mailbox {
+  volatile uint32_t seq;  // written last
+  int32_t pad[3];
+  PlanHdr hdr;
+};
+
+// ------------------------------------------------ repacked slot layout
+// Each matrix of R rows x C columns (nb = C/32 blocks per row) is stored as a
+// nibble plane [nb][R][16 bytes] followed by a scale plane [nb][R] fp16.
+// Block (r, b) of the canonical layout becomes nib[(b*R + r)*16 ..] and
+// scale[b*R + r]; the 16 nibble bytes keep their canonical order.
+struct MatLayout {
+  uint64_t nib_off, sc_off;  // byte offsets inside the slot
+  int32_t rows, nb;
+};
+
+struct SlotLayout {
+  MatLayout gate, up, down;
+  uint64_t bytes;   // = canonical expert bytes
+  uint64_t stride;  // slot stride in device memory (bytes, 256-aligned)
+};
+
+inline SlotLayout make_slot_layout(int H, int F) {
+  SlotLayout s;
+  uint64_t mg = (uint64_t)F * (H / 32);
+  uint64_t md = (uint64_t)H * (F / 32);
+  s.gate = {0, mg * 16, F, H / 32};
+  s.up = {mg * 18, mg * 18 + mg * 16, F, H / 32};
+  s.down = {2 * mg * 18, 2 * mg * 18 + md * 16, H, F / 32};
+  s.bytes = 2 * mg * 18 + md * 18;
+  s.stride = (s.bytes + 255) / 256 * 256;
+  return s;
+}
+
+// ------------------------------------------------------------ launchers
+struct PlanArgs {
+  const float *logits;  // [T, E]
+  int T, E, k, S, weight_mode;
+  // per-layer state
+  int32_t *slot_expert;  // [S]
+  int32_t *expert_slot;  // [E]
+  uint64_t *slot_stamp;  // [S]
+  uint64_t *clock;       // [1]
+  uint64_t *stats;       // [kNStat]
+  uint64_t expert_bytes;
+  // per-call outputs
+  int32_t *ids;       // [T*k]
+  float *w;           // [T*k]
+  int32_t *gpu_slot;  // [T*k]
+  int32_t *stage;     // [T*k]
+  int32_t *perm;      // [T*k] pair ids grouped by work item
+  WorkItem *items;    // [min(E, T*k)]
+  WorkUnit *units;    // [min(E,T*k) + T*k/kTokPerUnit + 1]
+  int32_t *unit_begin;  // [n_stages + 1] (capacity min(E,T*k) + 2)
+  MissItem *miss;     // [min(E, T*k)]
+  PlanHdr *hdr;
+  int32_t *err_flag;  // sticky device error word of the handle
+  Mailbox *mailbox;   // device alias of the mapped host mailbox, or null
+  int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
+  uint32_t seq;
+};
+
+cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
+size_t plan_smem_bytes(int E, int S);
+
+struct FfnArgs {
+  const uint8_t *slots;  // layer's slot 0
+  uint64_t slot_stride;
+  SlotLayout lay;
+  int H, F, k;
+  const void *x;  // [T, H] fp32 or bf16
+  int x_bf16;
+  const int32_t *perm;
+  const WorkItem *items;
+  const WorkUnit *units;
+  const int32_t *unit_begin;
+  const PlanHdr *hdr;
+  float *h;  // [T*k, F]
+  float *y;  // [T*k, H]
+  int max_tok;  // largest pair count of one work unit this call can have (<= kTokPerUnit)
+};
+
+// Units [unit_lo, unit_hi) are read from unit_begin on the device:
+// range_kind 0: stage-0 hit units; 1: stage `stage` units that are misses;
+// 2: all units of stage `stage`.
+cudaError_t launch_gateup(const FfnArgs &a, int range_kind, int stage, int max_units,
+                          cudaStream_t st);
+cudaError_t launch_down(const FfnArgs &a, int range_kind, int stage, int max_units,
+                        cudaStream_t st);
+cudaError_t launch_combine(const float *y, const float *w, const PlanHdr *hdr, int T, int k,
+                           int H, float *out, cudaStream_t st);
+
+struct RepackArgs {
+  const uint8_t *src_base;  // canonical source: staging (device) or mapped host store
+  uint64_t src_layer_off;   // host store: layer offset; staging: 0
+  uint64_t src_expert_stride;  // host store: expert stride; staging: 0 (use src_slot_stride)
+  uint64_t src_slot_stride;    // staging: bytes per staged block
+  int by_expert;               // 1: source indexed by expert id; 0: by miss index in stage
+  uint8_t *slots;
+  uint64_t slot_stride;
+  SlotLayout lay;
+  const MissItem *miss;
+  const PlanHdr *hdr;
+  int stage;  // misses of this stage
+};
+cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t st);
+
+enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,
+                  K_GATHER, K_MEMCPY, K_NKINDS };
+
+}  // namespace moe

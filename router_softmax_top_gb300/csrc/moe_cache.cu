@@ -1,0 +1,692 @@
+// Host runtime and C ABI of the routed-MoE expert-slot cache (see
+// include/moe_cache.h for the contract of every entry point).
+//
+// Per layer call, on the caller's stream:
+//   plan kernel (router + LRU slot map + work lists)
+//   -> stage-0 hit gate/up (does not wait for any copy)
+//   -> [fill] misses of the stage: cudaMemcpyAsync per block on the side stream
+//      into staging, then a repack kernel into the slots (MOE_FILL_MEMCPY), or a
+//      repack kernel reading the mapped host store directly (MOE_FILL_PULL)
+//   -> miss gate/up -> down -> (next stage ...) -> weighted combine.
+// The host learns the miss list from a mapped mailbox the plan kernel writes
+// ("Longhaul MoE loading": one synchronisation per routed layer to discover the
+// selected experts and populate missing slots).  A slot is only read by kernels
+// ordered after its copy ("llama.cpp + MoE expert cache", "Keeping the cache
+// fresh": publish after the copy completes).
+#include <algorithm>
+#include <atomic>
+#include <chrono>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "common.cuh"
+#include "moe_cache.h"
+
+#define MOE_API extern "C" __attribute__((visibility("default")))
+
+using namespace moe;
+
+namespace {
+
+struct TimingPool {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;  // pairs
+  std::vector<int> kind;
+  int used = 0;
+  double ms[K_NKINDS] = {};
+  uint64_t n[K_NKINDS] = {};
+};
+
+}  // namespace
+
+struct moe_cache {
+  moe_cache_config cfg;
+  moe_host_store store;
+  int device = 0;
+  bool registered = false;
+  const uint8_t *host_dev = nullptr;  // device-visible alias of the host store
+  SlotLayout lay;
+  uint64_t expert_bytes = 0;
+  int maxP = 0, maxU = 0, maxUnits = 0, maxStages = 0;
+
+  // persistent device state
+  uint8_t *d_slots = nullptr;
+  int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
+  uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
+
+  // per-call scratch
+  int32_t *d_ids = nullptr, *d_gpu_slot = nullptr, *d_stage = nullptr, *d_perm = nullptr;
+  int32_t *d_unit_begin = nullptr;
+  float *d_w = nullptr, *d_h = nullptr, *d_y = nullptr;
+  WorkItem *d_items = nullptr;
+  WorkUnit *d_units = nullptr;
+  MissItem *d_miss = nullptr;
+  PlanHdr *d_hdr = nullptr;
+  uint8_t *d_staging = nullptr;
+  int staging_blocks = 0;
+
+  // mapped host words
+  unsigned char *h_mail_raw = nullptr;
+  Mailbox *h_mail = nullptr, *d_mail = nullptr;
+  int32_t *h_mail_ub = nullptr;
+  MissItem *h_mail_miss = nullptr;
+  int mail_stage_cap = 0;
+  int32_t *h_err = nullptr, *d_err = nullptr;
+  uint32_t seq = 0;
+
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_plan = nullptr;
+  std::vector<cudaEvent_t> ev_up, ev_done;
+
+  int poisoned = 0, last_error = MOE_OK;
+  int last_layer = -1, last_T = 0;
+  std::atomic<uint64_t> launches{0};
+  TimingPool tp;
+};
+
+namespace {
+
+const char *const kKindNames[K_NKINDS] = {"plan",      "repack",    "q4_gateup_gemv", "q4_down_gemv",
+                                          "combine",   "gemm_gateup", "gemm_down",    "gather",
+                                          "h2d_memcpy"};
+
+int poison(moe_cache *c, int code) {
+  if (!c->poisoned) {
+    c->poisoned = 1;
+    c->last_error = code;
+  }
+  return code;
+}
+
+// --- timing: event pairs on the launching stream
+void tp_flush(moe_cache *c) {
+  TimingPool &t = c->tp;
+  if (t.used == 0) return;
+  cudaEventSynchronize(t.ev[2 * (t.used - 1) + 1]);
+  for (int i = 0; i < t.used; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) == cudaSuccess) {
+      t.ms[t.kind[i]] += ms;
+      t.n[t.kind[i]] += 1;
+    }
+  }
+  t.used = 0;
+}
+
+int tp_begin(moe_cache *c, int kind, cudaStream_t st) {
+  TimingPool &t = c->tp;
+  if (!t.on) return -1;
+  if (t.used == (int)t.kind.size()) tp_flush(c);
+  const int i = t.used++;
+  t.kind[i] = kind;
+  cudaEventRecord(t.ev[2 * i], st);
+  return i;
+}
+
+void tp_end(moe_cache *c, int i, cudaStream_t st) {
+  if (i >= 0) cudaEventRecord(c->tp.ev[2 * i + 1], st);
+}
+
+struct Launch {
+  moe_cache *c;
+  cudaStream_t st;
+  int idx;
+  Launch(moe_cache *c_, int kind, cudaStream_t s) : c(c_), st(s) {
+    idx = tp_begin(c, kind, s);
+    if (kind != K_MEMCPY) c->launches.fetch_add(1, std::memory_order_relaxed);
+  }
+  ~Launch() { tp_end(c, idx, st); }
+};
+
+double now_us() {
+  using namespace std::chrono;
+  return (double)duration_cast<nanoseconds>(steady_clock::now().time_since_epoch()).count() * 1e-3;
+}
+
+// Wait for the plan kernel's mailbox write, bounded by cfg.timeout_us.
+int wait_mailbox(moe_cache *c, uint32_t seq, cudaStream_t st) {
+  const double t0 = now_us();
+  uint32_t *p = const_cast<uint32_t *>(&c->h_mail->seq);
+  for (uint64_t it = 0;; ++it) {
+    if (__atomic_load_n(p, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
+    if ((it & 255) == 255) {
+      const cudaError_t e = cudaStreamQuery(st);
+      if (e != cudaSuccess && e != cudaErrorNotReady) return MOE_ERR_CUDA;
+      if (e == cudaSuccess) {
+        // the stream drained: the plan kernel has finished, so its mailbox write
+        // must show up; give the host view a short grace period
+        const double t1 = now_us();
+        while (now_us() - t1 < 2000.0)
+          if (__atomic_load_n(p, __ATOMIC_ACQUIRE) == seq) return MOE_OK;
+        return MOE_ERR_CUDA;
+      }
+      if (now_us() - t0 > (double)c->cfg.timeout_us) return MOE_ERR_TIMEOUT;
+    }
+  }
+}
+
+int wait_stream(cudaStream_t st, int64_t timeout_us) {
+  const double t0 = now_us();
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(st);
+    if (e == cudaSuccess) return MOE_OK;
+    if (e != cudaErrorNotReady) return MOE_ERR_CUDA;
+    if (now_us() - t0 > (double)timeout_us) return MOE_ERR_TIMEOUT;
+  }
+}
+
+template <typename T>
+cudaError_t dalloc(T **p, size_t n) {
+  return cudaMalloc(reinterpret_cast<void **>(p), sizeof(T) * (n ? n : 1));
+}
+
+void free_all(moe_cache *c) {
+  cudaFree(c->d_slots);
+  cudaFree(c->d_slot_expert);
+  cudaFree(c->d_expert_slot);
+  cudaFree(c->d_slot_stamp);
+  cudaFree(c->d_clock);
+  cudaFree(c->d_stats);
+  cudaFree(c->d_ids);
+  cudaFree(c->d_gpu_slot);
+  cudaFree(c->d_stage);
+  cudaFree(c->d_perm);
+  cudaFree(c->d_unit_begin);
+  cudaFree(c->d_w);
+  cudaFree(c->d_h);
+  cudaFree(c->d_y);
+  cudaFree(c->d_items);
+  cudaFree(c->d_units);
+  cudaFree(c->d_miss);
+  cudaFree(c->d_hdr);
+  cudaFree(c->d_staging);
+  if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
+  if (c->h_err) cudaFreeHost(c->h_err);
+  if (c->side) cudaStreamDestroy(c->side);
+  if (c->ev_plan) cudaEventDestroy(c->ev_plan);
+  for (auto e : c->ev_up) cudaEventDestroy(e);
+  for (auto e : c->ev_done) cudaEventDestroy(e);
+  for (auto e : c->tp.ev) cudaEventDestroy(e);
+  if (c->registered) cudaHostUnregister(const_cast<void *>(c->store.base));
+}
+
+int check_config(const moe_cache_config *g) {
+  if (g->n_layers < 1 || g->n_experts < 1 || g->n_experts > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (g->top_k < 1 || g->top_k > g->n_experts || g->top_k > kMaxTopK) return MOE_ERR_INVALID_ARG;
+  if (g->slots_per_layer < 1 || g->slots_per_layer > g->n_experts) return MOE_ERR_INVALID_ARG;
+  if (g->max_tokens < 1 || (int64_t)g->max_tokens * g->top_k > (1 << 22)) return MOE_ERR_INVALID_ARG;
+  if (g->weight_mode != 0 && g->weight_mode != 1) return MOE_ERR_INVALID_ARG;
+  if (g->act_dtype != 0 && g->act_dtype != 1) return MOE_ERR_INVALID_ARG;
+  if (g->fill_mode != MOE_FILL_MEMCPY && g->fill_mode != MOE_FILL_PULL) return MOE_ERR_INVALID_ARG;
+  if (g->gemm_min_tokens < 0 || g->reserved != 0 || g->timeout_us <= 0) return MOE_ERR_INVALID_ARG;
+  if (g->hidden < 64 || g->hidden % 64 || g->ffn < 64 || g->ffn % 64) return MOE_ERR_UNSUPPORTED;
+  if (g->hidden > 16384 || g->ffn > 16384) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+
+// ======================================================================= ABI
+
+MOE_API uint64_t moe_expert_bytes(int32_t hidden, int32_t ffn) {
+  if (hidden <= 0 || ffn <= 0) return 0;
+  return 3ull * (uint64_t)ffn * (uint64_t)(hidden / 32) * 18ull;
+}
+
+MOE_API const char *moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_OOM: return "out of memory";
+    case MOE_ERR_TIMEOUT: return "timed out";
+    case MOE_ERR_HOST_STORE: return "host store invalid or not registrable";
+    case MOE_ERR_POISONED: return "handle poisoned by an earlier failure";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    default: return "unknown error";
+  }
+}
+
+MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *store,
+                           void *cuda_stream, moe_cache **out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || !store) return MOE_ERR_INVALID_ARG;
+  int rc = check_config(cfg);
+  if (rc != MOE_OK) return rc;
+  const uint64_t eb = moe_expert_bytes(cfg->hidden, cfg->ffn);
+  if (!store->base || store->expert_stride < eb || store->layer_stride == 0) return MOE_ERR_HOST_STORE;
+  if ((uintptr_t)store->base % 16 || store->expert_stride % 16 || store->layer_stride % 16)
+    return MOE_ERR_HOST_STORE;
+  const uint64_t last = (uint64_t)(cfg->n_layers - 1) * store->layer_stride +
+                        (uint64_t)(cfg->n_experts - 1) * store->expert_stride + eb;
+  if (last > store->bytes) return MOE_ERR_HOST_STORE;
+
+  moe_cache *c = new (std::nothrow) moe_cache();
+  if (!c) return MOE_ERR_OOM;
+  c->cfg = *cfg;
+  c->store = *store;
+  c->lay = make_slot_layout(cfg->hidden, cfg->ffn);
+  c->expert_bytes = eb;
+  const int E = cfg->n_experts, S = cfg->slots_per_layer, L = cfg->n_layers, k = cfg->top_k;
+  c->maxP = cfg->max_tokens * k;
+  c->maxU = std::min(E, c->maxP);
+  c->maxUnits = c->maxU + (c->maxP + kTokPerUnit - 1) / kTokPerUnit + 1;
+  c->maxStages = 2 + (c->maxU + S - 1) / S;
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+
+  auto fail = [&](int code) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return code;
+  };
+  if (cudaGetDevice(&c->device) != cudaSuccess) return fail(MOE_ERR_CUDA);
+
+  // host store: pinned and mapped
+  cudaPointerAttributes pa;
+  if (cudaPointerGetAttributes(&pa, store->base) != cudaSuccess) {
+    cudaGetLastError();
+    pa.type = cudaMemoryTypeUnregistered;
+  }
+  if (pa.type != cudaMemoryTypeHost) {
+    if (cudaHostRegister(const_cast<void *>(store->base), store->bytes,
+                         cudaHostRegisterMapped | cudaHostRegisterPortable) != cudaSuccess)
+      return fail(MOE_ERR_HOST_STORE);
+    c->registered = true;
+  }
+  void *hd = nullptr;
+  if (cudaHostGetDevicePointer(&hd, const_cast<void *>(store->base), 0) != cudaSuccess) {
+    cudaGetLastError();
+    if (cfg->fill_mode == MOE_FILL_PULL) return fail(MOE_ERR_HOST_STORE);
+    hd = nullptr;
+  }
+  c->host_dev = static_cast<const uint8_t *>(hd);
+
+  // device memory
+  const size_t slot_bytes = (size_t)L * S * c->lay.stride;
+  bool ok = cudaMalloc(&c->d_slots, slot_bytes) == cudaSuccess;
+  ok = ok && dalloc(&c->d_slot_expert, (size_t)L * S) == cudaSuccess;
+  ok = ok && dalloc(&c->d_expert_slot, (size_t)L * E) == cudaSuccess;
+  ok = ok && dalloc(&c->d_slot_stamp, (size_t)L * S) == cudaSuccess;
+  ok = ok && dalloc(&c->d_clock, (size_t)L) == cudaSuccess;
+  ok = ok && dalloc(&c->d_stats, (size_t)L * kNStat) == cudaSuccess;
+  ok = ok && dalloc(&c->d_ids, c->maxP) == cudaSuccess;
+  ok = ok && dalloc(&c->d_gpu_slot, c->maxP) == cudaSuccess;
+  ok = ok && dalloc(&c->d_stage, c->maxP) == cudaSuccess;
+  ok = ok && dalloc(&c->d_perm, c->maxP) == cudaSuccess;
+  ok = ok && dalloc(&c->d_unit_begin, c->maxStages + 1) == cudaSuccess;
+  ok = ok && dalloc(&c->d_w, c->maxP) == cudaSuccess;
+  ok = ok && dalloc(&c->d_h, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
+  ok = ok && dalloc(&c->d_y, (size_t)c->maxP * cfg->hidden) == cudaSuccess;
+  ok = ok && dalloc(&c->d_items, c->maxU) == cudaSuccess;
+  ok = ok && dalloc(&c->d_units, c->maxUnits) == cudaSuccess;
+  ok = ok && dalloc(&c->d_miss, c->maxU) == cudaSuccess;
+  ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
+  if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
+    c->staging_blocks = std::min(S, c->maxU);
+    ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess;
+  } else if (ok) {
+    c->staging_blocks = 1;  // used by the bandwidth probe only
+    ok = cudaMalloc(&c->d_staging, eb) == cudaSuccess;
+  }
+  if (!ok) return fail(MOE_ERR_OOM);
+
+  // mapped mailbox and error word
+  c->mail_stage_cap = c->maxStages + 1;
+  const size_t mail_bytes = sizeof(Mailbox) + sizeof(int32_t) * c->mail_stage_cap +
+                            sizeof(MissItem) * c->maxU;
+  if (cudaHostAlloc(&c->h_mail_raw, mail_bytes, cudaHostAllocMapped) != cudaSuccess)
+    return fail(MOE_ERR_OOM);
+  memset(c->h_mail_raw, 0, mail_bytes);
+  c->h_mail = reinterpret_cast<Mailbox *>(c->h_mail_raw);
+  c->h_mail_ub = reinterpret_cast<int32_t *>(c->h_mail + 1);
+  c->h_mail_miss = reinterpret_cast<MissItem *>(c->h_mail_ub + c->mail_stage_cap);
+  void *dm = nullptr;
+  if (cudaHostGetDevicePointer(&dm, c->h_mail_raw, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  c->d_mail = static_cast<Mailbox *>(dm);
+  if (cudaHostAlloc(&c->h_err, sizeof(int32_t) * 4, cudaHostAllocMapped) != cudaSuccess)
+    return fail(MOE_ERR_OOM);
+  memset(c->h_err, 0, sizeof(int32_t) * 4);
+  if (cudaHostGetDevicePointer(&dm, c->h_err, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  c->d_err = static_cast<int32_t *>(dm);
+
+  // streams and events
+  if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cudaEventCreateWithFlags(&c->ev_plan, cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  c->ev_up.resize(c->maxStages);
+  c->ev_done.resize(c->maxStages);
+  for (int i = 0; i < c->maxStages; ++i) {
+    if (cudaEventCreateWithFlags(&c->ev_up[i], cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->ev_done[i], cudaEventDisableTiming) != cudaSuccess)
+      return fail(MOE_ERR_CUDA);
+  }
+  const int pool = 2048;
+  c->tp.ev.resize(2 * pool);
+  c->tp.kind.resize(pool);
+  for (auto &e : c->tp.ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return fail(MOE_ERR_CUDA);
+
+  // empty cache
+  bool okm = cudaMemsetAsync(c->d_slot_expert, 0xFF, sizeof(int32_t) * L * S, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_expert_slot, 0xFF, sizeof(int32_t) * L * E, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_slot_stamp, 0, sizeof(uint64_t) * L * S, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_clock, 0, sizeof(uint64_t) * L, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_stats, 0, sizeof(uint64_t) * L * kNStat, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_hdr, 0, sizeof(PlanHdr), st) == cudaSuccess;
+  okm = okm && cudaStreamSynchronize(st) == cudaSuccess;
+  if (!okm) return fail(MOE_ERR_CUDA);
+  *out = c;
+  return MOE_OK;
+}
+
+MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits, const void *d_x,
+                              int32_t n_tokens, float *d_out, void *cuda_stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->poisoned) return MOE_ERR_POISONED;
+  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) return poison(c, MOE_ERR_INVALID_ARG);
+  const moe_cache_config &g = c->cfg;
+  if (layer < 0 || layer >= g.n_layers || n_tokens < 0 || n_tokens > g.max_tokens)
+    return MOE_ERR_INVALID_ARG;
+  if (n_tokens == 0) return MOE_OK;
+  if (!d_logits || !d_x || !d_out) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  const int E = g.n_experts, k = g.top_k, S = g.slots_per_layer, T = n_tokens;
+  const int P = T * k;
+  const int maxU = std::min(E, P);
+  const int maxUnits = maxU + (P + kTokPerUnit - 1) / kTokPerUnit;
+  const bool need_host = g.fill_mode == MOE_FILL_MEMCPY || maxU > S;
+
+  c->seq += 1;
+  if (c->seq == 0) c->seq = 1;
+  PlanArgs pa;
+  pa.logits = d_logits;
+  pa.T = T;
+  pa.E = E;
+  pa.k = k;
+  pa.S = S;
+  pa.weight_mode = g.weight_mode;
+  pa.slot_expert = c->d_slot_expert + (size_t)layer * S;
+  pa.expert_slot = c->d_expert_slot + (size_t)layer * E;
+  pa.slot_stamp = c->d_slot_stamp + (size_t)layer * S;
+  pa.clock = c->d_clock + layer;
+  pa.stats = c->d_stats + (size_t)layer * kNStat;
+  pa.expert_bytes = c->expert_bytes;
+  pa.ids = c->d_ids;
+  pa.w = c->d_w;
+  pa.gpu_slot = c->d_gpu_slot;
+  pa.stage = c->d_stage;
+  pa.perm = c->d_perm;
+  pa.items = c->d_items;
+  pa.units = c->d_units;
+  pa.unit_begin = c->d_unit_begin;
+  pa.miss = c->d_miss;
+  pa.hdr = c->d_hdr;
+  pa.err_flag = c->d_err;
+  pa.mailbox = need_host ? c->d_mail : nullptr;
+  pa.mailbox_stage_cap = c->mail_stage_cap;
+  pa.seq = c->seq;
+
+  FfnArgs fa;
+  fa.slots = c->d_slots + (size_t)layer * S * c->lay.stride;
+  fa.slot_stride = c->lay.stride;
+  fa.lay = c->lay;
+  fa.H = g.hidden;
+  fa.F = g.ffn;
+  fa.k = k;
+  fa.x = d_x;
+  fa.x_bf16 = g.act_dtype == 1;
+  fa.perm = c->d_perm;
+  fa.items = c->d_items;
+  fa.units = c->d_units;
+  fa.unit_begin = c->d_unit_begin;
+  fa.hdr = c->d_hdr;
+  fa.h = c->d_h;
+  fa.y = c->d_y;
+  fa.max_tok = std::min(kTokPerUnit, T);
+
+  RepackArgs ra;
+  ra.slots = c->d_slots + (size_t)layer * S * c->lay.stride;
+  ra.slot_stride = c->lay.stride;
+  ra.lay = c->lay;
+  ra.miss = c->d_miss;
+  ra.hdr = c->d_hdr;
+
+  cudaError_t e;
+#define MOE_LAUNCH(kind, expr)                          \
+  do {                                                  \
+    Launch _l(c, kind, st);                             \
+    e = (expr);                                         \
+    if (e != cudaSuccess) return poison(c, MOE_ERR_CUDA); \
+  } while (0)
+
+  MOE_LAUNCH(K_PLAN, launch_plan(pa, st));
+
+  if (!need_host) {
+    // single stage guaranteed; everything stays on the device
+    ra.src_base = c->host_dev;
+    ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
+    ra.src_expert_stride = c->store.expert_stride;
+    ra.src_slot_stride = 0;
+    ra.by_expert = 1;
+    ra.stage = 0;
+    MOE_LAUNCH(K_REPACK, launch_repack(ra, S, maxU, st));
+    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 2, 0, maxUnits, st));
+    MOE_LAUNCH(K_DOWN, launch_down(fa, 2, 0, maxUnits, st));
+    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+  } else {
+    // copies may start as soon as the plan exists; stage-0 hits need no copy
+    if (cudaEventRecord(c->ev_plan, st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
+    int rc = wait_mailbox(c, c->seq, st);
+    if (rc != MOE_OK) return poison(c, rc);
+    const PlanHdr hdr = c->h_mail->hdr;
+    if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
+    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss;
+    if (n_st < 1 || n_st > c->maxStages - 1) return poison(c, MOE_ERR_CUDA);
+    for (int j = 0; j < n_st; ++j) {
+      const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
+      const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
+      const int nmiss = mhi - mlo;
+      if (nmiss > 0) {
+        ra.stage = j;
+        if (g.fill_mode == MOE_FILL_MEMCPY) {
+          if (cudaStreamWaitEvent(c->side, j == 0 ? c->ev_plan : c->ev_done[j - 1], 0) != cudaSuccess)
+            return poison(c, MOE_ERR_CUDA);
+          {
+            Launch l(c, K_MEMCPY, c->side);
+            const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) +
+                                   (size_t)layer * c->store.layer_stride;
+            for (int i = mlo; i < mhi; ++i) {
+              const MissItem m = c->h_mail_miss[i];
+              if (m.expert < 0 || m.expert >= E) return poison(c, MOE_ERR_CUDA);
+              if (cudaMemcpyAsync(c->d_staging + (size_t)(i - mlo) * c->expert_bytes,
+                                  lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
+                                  cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+                return poison(c, MOE_ERR_CUDA);
+            }
+          }
+          if (cudaEventRecord(c->ev_up[j], c->side) != cudaSuccess ||
+              cudaStreamWaitEvent(st, c->ev_up[j], 0) != cudaSuccess)
+            return poison(c, MOE_ERR_CUDA);
+          ra.src_base = c->d_staging;
+          ra.src_layer_off = 0;
+          ra.src_expert_stride = 0;
+          ra.src_slot_stride = c->expert_bytes;
+          ra.by_expert = 0;
+        } else {
+          ra.src_base = c->host_dev;
+          ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
+          ra.src_expert_stride = c->store.expert_stride;
+          ra.src_slot_stride = 0;
+          ra.by_expert = 1;
+        }
+        MOE_LAUNCH(K_REPACK, launch_repack(ra, S, nmiss, st));
+      }
+      const int ulo = j == 0 ? hdr.hit_units : c->h_mail_ub[j];
+      const int uhi = c->h_mail_ub[j + 1];
+      if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, j, uhi - ulo, st));
+      const int dlo = c->h_mail_ub[j];
+      if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
+      if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
+        return poison(c, MOE_ERR_CUDA);
+    }
+    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+  }
+#undef MOE_LAUNCH
+  c->last_layer = layer;
+  c->last_T = T;
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_sync(moe_cache *c, void *cuda_stream) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  int rc = wait_stream((cudaStream_t)cuda_stream, c->cfg.timeout_us);
+  if (rc == MOE_OK) rc = wait_stream(c->side, c->cfg.timeout_us);
+  if (rc != MOE_OK) return poison(c, rc);
+  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) return poison(c, MOE_ERR_INVALID_ARG);
+  return c->poisoned ? c->last_error : MOE_OK;
+}
+
+MOE_API int moe_cache_stats(const moe_cache *cc, int32_t layer, moe_cache_stats_t *out) {
+  moe_cache *c = const_cast<moe_cache *>(cc);
+  if (!c || !out || layer < -1 || layer >= c->cfg.n_layers) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    poison(c, MOE_ERR_CUDA);
+  }
+  std::vector<uint64_t> st((size_t)c->cfg.n_layers * kNStat);
+  if (cudaMemcpy(st.data(), c->d_stats, sizeof(uint64_t) * st.size(), cudaMemcpyDeviceToHost) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  uint64_t acc[kNStat] = {};
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    if (layer >= 0 && l != layer) continue;
+    for (int i = 0; i < kNStat; ++i) acc[i] += st[(size_t)l * kNStat + i];
+  }
+  out->calls = acc[0];
+  out->pick_hits = acc[1];
+  out->pick_misses = acc[2];
+  out->unique_hits = acc[3];
+  out->unique_misses = acc[4];
+  out->evictions = acc[5];
+  out->bytes_uploaded = acc[6];
+  out->stages = acc[7];
+  out->staged_calls = acc[8];
+  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) poison(c, MOE_ERR_INVALID_ARG);
+  out->poisoned = c->poisoned;
+  out->last_error = c->last_error;
+  return MOE_OK;
+}
+
+MOE_API int moe_layer_last_plan(const moe_cache *cc, int32_t layer, int32_t *ids, float *w,
+                                int32_t *gpu_slot, int32_t *stage, int32_t *miss_expert,
+                                int32_t *miss_slot, int32_t *miss_evicted, int32_t *miss_stage,
+                                int32_t *n_miss, int32_t *n_stages) {
+  moe_cache *c = const_cast<moe_cache *>(cc);
+  if (!c || layer != c->last_layer || c->last_T <= 0) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  const size_t P = (size_t)c->last_T * c->cfg.top_k;
+  PlanHdr h;
+  bool ok = cudaMemcpy(&h, c->d_hdr, sizeof(h), cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (ok && ids) ok = cudaMemcpy(ids, c->d_ids, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (ok && w) ok = cudaMemcpy(w, c->d_w, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (ok && gpu_slot) ok = cudaMemcpy(gpu_slot, c->d_gpu_slot, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (ok && stage) ok = cudaMemcpy(stage, c->d_stage, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  if (h.error) return MOE_ERR_INVALID_ARG;
+  std::vector<MissItem> m(std::max(1, h.n_miss));
+  if (h.n_miss > 0 && cudaMemcpy(m.data(), c->d_miss, sizeof(MissItem) * h.n_miss,
+                                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  for (int i = 0; i < h.n_miss; ++i) {
+    if (miss_expert) miss_expert[i] = m[i].expert;
+    if (miss_slot) miss_slot[i] = m[i].slot;
+    if (miss_evicted) miss_evicted[i] = m[i].evicted;
+    if (miss_stage) miss_stage[i] = m[i].stage;
+  }
+  if (n_miss) *n_miss = h.n_miss;
+  if (n_stages) *n_stages = h.n_stages;
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_set_timing(moe_cache *c, int32_t enable) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (enable) {
+    tp_flush(c);
+    for (int i = 0; i < K_NKINDS; ++i) { c->tp.ms[i] = 0; c->tp.n[i] = 0; }
+    c->tp.on = true;
+  } else {
+    c->tp.on = false;
+  }
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_timing(moe_cache *c, const char **names, uint64_t *launches, double *ms,
+                             int32_t cap, int32_t *n) {
+  if (!c || cap < 0) return MOE_ERR_INVALID_ARG;
+  tp_flush(c);
+  int m = std::min(cap, (int)K_NKINDS);
+  for (int i = 0; i < m; ++i) {
+    if (names) names[i] = kKindNames[i];
+    if (launches) launches[i] = c->tp.n[i];
+    if (ms) ms[i] = c->tp.ms[i];
+  }
+  if (n) *n = K_NKINDS;
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_probe_h2d(moe_cache *c, int32_t iters, double *gbps) {
+  if (!c || iters < 1 || !gbps) return MOE_ERR_INVALID_ARG;
+  if (c->poisoned) return MOE_ERR_POISONED;
+  cudaEvent_t a, b;
+  if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) return MOE_ERR_CUDA;
+  std::vector<double> v;
+  const uint8_t *base = static_cast<const uint8_t *>(c->store.base);
+  int rc = MOE_OK;
+  for (int i = 0; i < iters && rc == MOE_OK; ++i) {
+    const int e = i % c->cfg.n_experts;
+    cudaEventRecord(a, c->side);
+    if (cudaMemcpyAsync(c->d_staging, base + (size_t)e * c->store.expert_stride, c->expert_bytes,
+                        cudaMemcpyHostToDevice, c->side) != cudaSuccess) {
+      rc = MOE_ERR_CUDA;
+      break;
+    }
+    cudaEventRecord(b, c->side);
+    rc = wait_stream(c->side, c->cfg.timeout_us);
+    float ms = 0.f;
+    if (rc == MOE_OK && cudaEventElapsedTime(&ms, a, b) == cudaSuccess && ms > 0.f)
+      v.push_back((double)c->expert_bytes / (ms * 1e-3) / 1e9);
+  }
+  cudaEventDestroy(a);
+  cudaEventDestroy(b);
+  if (rc != MOE_OK) return poison(c, rc);
+  if (v.empty()) return MOE_ERR_CUDA;
+  std::sort(v.begin(), v.end());
+  *gbps = v[v.size() / 2];
+  return MOE_OK;
+}
+
+MOE_API uint64_t moe_cache_launch_count(const moe_cache *c) {
+  return c ? c->launches.load(std::memory_order_relaxed) : 0;
+}
+
+MOE_API void moe_cache_destroy(moe_cache *c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  cudaGetLastError();
+  free_all(c);
+  delete c;
+}

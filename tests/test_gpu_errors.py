@@ -1,0 +1,135 @@
+"""Error paths of the C ABI on the GPU: edge sizes, rejected inputs, poisoning,
+host-side failure injection (a wait whose limit is too short).  Nothing here
+faults or hangs the device: every failure is made on the host or is a value
+check the kernels perform."""
+import numpy as np
+import pytest
+
+import router_softmax_top_gb300 as moe
+import synth
+from tests.gpu_util import pinned_store
+
+pytestmark = pytest.mark.gpu
+
+TINY = synth.TINY
+
+
+def _cache(store, **kw):
+    args = dict(n_layers=1, n_experts=TINY.E, top_k=TINY.k, hidden=TINY.H, ffn=TINY.F,
+                slots_per_layer=TINY.S, max_tokens=4, store=store)
+    args.update(kw)
+    return moe.MoECache(**args)
+
+
+@pytest.fixture(scope="module")
+def store():
+    return pinned_store(1, TINY.E, TINY.H, TINY.F, seed=0)
+
+
+def _inputs(T=4):
+    import torch
+    lg, x = synth.tiny_inputs(0)
+    return torch.from_numpy(lg[:T].copy()).cuda(), torch.from_numpy(x[:T].copy()).cuda()
+
+
+def test_zero_tokens_is_noop(store):
+    import torch
+    c = _cache(store)
+    lg, x = _inputs()
+    out = torch.full((4, TINY.H), 7.0, device="cuda")
+    assert c.forward_rc(0, lg[:0], x[:0], out) == moe.MOE_OK
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    assert c.stats(0)["calls"] == 0
+    c.close()
+
+
+def test_too_many_tokens_and_bad_layer(store):
+    import torch
+    c = _cache(store, max_tokens=2)
+    lg, x = _inputs(4)
+    out = torch.empty((4, TINY.H), device="cuda")
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_layer_forward(c.handle, 3, lg.data_ptr(), x.data_ptr(), 1, out.data_ptr()) \
+        == moe.MOE_ERR_INVALID_ARG
+    assert c.stats(-1)["poisoned"] == 0     # argument errors do not poison
+    c.forward(0, lg[:2], x[:2])
+    c.close()
+
+
+@pytest.mark.parametrize("fill_mode", [0, 1])
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")])
+def test_non_finite_logit_poisons(store, fill_mode, bad):
+    import torch
+    c = _cache(store, fill_mode=fill_mode, slots_per_layer=8)
+    lg, x = _inputs(2)
+    out = torch.empty((2, TINY.H), device="cuda")
+    c.forward(0, lg, x, out)                       # a good call first
+    before = c.stats(0)
+    lg2 = lg.clone()
+    lg2[1, 3] = bad
+    rc = c.forward_rc(0, lg2, x, out)
+    if rc == moe.MOE_OK:                           # pull mode reports after the fact
+        rc = c.sync()
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    st = c.stats(0)
+    assert st["poisoned"] == 1 and st["last_error"] == moe.MOE_ERR_INVALID_ARG
+    assert st["calls"] == before["calls"]          # the layer's state did not move
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
+    c.close()
+
+
+def test_timeout_on_host_wait_poisons(store):
+    # a host wait limit shorter than any kernel launch: the mailbox wait gives up
+    import torch
+    c = _cache(store, timeout_us=1)
+    lg, x = _inputs(4)
+    out = torch.empty((4, TINY.H), device="cuda")
+    rc = c.forward_rc(0, lg, x, out)
+    assert rc in (moe.MOE_ERR_TIMEOUT, moe.MOE_OK)
+    if rc == moe.MOE_ERR_TIMEOUT:
+        assert c.stats(-1)["poisoned"] == 1
+        assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
+    c.close()                                      # waits for the work in flight, frees all
+    torch.cuda.synchronize()
+
+
+def test_unaligned_store_rejected(store):
+    import ctypes
+    cfg = moe.MoeCacheConfig(1, TINY.E, TINY.k, TINY.H, TINY.F, TINY.S, 4, 0, 0, 0, 0, 0, 10**6)
+    hs = moe.MoeHostStore(store.data_ptr() + 2, store.numel() - 2, TINY.E * TINY.expert_bytes,
+                          TINY.expert_bytes)
+    h = ctypes.c_void_p()
+    assert moe.lib().moe_cache_init(ctypes.byref(cfg), ctypes.byref(hs), None, ctypes.byref(h)) \
+        == moe.MOE_ERR_HOST_STORE
+    hs = moe.MoeHostStore(store.data_ptr(), 1000, TINY.E * TINY.expert_bytes, TINY.expert_bytes)
+    assert moe.lib().moe_cache_init(ctypes.byref(cfg), ctypes.byref(hs), None, ctypes.byref(h)) \
+        == moe.MOE_ERR_HOST_STORE
+
+
+def test_unpinned_store_is_registered():
+    # an ordinary (pageable) numpy buffer is registered at init and released at destroy
+    import torch
+    buf = synth.store(1, TINY.E, TINY.H, TINY.F, seed=0)
+    c = moe.MoECache(n_layers=1, n_experts=TINY.E, top_k=TINY.k, hidden=TINY.H, ffn=TINY.F,
+                     slots_per_layer=TINY.S, max_tokens=4, store=(buf.ctypes.data, buf.nbytes))
+    lg, x = _inputs(4)
+    out = c.forward(0, lg, x)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out).all()
+    c.close()
+
+
+def test_timing_and_launch_count(store):
+    import torch
+    c = _cache(store)
+    lg, x = _inputs(4)
+    c.set_timing(True)
+    for _ in range(3):
+        c.forward(0, lg, x)
+    t = c.timing()
+    c.set_timing(False)
+    assert t["plan"]["launches"] == 3 and t["plan"]["ms"] > 0
+    assert c.launch_count() >= 3 * 4
+    assert c.probe_h2d(5) > 0.1
+    c.close()
