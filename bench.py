@@ -1,0 +1,384 @@
+"""Benchmark of the routed-MoE expert-slot cache on one GB300 (or N replicas).
+
+Default workload (decode): 30 MoE layers, 128 experts/layer, top-8, hidden 2816,
+expert FFN 704, Q4_0 experts (3,345,408 B each) in pinned host RAM, 32 slots per
+layer, one token per step, Zipf(1.1) routing with 39% of a token's picks copied
+from the previous token, fp32 activations N(0,1).  One step = one token through
+all 30 layer calls (router, slot map, miss fill, FFN, combine).
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle on the
+host cores instead (a bounded sample of the same workload).
+N > 1 (torchrun): every rank runs its own replica on its own token stream
+(independent sequences; no data-path collective), value = all ranks' tokens / max
+time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s vs roofline; cache hit rate"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=448)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--fill", default="memcpy", choices=["memcpy", "pull"])
+    ap.add_argument("--workload", default="decode", choices=["decode"])
+    ap.add_argument("--cpu-sample-steps", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-kernel-pass", action="store_true")
+    ap.add_argument("--threads", type=int, default=0)
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_config(sh, fill):
+    return {
+        "workload": (f"decode: {sh.L} MoE layers, {sh.E} experts/layer, top-{sh.k}, hidden {sh.H}, "
+                     f"expert FFN {sh.F}, Q4_0 experts ({sh.expert_bytes} B) in pinned host RAM, "
+                     f"{sh.S} slots/layer, 1 token/step, Zipf({sh.zipf}) routing with "
+                     f"{int(sh.sticky * 100)}% of picks copied from the previous token, fp32 "
+                     f"activations N(0,1)"),
+        "layers": sh.L, "experts": sh.E, "top_k": sh.k, "hidden": sh.H, "ffn": sh.F,
+        "slots_per_layer": sh.S, "tokens_per_step": 1, "expert_bytes": sh.expert_bytes,
+        "host_store_bytes": sh.store_bytes, "fill_mode": fill,
+        "l2": "inputs larger than L2: each step streams ~0.8 GB of expert weights (> 129 MB L2)",
+    }
+
+
+# --------------------------------------------------------------- clocks
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.25)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------- oracle (baseline)
+def run_oracle_sample(sh, store_np, logits, x, n_steps, threads):
+    """Time the CPU oracle over the first n_steps steps (all layers, outputs computed)."""
+    import oracle
+    c = oracle.Cache(sh.L, sh.E, sh.k, sh.H, sh.F, sh.S, store_np, threads=threads)
+    t0 = time.perf_counter()
+    for s in range(n_steps):
+        for l in range(sh.L):
+            c.forward(l, logits[s, l], x[s, l], compute=True)
+    dt = time.perf_counter() - t0
+    return n_steps / dt, dt, (threads if threads > 0 else oracle.max_threads())
+
+
+def run_reference(args):
+    """The oracle as it stands on the host cores.  One step = one layer call of the
+    decode trace (layers visited in turn), tokens/s = 1 / (L x mean layer-call time)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    sh = synth.DECODE
+    t0 = time.time()
+    W, K = max(3, args.warmup), max(1, args.steps)
+    nsteps = (W + K + sh.L - 1) // sh.L + 1
+    store = synth.store(sh.L, sh.E, sh.H, sh.F, seed=0, threads=args.threads)
+    _, logits, x = synth.decode_inputs(sh, nsteps, batch=1, seed=0)
+    c = oracle.Cache(sh.L, sh.E, sh.k, sh.H, sh.F, sh.S, store, threads=args.threads)
+    cores = args.threads if args.threads > 0 else oracle.max_threads()
+    calls = [(s, l) for s in range(nsteps) for l in range(sh.L)]
+    for s, l in calls[:W]:                      # warm-up: slot maps only
+        c.forward(l, logits[s, l], x[s, l], compute=False)
+    setup = time.time() - t0
+    t1 = time.perf_counter()
+    for s, l in calls[W:W + K]:
+        c.forward(l, logits[s, l], x[s, l], compute=True)
+    dt = time.perf_counter() - t1
+    value = K / (dt * sh.L)                     # tokens/s: one token needs L layer calls
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": W, "ms_per_step": 1e3 * dt / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(sh, "oracle"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{K} single-layer decode calls (layers in turn), outputs "
+                                       f"computed; tokens/s = 1 / ({sh.L} x mean call time)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "setup_s": setup}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import router_softmax_top_gb300 as moe
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sh = synth.DECODE
+    W, K = args.warmup, args.steps
+    assert W >= 3 and K >= 1
+    t_setup = time.time()
+    nsteps = W + 3 * K
+    eb = sh.expert_bytes
+    store = torch.empty(sh.L * sh.E * eb, dtype=torch.uint8, pin_memory=True)
+    synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
+    picks, logits_h, x_h = synth.decode_inputs(sh, nsteps, batch=1, seed=rank)
+    logits_d = torch.from_numpy(logits_h).cuda()     # [steps, L, 1, E]
+    x_d = torch.from_numpy(x_h).cuda()               # [steps, L, 1, H]
+    out_d = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
+    fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
+    cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
+                         slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=fill,
+                         timeout_us=30_000_000)
+    setup_s = time.time() - t_setup
+    h2d_gbps = cache.probe_h2d(24)
+    L = moe.lib()
+    fwd = L.moe_layer_forward
+    handle = cache.handle
+    stream = torch.cuda.current_stream()
+    sh_ = ctypes.c_void_p(stream.cuda_stream)
+    lg_ptr = [[ctypes.c_void_p(logits_d[s, l].data_ptr()) for l in range(sh.L)] for s in range(nsteps)]
+    x_ptr = [[ctypes.c_void_p(x_d[s, l].data_ptr()) for l in range(sh.L)] for s in range(nsteps)]
+    o_ptr = [ctypes.c_void_p(out_d[l].data_ptr()) for l in range(sh.L)]
+
+    def run_steps(s0, s1):
+        for s in range(s0, s1):
+            lp, xp = lg_ptr[s], x_ptr[s]
+            for l in range(sh.L):
+                rc = fwd(handle, l, lp[l], xp[l], 1, o_ptr[l], sh_)
+                if rc != 0:
+                    raise moe.MoeError(rc, f"moe_layer_forward step {s} layer {l}")
+
+    # ---- cold start: the first W steps from an empty cache (also the warm-up)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    st0 = cache.stats(-1)
+    e0.record()
+    run_steps(0, W)
+    e1.record()
+    torch.cuda.synchronize()
+    cold_ms = e0.elapsed_time(e1)
+    st1 = cache.stats(-1)
+
+    # ---- timed region: K steps, inputs resident in HBM
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    n_launch0 = cache.launch_count()
+    e0.record()
+    run_steps(W, W + K)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    n_launch = cache.launch_count() - n_launch0
+    dev_ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    st2 = cache.stats(-1)
+
+    # ---- per-kernel pass: the next K steps again with CUDA events around every
+    # launch (on the stream each kernel runs on); kept out of the headline
+    kpass_ms = 0.0
+    if not args.no_kernel_pass:
+        cache.set_timing(True)
+        e0.record()
+        run_steps(W + K, W + 2 * K)
+        e1.record()
+        torch.cuda.synchronize()
+        kpass_ms = e0.elapsed_time(e1)
+    ktime = cache.timing()
+    cache.set_timing(False)
+    st3 = cache.stats(-1)
+
+    # ---- e2e: same metric through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        lg_pin = torch.from_numpy(logits_h).pin_memory()
+        x_pin = torch.from_numpy(x_h).pin_memory()
+        out_pin = torch.empty((K, sh.L, 1, sh.H), dtype=torch.float32, pin_memory=True)
+        lg_step = torch.empty((sh.L, 1, sh.E), dtype=torch.float32, device="cuda")
+        x_step = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
+        lg_sp = [ctypes.c_void_p(lg_step[l].data_ptr()) for l in range(sh.L)]
+        x_sp = [ctypes.c_void_p(x_step[l].data_ptr()) for l in range(sh.L)]
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i, s in enumerate(range(W + 2 * K, W + 3 * K)):
+            lg_step.copy_(lg_pin[s], non_blocking=True)
+            x_step.copy_(x_pin[s], non_blocking=True)
+            for l in range(sh.L):
+                rc = fwd(handle, l, lg_sp[l], x_sp[l], 1, o_ptr[l], sh_)
+                if rc != 0:
+                    raise moe.MoeError(rc, "moe_layer_forward (e2e)")
+            out_pin[i].copy_(out_d, non_blocking=True)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_s = time.perf_counter() - t0
+        e2e = {"value": K / e2e_s, "unit": UNIT,
+               "h2d_bytes_per_step": int(lg_step.numel() * 4 + x_step.numel() * 4),
+               "d2h_bytes_per_step": int(out_d.numel() * 4),
+               "ms_per_step": 1e3 * e2e_s / K}
+
+    # ---- aggregate over ranks
+    t_step = torch.tensor([dev_ms], dtype=torch.float64, device="cuda")
+    if world > 1:
+        dist.all_reduce(t_step, op=dist.ReduceOp.MAX)
+        if e2e is not None:
+            te = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+            e2e["value"] = world * 1e3 / float(te.item())
+    dev_ms_max = float(t_step.item())
+    value = world * K / (dev_ms_max * 1e-3)
+
+    # ---- roofline of the dominant kernel and of the whole step
+    hbm_peak, _, peak_kind = measured_peaks()
+    d = {key: st2[key] - st1[key] for key in st2 if key not in ("poisoned", "last_error")}
+    dk = {key: st3[key] - st2[key] for key in st3 if key not in ("poisoned", "last_error")}
+    uniq = d["unique_hits"] + d["unique_misses"]
+    uniq_k = dk["unique_hits"] + dk["unique_misses"]
+    picks_k = dk["pick_hits"] + dk["pick_misses"]
+    mat = sh.F * sh.H // 32 * 18                      # one Q4_0 matrix (gate, up or down)
+    kinds = {k2: v for k2, v in ktime.items() if v["launches"] > 0 and k2 != "h2d_memcpy"}
+    dom = max(kinds, key=lambda k2: kinds[k2]["ms"]) if kinds else "q4_gateup_gemv"
+    gu = ktime.get("q4_gateup_gemv", {"launches": 0, "ms": 0.0})
+    dn = ktime.get("q4_down_gemv", {"launches": 0, "ms": 0.0})
+    # algorithmic bytes: every distinct expert of a call read once; activations in, results out
+    gu_bytes = uniq_k * 2 * mat + picks_k * (sh.H * 4 + sh.F * 4)
+    dn_bytes = uniq_k * mat + picks_k * (sh.F * 4 + 4) + sh.H * 4 * picks_k // sh.k
+    kb = {"q4_gateup_gemv": (gu_bytes, gu), "q4_down_gemv": (dn_bytes, dn)}
+    rk = dom if dom in kb else "q4_gateup_gemv"
+    alg_bytes, kt = kb[rk]
+    achieved = alg_bytes / (kt["ms"] * 1e-3) / 1e9 if kt["ms"] > 0 else 0.0
+    roofline = {"kernel": rk, "bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_kind,
+                "launches": kt["launches"], "avg_launch_us": 1e3 * kt["ms"] / max(1, kt["launches"]),
+                "alg_bytes_per_launch": alg_bytes / max(1, kt["launches"])}
+    t_roof = (d["unique_hits"] * sh.expert_bytes / (hbm_peak * 1e9) +
+              d["unique_misses"] * sh.expert_bytes / (h2d_gbps * 1e9))
+    t_roof_strict = t_roof + d["unique_misses"] * sh.expert_bytes / (hbm_peak * 1e9)
+    step_roof = {"bound": "hbm+h2d", "t_roof_ms": 1e3 * t_roof, "t_meas_ms": dev_ms,
+                 "frac": t_roof / (dev_ms * 1e-3), "frac_strict": t_roof_strict / (dev_ms * 1e-3),
+                 "hbm_gbs": hbm_peak, "h2d_gbs_measured": h2d_gbps,
+                 "hit_bytes": d["unique_hits"] * sh.expert_bytes,
+                 "miss_bytes": d["unique_misses"] * sh.expert_bytes}
+    picks_t = d["pick_hits"] + d["pick_misses"]
+    cold = {k2: st1[k2] - st0[k2] for k2 in ("pick_hits", "pick_misses", "unique_hits", "unique_misses")}
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(sh, args.fill),
+        "hit_rate": {"pick": d["pick_hits"] / max(1, picks_t),
+                     "unique": d["unique_hits"] / max(1, uniq)},
+        "cold_start": {"steps": W, "tokens_per_s": W / (cold_ms * 1e-3),
+                       "pick_hit_rate": cold["pick_hits"] / max(1, cold["pick_hits"] + cold["pick_misses"])},
+        "achieved_hbm_gbs_step": (d["unique_hits"] + d["unique_misses"]) * sh.expert_bytes / (dev_ms * 1e-3) / 1e9,
+        "roofline": roofline,
+        "step_roofline": step_roof,
+        "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 4)} for k2, v in ktime.items()
+                    if v["launches"]},
+        "kernel_pass_ms_per_step": kpass_ms / K,
+        "gpu_launches": int(n_launch),
+        "clocks": clk,
+        "e2e": e2e,
+        "setup_s": setup_s,
+    }
+    # ---- CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = max(1, args.cpu_sample_steps)
+        v, dt, cores = run_oracle_sample(sh, store.numpy(), logits_h, x_h, n, args.threads)
+        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": f"first {n} decode steps (one token through all {sh.L} "
+                                            f"layers, outputs computed) from a cold cache; {dt:.1f} s"}
+    cache.close()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -76,8 +76,8 @@ typedef struct {
     int32_t n_layers;        /* L >= 1                                             */
     int32_t n_experts;       /* E, 1..1024                                         */
     int32_t top_k;           /* k, 1..min(E, 32)                                   */
-    int32_t hidden;          /* H, multiple of 256                                 */
-    int32_t ffn;             /* F, multiple of 32 with F*H a multiple of 256       */
+    int32_t hidden;          /* H, multiple of 64, <= 16384                        */
+    int32_t ffn;             /* F, multiple of 64, <= 16384                        */
     int32_t slots_per_layer; /* S, 1..E: the per-layer budget of device slots      */
     int32_t max_tokens;      /* largest n_tokens of any call, >= 1                 */
     int32_t weight_mode;     /* 0: softmax over all E (default); 1: over chosen k  */
@@ -108,6 +108,8 @@ typedef struct {
     uint64_t staged_calls;   /* calls that needed more than one stage              */
     int32_t poisoned;        /* 1 once a call on the handle has failed             */
     int32_t last_error;      /* the code that poisoned it (or MOE_OK)              */
+    int32_t cuda_error;      /* the cudaError_t behind MOE_ERR_CUDA (0 if none)     */
+    int32_t reserved;
 } moe_cache_stats_t;
 
 /*

@@ -55,7 +55,8 @@ class MoeCacheStats(ctypes.Structure):
                 ("unique_misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64),
                 ("bytes_uploaded", ctypes.c_uint64), ("stages", ctypes.c_uint64),
                 ("staged_calls", ctypes.c_uint64), ("poisoned", ctypes.c_int32),
-                ("last_error", ctypes.c_int32)]
+                ("last_error", ctypes.c_int32), ("cuda_error", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}

@@ -12,7 +12,7 @@ namespace moe {
 // ---------------------------------------------------------------- limits
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
 constexpr int kNStat = 9;  // calls, pick_hits, pick_misses, unique_hits, unique_misses,
                            // evictions, bytes_uploaded, stages, staged_calls
 constexpr int kTokPerUnit = 8;  // tokens of one expert handled by one GEMV work unit
@@ -73,9 +73,17 @@ struct Mailbox {
 
 // ------------------------------------------------ repacked slot layout
 // Each matrix of R rows x C columns (nb = C/32 blocks per row) is stored as a
-// nibble plane [nb][R][16 bytes] followed by a scale plane [nb][R] fp16.
-// Block (r, b) of the canonical layout becomes nib[(b*R + r)*16 ..] and
-// scale[b*R + r]; the 16 nibble bytes keep their canonical order.
+// nibble plane followed by a scale plane, both ordered by 32-row tiles:
+//   nibbles: [R/32 tiles][nb blocks][32 rows][16 bytes]
+//   scales:  [R/32 tiles][nb blocks][32 rows] fp16
+// so one tile of 32 rows is two contiguous regions (nb*512 and nb*64 bytes)
+// that a single bulk copy each brings into shared memory, and the 32 rows of
+// one block are 512 consecutive bytes (one 16-byte load per lane).  The 16
+// nibble bytes of a block keep their canonical order.
+__host__ __device__ inline uint64_t tile_elem(int r, int b, int nb) {
+  return ((uint64_t)(r >> 5) * nb + b) * 32 + (r & 31);
+}
+
 struct MatLayout {
   uint64_t nib_off, sc_off;  // byte offsets inside the slot
   int32_t rows, nb;
@@ -97,6 +105,18 @@ inline SlotLayout make_slot_layout(int H, int F) {
   s.bytes = 2 * mg * 18 + md * 18;
   s.stride = (s.bytes + 255) / 256 * 256;
   return s;
+}
+
+// Raise a kernel's dynamic shared memory limit to `bytes` when needed (the
+// limit plus the kernel's static shared memory must stay within the opt-in
+// maximum, so it is raised to what a launch needs, not to the maximum).
+template <typename Kern>
+inline cudaError_t ensure_dyn_smem(Kern kernel, size_t bytes, size_t &current) {
+  if (bytes <= 48 * 1024 || bytes <= current) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) current = bytes;
+  return e;
 }
 
 // ------------------------------------------------------------ launchers
@@ -145,6 +165,7 @@ struct FfnArgs {
   float *h;  // [T*k, F]
   float *y;  // [T*k, H]
   int max_tok;  // largest pair count of one work unit this call can have (<= kTokPerUnit)
+  int32_t *err;  // mapped error word: set on a device-side failure
 };
 
 // Units [unit_lo, unit_hi) are read from unit_begin on the device:
@@ -156,6 +177,11 @@ cudaError_t launch_down(const FfnArgs &a, int range_kind, int stage, int max_uni
                         cudaStream_t st);
 cudaError_t launch_combine(const float *y, const float *w, const PlanHdr *hdr, int T, int k,
                            int H, float *out, cudaStream_t st);
+// Down projection of all picks of each token plus the weighted sum, for calls
+// that run in one stage (out[T, H] written directly).
+cudaError_t launch_down_combine(const FfnArgs &a, const float *w, const int32_t *gpu_slot, int T,
+                                float *out, cudaStream_t st);
+bool down_combine_supported(int F, int k);
 
 struct RepackArgs {
   const uint8_t *src_base;  // canonical source: staging (device) or mapped host store

@@ -1,25 +1,88 @@
 // Expert FFN kernels of the GEMV (decode / small-batch) path and the slot fill.
 //
-//  * repack_kernel: one missed canonical Q4_0 expert block (from the staging
-//    area or straight from the mapped host store) -> repacked slot planes.
-//  * q4_gemv_kernel<2>: gate and up rows of one expert for up to 8 of its
-//    tokens, then h = silu(g) * u ("llama.cpp + MoE expert cache",
-//    "Limitations": merged gate/up, SiLU).
-//  * q4_gemv_kernel<1>: down rows, y = W_down h per pair.
-//  * combine_kernel: out_t = sum over picks in ascending order of w * y
-//    ("The idea: cache the hot experts on the GPU", step 4).
+//  * fill_kernel: missed canonical Q4_0 expert blocks (from the staging area or
+//    straight from the mapped host store) -> repacked slot planes.  A bounded
+//    grid loops over (miss, 32-row tile) pairs with cp.async double buffering,
+//    so many host reads are in flight while SMs stay free for the hit compute.
+//  * q4_tile_gemv_kernel<2>: gate and up rows (one 32-row tile) of one expert
+//    for up to 8 of its tokens, then h = silu(g) * u ("llama.cpp + MoE expert
+//    cache", "Limitations": merged gate/up, SiLU).
+//  * q4_tile_gemv_kernel<1>: down rows, y = W_down h per pair (staged calls).
+//  * down_combine_kernel: down rows of all k picks of one token and the
+//    weighted sum over picks in ascending order ("The idea: cache the hot
+//    experts on the GPU", step 4), for single-stage calls.
+//  * combine_kernel: the weighted sum from stored y (staged calls).
 //
-// Each output of a pair is computed by the same code in the same order
-// whatever the slot, the stage or the other tokens of its work unit, so the
-// result does not depend on the slot budget.
+// Weight tiles reach shared memory by bulk copies (cp.async.bulk, completion on
+// an mbarrier): a 32-row tile of one matrix is two contiguous regions in the
+// slot.  Compute reads them back lane-per-row (conflict-free 16-byte loads).
+//
+// Budget invariance: every output of a pair is reduced in one canonical order
+// whatever kernel, slot, stage or work unit computes it: warp w of 8 sums the
+// 32-blocks b = w, w+8, w+16, ... in ascending order, the 8 partial sums are
+// added in warp order, and the weighted sum runs over picks in ascending order.
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kGemvThreads = 256;
-constexpr int kGemvWarps = kGemvThreads / 32;
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kFillCtas = 48;
+constexpr uint32_t kSpinLimit = 1u << 26;  // bounded mbarrier waits
 
+// ------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for phase `parity` of bar; gives up after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Records a device-side failure (a bulk copy that never completed) in the
+// handle's mapped error word.
+__device__ __forceinline__ void flag_error(int32_t *err, int code) {
+  if (err) atomicExch(err, code);
+}
+
+// ----------------------------------------------------------- Q4_0 math
 // Four nibbles, one per byte of v (values 0..15), as floats 0.5 + q/256: the
 // byte lands in bits 16..19 under exponent 126, so no conversion instruction is
 // needed.  sum (0.5 + q/256) x = X/2 + (sum q x)/256, hence
@@ -42,6 +105,7 @@ __device__ __forceinline__ void decode_block(const uint4 q, float f[32]) {
   }
 }
 
+// s = sum_j f_j x_j over one block (x from shared memory, broadcast reads).
 __device__ __forceinline__ float dot32(const float f[32], const float *xb) {
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -60,37 +124,42 @@ __device__ __forceinline__ float dot32(const float f[32], const float *xb) {
   return s0 + s1;
 }
 
-__device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
+// acc + d * (sum (q - 8) x) for one block.
+__device__ __forceinline__ float block_term(const float f[32], float d, const float *xb,
+                                            float xsum, float acc) {
+  return fmaf(d, fmaf(256.f, dot32(f, xb), -136.f * xsum), acc);
 }
 
-__device__ __forceinline__ unsigned short ld_stream_u16(const void *p) {
-  unsigned short r;
-  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(r) : "l"(p));
-  return r;
+__device__ __forceinline__ float half_bits(unsigned short v) {
+  return __half2float(__ushort_as_half(v));
 }
 
-struct GemvJob {
-  const uint8_t *slots;
-  uint64_t slot_stride;
-  MatLayout m0, m1;  // m1 used when two matrices share the input (gate, up)
-  int R, nb;         // rows and 32-blocks per row
-  const void *x;     // rows of K = 32 nb values
-  int x_bf16;
-  int x_div;         // input row of pair p is p / x_div
-  const int32_t *perm;
-  const WorkItem *items;
-  const WorkUnit *units;
-  const int32_t *unit_begin;
-  const PlanHdr *hdr;
-  int range_kind, stage;
-  float *out;        // out[pair * R + r]
-  int max_tok;       // tokens per unit the shared memory was sized for
-};
+// Stage n input rows of K values (fp32 or bf16) into shared memory and the
+// per-block sums X_b (one warp per block: lane j holds value j, fixed xor tree).
+__device__ __forceinline__ void stage_rows(float *xs, float *xsum, const void *x, int x_bf16,
+                                           const int *rows, int n, int K) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nb = K / 32;
+  for (int t = 0; t < n; ++t) {
+    const int row = rows[t];
+    if (x_bf16) {
+      const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(x) + (size_t)row * K;
+      for (int c = tid; c < K; c += kThreads) xs[t * K + c] = __bfloat162float(src[c]);
+    } else {
+      const float4 *src =
+          reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)row * K);
+      float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * K);
+      for (int c = tid; c < K / 4; c += kThreads) dst[c] = src[c];
+    }
+  }
+  __syncthreads();
+  for (int i = warp; i < n * nb; i += kWarps) {
+    float v = xs[(size_t)i * 32 + lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) xsum[i] = v;
+  }
+  __syncthreads();
+}
 
 __device__ __forceinline__ bool unit_range(const PlanHdr *h, const int32_t *ub, int kind, int stage,
                                            int &lo, int &hi) {
@@ -101,139 +170,245 @@ __device__ __forceinline__ bool unit_range(const PlanHdr *h, const int32_t *ub, 
   return true;
 }
 
+// ------------------------------------------------------ tile GEMV (units)
+struct TileJob {
+  const uint8_t *slots;
+  uint64_t slot_stride;
+  MatLayout m0, m1;  // m1 used when two matrices share the input (gate, up)
+  int R, nb;         // rows and 32-blocks per row
+  const void *x;     // input rows of K = 32 nb values
+  int x_bf16;
+  int x_div;         // input row of pair p is p / x_div
+  const int32_t *perm;
+  const WorkItem *items;
+  const WorkUnit *units;
+  const int32_t *unit_begin;
+  const PlanHdr *hdr;
+  int range_kind, stage;
+  float *out;        // out[pair * R + r]
+  int G;             // tokens per shared-memory group of inputs (<= kTokPerUnit)
+  int32_t *err;
+};
+
+size_t tile_smem(int NMAT, int nb, int G) {
+  return 128 + (size_t)NMAT * nb * (512 + 64) + sizeof(float) * ((size_t)G * 32 * nb + (size_t)G * nb +
+                                                                  (size_t)kWarps * NMAT * G * 32);
+}
+
 template <int NMAT>
-__global__ void __launch_bounds__(kGemvThreads) q4_gemv_kernel(GemvJob j) {
+__global__ void __launch_bounds__(kThreads) q4_tile_gemv_kernel(TileJob j) {
   int lo, hi;
   if (!unit_range(j.hdr, j.unit_begin, j.range_kind, j.stage, lo, hi)) return;
   const int u = lo + (int)blockIdx.y;
   if (u >= hi) return;
   const WorkUnit wu = j.units[u];
   const WorkItem it = j.items[wu.item];
-  const int n = wu.pair_count;
-  const int K = 32 * j.nb, nb = j.nb, R = j.R;
+  const int n = wu.pair_count, G = j.G, nb = j.nb, K = 32 * nb;
+  const int tile = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  extern __shared__ __align__(16) float sm[];
-  float *xs = sm;                                  // [max_tok][K]
-  float *xsum = xs + (size_t)j.max_tok * K;        // [max_tok][nb]
-  float *red = xsum + (size_t)j.max_tok * nb;      // [warps][NMAT][max_tok][32]
+  extern __shared__ __align__(128) unsigned char sm[];
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm);
+  unsigned char *p = sm + 128;
+  uint4 *wn[2];
+  unsigned short *ws[2];
+#pragma unroll
+  for (int m = 0; m < NMAT; ++m) {
+    wn[m] = reinterpret_cast<uint4 *>(p);
+    p += (size_t)nb * 512;
+    ws[m] = reinterpret_cast<unsigned short *>(p);
+    p += (size_t)nb * 64;
+  }
+  float *xs = reinterpret_cast<float *>(p);
+  float *xsum = xs + (size_t)G * K;
+  float *red = xsum + (size_t)G * nb;  // [warps][NMAT][G][32]
+  __shared__ int rows[kTokPerUnit];
 
-  for (int t = 0; t < n; ++t) {
-    const int pair = j.perm[wu.pair_begin + t];
-    const int row = pair / j.x_div;
-    if (j.x_bf16) {
-      const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(j.x) + (size_t)row * K;
-      for (int c = tid; c < K; c += kGemvThreads) xs[t * K + c] = __bfloat162float(src[c]);
-    } else {
-      const float4 *src = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(j.x) +
-                                                           (size_t)row * K);
-      float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * K);
-      for (int c = tid; c < K / 4; c += kGemvThreads) dst[c] = src[c];
-    }
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  for (int i = tid; i < n * nb; i += kGemvThreads) {
-    const int t = i / nb, b = i - t * nb;
-    const float *xb = xs + (size_t)t * K + 32 * b;
-    float s = 0.f;
+  if (tid == 0) {
+    const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
+    const uint32_t bn = (uint32_t)nb * 512, bs = (uint32_t)nb * 64;
+    mbar_expect_tx(bar, NMAT * (bn + bs));
+    const MatLayout *mats[2] = {&j.m0, &j.m1};
 #pragma unroll
-    for (int q = 0; q < 32; ++q) s += xb[q];
-    xsum[t * nb + b] = s;
+    for (int m = 0; m < NMAT; ++m) {
+      bulk_g2s(wn[m], slot + mats[m]->nib_off + (uint64_t)tile * bn, bn, bar);
+      bulk_g2s(ws[m], slot + mats[m]->sc_off + (uint64_t)tile * bs, bs, bar);
+    }
   }
+  if (tid < n) rows[tid] = j.perm[wu.pair_begin + tid] / j.x_div;
   __syncthreads();
 
-  const int r = blockIdx.x * 32 + lane;
-  const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
-  const uint4 *nib0 = reinterpret_cast<const uint4 *>(slot + j.m0.nib_off);
-  const unsigned short *sc0 = reinterpret_cast<const unsigned short *>(slot + j.m0.sc_off);
-  const uint4 *nib1 = reinterpret_cast<const uint4 *>(slot + j.m1.nib_off);
-  const unsigned short *sc1 = reinterpret_cast<const unsigned short *>(slot + j.m1.sc_off);
-
-  const int bpw = (nb + kGemvWarps - 1) / kGemvWarps;
-  const int b0 = warp * bpw, b1 = min(nb, b0 + bpw);
-  float acc0[kTokPerUnit], acc1[kTokPerUnit];
-#pragma unroll
-  for (int t = 0; t < kTokPerUnit; ++t) { acc0[t] = 0.f; acc1[t] = 0.f; }
-
-  for (int b = b0; b < b1; ++b) {
-    const size_t e = (size_t)b * R + r;
-    const uint4 q0 = ld_stream(nib0 + e);
-    const float d0 = __half2float(__ushort_as_half(ld_stream_u16(sc0 + e)));
-    float f0[32];
-    decode_block(q0, f0);
-    float f1[32];
-    float d1 = 0.f;
-    if (NMAT == 2) {
-      const uint4 q1 = ld_stream(nib1 + e);
-      d1 = __half2float(__ushort_as_half(ld_stream_u16(sc1 + e)));
-      decode_block(q1, f1);
+  for (int g0 = 0; g0 < n; g0 += G) {
+    const int gn = min(G, n - g0);
+    stage_rows(xs, xsum, j.x, j.x_bf16, rows + g0, gn, K);
+    if (g0 == 0 && !mbar_wait(bar, 0)) {
+      flag_error(j.err, 2);
+      mbar_wait(bar, 0);
+      return;
     }
+    float acc0[kTokPerUnit], acc1[kTokPerUnit];
 #pragma unroll
-    for (int t = 0; t < kTokPerUnit; ++t) {
-      if (t < n) {
-        const float *xb = xs + (size_t)t * K + 32 * b;
-        const float cx = -136.f * xsum[t * nb + b];
-        const float s0 = dot32(f0, xb);
-        acc0[t] = fmaf(d0, fmaf(256.f, s0, cx), acc0[t]);
-        if (NMAT == 2) {
-          const float s1 = dot32(f1, xb);
-          acc1[t] = fmaf(d1, fmaf(256.f, s1, cx), acc1[t]);
+    for (int t = 0; t < kTokPerUnit; ++t) { acc0[t] = 0.f; acc1[t] = 0.f; }
+#pragma unroll 1
+    for (int b = warp; b < nb; b += kWarps) {
+      float f0[32], f1[32];
+      const float d0 = half_bits(ws[0][b * 32 + lane]);
+      decode_block(wn[0][b * 32 + lane], f0);
+      float d1 = 0.f;
+      if (NMAT == 2) {
+        d1 = half_bits(ws[1][b * 32 + lane]);
+        decode_block(wn[1][b * 32 + lane], f1);
+      }
+#pragma unroll
+      for (int t = 0; t < kTokPerUnit; ++t) {
+        if (t < gn) {
+          const float *xb = xs + (size_t)t * K + 32 * b;
+          const float xsb = xsum[t * nb + b];
+          acc0[t] = block_term(f0, d0, xb, xsb, acc0[t]);
+          if (NMAT == 2) acc1[t] = block_term(f1, d1, xb, xsb, acc1[t]);
         }
       }
     }
-  }
 #pragma unroll
-  for (int t = 0; t < kTokPerUnit; ++t) {
-    if (t < n) {
-      red[((warp * NMAT + 0) * j.max_tok + t) * 32 + lane] = acc0[t];
-      if (NMAT == 2) red[((warp * NMAT + 1) * j.max_tok + t) * 32 + lane] = acc1[t];
+    for (int t = 0; t < kTokPerUnit; ++t) {
+      if (t < gn) {
+        red[((warp * NMAT + 0) * G + t) * 32 + lane] = acc0[t];
+        if (NMAT == 2) red[((warp * NMAT + 1) * G + t) * 32 + lane] = acc1[t];
+      }
     }
-  }
-  __syncthreads();
-  // warp t finishes token t (fixed summation order over the K-split warps)
-  for (int t = warp; t < n; t += kGemvWarps) {
-    float g = 0.f, v = 0.f;
-    for (int w = 0; w < kGemvWarps; ++w) {
-      g += red[((w * NMAT + 0) * j.max_tok + t) * 32 + lane];
-      if (NMAT == 2) v += red[((w * NMAT + 1) * j.max_tok + t) * 32 + lane];
+    __syncthreads();
+    for (int t = warp; t < gn; t += kWarps) {
+      float g = 0.f, v = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        g += red[((w * NMAT + 0) * G + t) * 32 + lane];
+        if (NMAT == 2) v += red[((w * NMAT + 1) * G + t) * 32 + lane];
+      }
+      const int pair = j.perm[wu.pair_begin + g0 + t];
+      const float o = (NMAT == 2) ? g / (1.f + expf(-g)) * v : g;
+      j.out[(size_t)pair * j.R + tile * 32 + lane] = o;
     }
-    const int pair = j.perm[wu.pair_begin + t];
-    float o;
-    if (NMAT == 2) o = g / (1.f + expf(-g)) * v;
-    else o = g;
-    j.out[(size_t)pair * R + r] = o;
+    __syncthreads();
   }
-}
-
-size_t gemv_smem(int NMAT, int max_tok, int nb) {
-  return sizeof(float) * ((size_t)max_tok * 32 * nb + (size_t)max_tok * nb +
-                          (size_t)kGemvWarps * NMAT * max_tok * 32);
 }
 
 template <int NMAT>
-cudaError_t launch_gemv(GemvJob j, int max_units, cudaStream_t st) {
+cudaError_t launch_tile(TileJob j, int max_units, cudaStream_t st) {
   if (max_units <= 0) return cudaSuccess;
-  const size_t smem = gemv_smem(NMAT, j.max_tok, j.nb);
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(q4_gemv_kernel<NMAT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  if (j.R % 32) return cudaErrorInvalidValue;
+  const size_t budget = 200 * 1024;
+  int G = j.G;
+  while (G > 1 && tile_smem(NMAT, j.nb, G) > budget) --G;
+  j.G = G;
+  const size_t smem = tile_smem(NMAT, j.nb, G);
+  if (smem > budget) return cudaErrorInvalidValue;
+  static size_t cur = 0;
+  const cudaError_t e = ensure_dyn_smem(q4_tile_gemv_kernel<NMAT>, smem, cur);
+  if (e != cudaSuccess) return e;
   dim3 grid(j.R / 32, max_units);
-  q4_gemv_kernel<NMAT><<<grid, kGemvThreads, smem, st>>>(j);
+  q4_tile_gemv_kernel<NMAT><<<grid, kThreads, smem, st>>>(j);
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------- repack
-struct RepackJob {
-  RepackArgs a;
-  int S;
+// ------------------------------------------------------ down + combine
+struct DownCombineJob {
+  const uint8_t *slots;
+  uint64_t slot_stride;
+  MatLayout down;
+  int H, F, k;
+  const float *h;  // [T*k, F]
+  const float *w;  // [T*k]
+  const int32_t *gpu_slot;
+  const PlanHdr *hdr;
+  float *out;      // [T, H]
+  int NS;          // tile stages in shared memory
+  int32_t *err;
 };
 
-__global__ void __launch_bounds__(256) repack_kernel(RepackJob jb) {
+size_t dc_smem(int nb, int k, int NS) {
+  return 128 + (size_t)NS * nb * 576 + sizeof(float) * ((size_t)k * 32 * nb + (size_t)k * nb +
+                                                         (size_t)k * kWarps * 32);
+}
+
+__global__ void __launch_bounds__(kThreads) down_combine_kernel(DownCombineJob j) {
+  if (j.hdr->error) return;
+  const int t = blockIdx.y, tile = blockIdx.x, k = j.k, nb = j.F / 32, F = j.F, NS = j.NS;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t bn = (uint32_t)nb * 512, bs = (uint32_t)nb * 64;
+
+  extern __shared__ __align__(128) unsigned char sm[];
+  uint64_t *bar = reinterpret_cast<uint64_t *>(sm);  // [NS] (NS <= 8)
+  unsigned char *stages = sm + 128;
+  float *xs = reinterpret_cast<float *>(stages + (size_t)NS * nb * 576);
+  float *xsum = xs + (size_t)k * F;
+  float *red = xsum + (size_t)k * nb;  // [k][warps][32]
+  __shared__ int rows[kMaxTopK];
+
+  auto issue = [&](int q) {
+    const int s = q % NS;
+    unsigned char *dst = stages + (size_t)s * nb * 576;
+    const uint8_t *slot = j.slots + (uint64_t)j.gpu_slot[t * k + q] * j.slot_stride;
+    mbar_expect_tx(&bar[s], bn + bs);
+    bulk_g2s(dst, slot + j.down.nib_off + (uint64_t)tile * bn, bn, &bar[s]);
+    bulk_g2s(dst + bn, slot + j.down.sc_off + (uint64_t)tile * bs, bs, &bar[s]);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int q = 0; q < NS && q < k; ++q) issue(q);
+  if (tid < k) rows[tid] = t * k + tid;
+  __syncthreads();
+  stage_rows(xs, xsum, j.h, 0, rows, k, F);
+
+  for (int q = 0; q < k; ++q) {
+    const int s = q % NS;
+    if (!mbar_wait(&bar[s], (uint32_t)(q / NS) & 1u)) {
+      flag_error(j.err, 2);
+      return;
+    }
+    const uint4 *wn = reinterpret_cast<const uint4 *>(stages + (size_t)s * nb * 576);
+    const unsigned short *wsc = reinterpret_cast<const unsigned short *>(stages + (size_t)s * nb * 576 + bn);
+    float acc = 0.f;
+#pragma unroll 1
+    for (int b = warp; b < nb; b += kWarps) {
+      float f[32];
+      decode_block(wn[b * 32 + lane], f);
+      acc = block_term(f, half_bits(wsc[b * 32 + lane]), xs + (size_t)q * F + 32 * b,
+                       xsum[q * nb + b], acc);
+    }
+    red[(q * kWarps + warp) * 32 + lane] = acc;
+    __syncthreads();  // stage s is free again
+    if (tid == 0 && q + NS < k) {
+      fence_proxy_async();
+      issue(q + NS);
+    }
+  }
+  if (warp == 0) {
+    float o = 0.f;
+    for (int q = 0; q < k; ++q) {
+      float y = 0.f;
+      for (int w = 0; w < kWarps; ++w) y += red[(q * kWarps + w) * 32 + lane];
+      o = fmaf(j.w[t * k + q], y, o);
+    }
+    j.out[(size_t)t * j.H + tile * 32 + lane] = o;
+  }
+}
+
+// ---------------------------------------------------------------- fill
+struct FillJob {
+  RepackArgs a;
+  int S;
+  int nb_max;
+};
+
+__global__ void __launch_bounds__(kThreads) fill_kernel(FillJob jb) {
   const RepackArgs &a = jb.a;
   const PlanHdr *h = a.hdr;
   if (h->error || a.stage >= h->n_stages) return;
@@ -241,43 +416,68 @@ __global__ void __launch_bounds__(256) repack_kernel(RepackJob jb) {
   int m_lo, m_hi;
   if (a.stage == 0) { m_lo = 0; m_hi = n0; }
   else { m_lo = n0 + (a.stage - 1) * S; m_hi = min(nM, n0 + a.stage * S); }
-  const int mi = m_lo + (int)blockIdx.y;
-  if (mi >= m_hi) return;
-  const MissItem m = a.miss[mi];
-  const uint8_t *src = a.by_expert
-                           ? a.src_base + a.src_layer_off + (uint64_t)m.expert * a.src_expert_stride
-                           : a.src_base + (uint64_t)(mi - m_lo) * a.src_slot_stride;
-  uint8_t *dst = a.slots + (uint64_t)m.slot * a.slot_stride;
-
   const int tg = a.lay.gate.rows / 32, td = a.lay.down.rows / 32;
-  int tile = blockIdx.x;
-  const MatLayout *L;
-  if (tile < tg) L = &a.lay.gate;
-  else if (tile < 2 * tg) { L = &a.lay.up; tile -= tg; }
-  else { L = &a.lay.down; tile -= 2 * tg; }
-  (void)td;
-  const int R = L->rows, nb = L->nb, r0 = tile * 32;
-  // the canonical matrix starts where its nibble plane starts (same byte count)
-  const uint4 *csrc = reinterpret_cast<const uint4 *>(src + L->nib_off + (uint64_t)r0 * nb * 18);
-  const int n16 = 32 * nb * 18 / 16;
+  const int tiles = 2 * tg + td;
+  const int n_work = (m_hi - m_lo) * tiles;
+  const size_t buf_bytes = (size_t)32 * jb.nb_max * 18;
+  extern __shared__ __align__(128) unsigned char rs[];
 
-  extern __shared__ __align__(16) unsigned char rs[];
-  uint4 *s4 = reinterpret_cast<uint4 *>(rs);
-  // plain loads: the source may be mapped host memory
-  for (int i = threadIdx.x; i < n16; i += blockDim.x) s4[i] = csrc[i];
-  __syncthreads();
+  // work item -> (source tile, destination slot, matrix, tile index)
+  auto locate = [&](int wk, const uint8_t *&src, uint8_t *&dst, const MatLayout *&L, int &tl) {
+    const int mi = m_lo + wk / tiles;
+    tl = wk % tiles;
+    const MissItem m = a.miss[mi];
+    const uint8_t *blk = a.by_expert
+                             ? a.src_base + a.src_layer_off + (uint64_t)m.expert * a.src_expert_stride
+                             : a.src_base + (uint64_t)(mi - m_lo) * a.src_slot_stride;
+    dst = a.slots + (uint64_t)m.slot * a.slot_stride;
+    if (tl < tg) L = &a.lay.gate;
+    else if (tl < 2 * tg) { L = &a.lay.up; tl -= tg; }
+    else { L = &a.lay.down; tl -= 2 * tg; }
+    // the canonical matrix starts where its nibble plane starts (same byte count)
+    src = blk + L->nib_off + (uint64_t)tl * 32 * L->nb * 18;
+  };
+  auto issue = [&](int wk, int buf) {
+    const uint8_t *src;
+    uint8_t *dst;
+    const MatLayout *L;
+    int tl;
+    locate(wk, src, dst, L, tl);
+    const int n16 = 36 * L->nb;  // 32 rows x nb blocks x 18 bytes / 16
+    unsigned char *b = rs + (size_t)buf * buf_bytes;
+    for (int i = threadIdx.x; i < n16; i += kThreads) cp_async16(b + 16 * i, src + 16 * i);
+  };
 
-  uint4 *nib = reinterpret_cast<uint4 *>(dst + L->nib_off);
-  unsigned short *sc = reinterpret_cast<unsigned short *>(dst + L->sc_off);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  for (int b = warp; b < nb; b += nw) {
-    const unsigned short *blk = reinterpret_cast<const unsigned short *>(rs + ((size_t)lane * nb + b) * 18);
-    uint32_t v[4];
+  int wk = blockIdx.x;
+  if (wk < n_work) issue(wk, 0);
+  cp_async_commit();
+  for (int it = 0; wk < n_work; ++it, wk += gridDim.x) {
+    const int nxt = wk + gridDim.x;
+    if (nxt < n_work) issue(nxt, (it + 1) & 1);
+    cp_async_commit();
+    cp_async_wait1();
+    __syncthreads();
+    const uint8_t *src;
+    uint8_t *dst;
+    const MatLayout *L;
+    int tl;
+    locate(wk, src, dst, L, tl);
+    const int nb = L->nb;
+    const unsigned char *b0 = rs + (size_t)(it & 1) * buf_bytes;
+    uint4 *nib = reinterpret_cast<uint4 *>(dst + L->nib_off);
+    unsigned short *sc = reinterpret_cast<unsigned short *>(dst + L->sc_off);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int b = warp; b < nb; b += kWarps) {
+      const unsigned short *blk =
+          reinterpret_cast<const unsigned short *>(b0 + ((size_t)lane * nb + b) * 18);
+      uint32_t v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
-    const size_t e = (size_t)b * R + r0 + lane;
-    nib[e] = make_uint4(v[0], v[1], v[2], v[3]);
-    sc[e] = blk[0];
+      for (int i = 0; i < 4; ++i) v[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
+      const uint64_t e = tile_elem(tl * 32 + lane, b, nb);
+      nib[e] = make_uint4(v[0], v[1], v[2], v[3]);
+      sc[e] = blk[0];
+    }
+    __syncthreads();
   }
 }
 
@@ -293,15 +493,25 @@ __global__ void combine_kernel(const float *y, const float *w, const PlanHdr *hd
   out[i] = acc;
 }
 
-}  // namespace
+TileJob base_job(const FfnArgs &a) {
+  TileJob j;
+  j.slots = a.slots;
+  j.slot_stride = a.slot_stride;
+  j.perm = a.perm;
+  j.items = a.items;
+  j.units = a.units;
+  j.unit_begin = a.unit_begin;
+  j.hdr = a.hdr;
+  j.G = a.max_tok;
+  j.err = a.err;
+  return j;
+}
 
-static int max_tok_for(const FfnArgs &) { return kTokPerUnit; }
+}  // namespace
 
 cudaError_t launch_gateup(const FfnArgs &a, int range_kind, int stage, int max_units,
                           cudaStream_t st) {
-  GemvJob j;
-  j.slots = a.slots;
-  j.slot_stride = a.slot_stride;
+  TileJob j = base_job(a);
   j.m0 = a.lay.gate;
   j.m1 = a.lay.up;
   j.R = a.F;
@@ -309,23 +519,15 @@ cudaError_t launch_gateup(const FfnArgs &a, int range_kind, int stage, int max_u
   j.x = a.x;
   j.x_bf16 = a.x_bf16;
   j.x_div = a.k;
-  j.perm = a.perm;
-  j.items = a.items;
-  j.units = a.units;
-  j.unit_begin = a.unit_begin;
-  j.hdr = a.hdr;
   j.range_kind = range_kind;
   j.stage = stage;
   j.out = a.h;
-  j.max_tok = a.max_tok > 0 ? a.max_tok : max_tok_for(a);
-  return launch_gemv<2>(j, max_units, st);
+  return launch_tile<2>(j, max_units, st);
 }
 
 cudaError_t launch_down(const FfnArgs &a, int range_kind, int stage, int max_units,
                         cudaStream_t st) {
-  GemvJob j;
-  j.slots = a.slots;
-  j.slot_stride = a.slot_stride;
+  TileJob j = base_job(a);
   j.m0 = a.lay.down;
   j.m1 = a.lay.down;
   j.R = a.H;
@@ -333,16 +535,46 @@ cudaError_t launch_down(const FfnArgs &a, int range_kind, int stage, int max_uni
   j.x = a.h;
   j.x_bf16 = 0;
   j.x_div = 1;
-  j.perm = a.perm;
-  j.items = a.items;
-  j.units = a.units;
-  j.unit_begin = a.unit_begin;
-  j.hdr = a.hdr;
   j.range_kind = range_kind;
   j.stage = stage;
   j.out = a.y;
-  j.max_tok = a.max_tok > 0 ? a.max_tok : max_tok_for(a);
-  return launch_gemv<1>(j, max_units, st);
+  return launch_tile<1>(j, max_units, st);
+}
+
+static int dc_stages(int F, int k) {
+  const int nb = F / 32;
+  int NS = k < 8 ? k : 8;
+  while (NS > 1 && dc_smem(nb, k, NS) > 200 * 1024) --NS;
+  return NS;
+}
+
+bool down_combine_supported(int F, int k) {
+  return dc_smem(F / 32, k, dc_stages(F, k)) <= 200 * 1024;
+}
+
+cudaError_t launch_down_combine(const FfnArgs &a, const float *w, const int32_t *gpu_slot, int T,
+                                float *out, cudaStream_t st) {
+  DownCombineJob j;
+  j.slots = a.slots;
+  j.slot_stride = a.slot_stride;
+  j.down = a.lay.down;
+  j.H = a.H;
+  j.F = a.F;
+  j.k = a.k;
+  j.h = a.h;
+  j.w = w;
+  j.gpu_slot = gpu_slot;
+  j.hdr = a.hdr;
+  j.out = out;
+  j.NS = dc_stages(a.F, a.k);
+  j.err = a.err;
+  const size_t smem = dc_smem(a.F / 32, a.k, j.NS);
+  static size_t cur = 0;
+  const cudaError_t e = ensure_dyn_smem(down_combine_kernel, smem, cur);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.H / 32, T);
+  down_combine_kernel<<<grid, kThreads, smem, st>>>(j);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_combine(const float *y, const float *w, const PlanHdr *hdr, int T, int k, int H,
@@ -352,25 +584,16 @@ cudaError_t launch_combine(const float *y, const float *w, const PlanHdr *hdr, i
   return cudaGetLastError();
 }
 
-size_t repack_smem(const SlotLayout &lay) {
-  const int nbmax = lay.gate.nb > lay.down.nb ? lay.gate.nb : lay.down.nb;
-  return (size_t)32 * nbmax * 18;
-}
-
 cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t st) {
   if (max_miss <= 0) return cudaSuccess;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(repack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  const size_t smem = repack_smem(a.lay);
-  if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  RepackJob jb{a, S};
-  dim3 grid(2 * a.lay.gate.rows / 32 + a.lay.down.rows / 32, max_miss);
-  repack_kernel<<<grid, 256, smem, st>>>(jb);
+  FillJob jb{a, S, a.lay.gate.nb > a.lay.down.nb ? a.lay.gate.nb : a.lay.down.nb};
+  const size_t smem = 2 * (size_t)32 * jb.nb_max * 18;
+  static size_t cur = 0;
+  const cudaError_t e = ensure_dyn_smem(fill_kernel, smem, cur);
+  if (e != cudaSuccess) return e;
+  const int tiles = 2 * a.lay.gate.rows / 32 + a.lay.down.rows / 32;
+  const int grid = tiles * max_miss < kFillCtas ? tiles * max_miss : kFillCtas;
+  fill_kernel<<<grid, kThreads, smem, st>>>(jb);
   return cudaGetLastError();
 }
 

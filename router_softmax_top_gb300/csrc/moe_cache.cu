@@ -80,7 +80,7 @@ struct moe_cache {
   cudaEvent_t ev_plan = nullptr;
   std::vector<cudaEvent_t> ev_up, ev_done;
 
-  int poisoned = 0, last_error = MOE_OK;
+  int poisoned = 0, last_error = MOE_OK, cuda_error = 0;
   int last_layer = -1, last_T = 0;
   std::atomic<uint64_t> launches{0};
   TimingPool tp;
@@ -96,8 +96,17 @@ int poison(moe_cache *c, int code) {
   if (!c->poisoned) {
     c->poisoned = 1;
     c->last_error = code;
+    if (code == MOE_ERR_CUDA) {
+      const cudaError_t e = cudaGetLastError();
+      if (!c->cuda_error) c->cuda_error = (int)e;
+    }
   }
   return code;
+}
+
+int poison_cuda(moe_cache *c, cudaError_t e) {
+  if (!c->poisoned && !c->cuda_error) c->cuda_error = (int)e;
+  return poison(c, MOE_ERR_CUDA);
 }
 
 // --- timing: event pairs on the launching stream
@@ -446,6 +455,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   fa.h = c->d_h;
   fa.y = c->d_y;
   fa.max_tok = std::min(kTokPerUnit, T);
+  fa.err = c->d_err;
 
   RepackArgs ra;
   ra.slots = c->d_slots + (size_t)layer * S * c->lay.stride;
@@ -459,26 +469,68 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   do {                                                  \
     Launch _l(c, kind, st);                             \
     e = (expr);                                         \
-    if (e != cudaSuccess) return poison(c, MOE_ERR_CUDA); \
+    if (e != cudaSuccess) return poison_cuda(c, e);     \
   } while (0)
 
   MOE_LAUNCH(K_PLAN, launch_plan(pa, st));
+  if (cudaEventRecord(c->ev_plan, st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+  const bool dc_ok = down_combine_supported(g.ffn, k);
+
+  // fill of stage j's misses on the side stream, after `after` (recorded on st);
+  // the main stream then waits for it.  src_host: pull from the mapped store.
+  auto fill_stage = [&](int j, int nmiss, cudaEvent_t after, int mlo, bool from_mailbox) -> int {
+    if (cudaStreamWaitEvent(c->side, after, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    ra.stage = j;
+    if (g.fill_mode == MOE_FILL_MEMCPY) {
+      {
+        Launch l(c, K_MEMCPY, c->side);
+        const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) +
+                               (size_t)layer * c->store.layer_stride;
+        for (int i = mlo; i < mlo + nmiss; ++i) {
+          const MissItem m = c->h_mail_miss[i];
+          if (!from_mailbox || m.expert < 0 || m.expert >= E) return MOE_ERR_CUDA;
+          if (cudaMemcpyAsync(c->d_staging + (size_t)(i - mlo) * c->expert_bytes,
+                              lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
+                              cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        }
+      }
+      ra.src_base = c->d_staging;
+      ra.src_layer_off = 0;
+      ra.src_expert_stride = 0;
+      ra.src_slot_stride = c->expert_bytes;
+      ra.by_expert = 0;
+    } else {
+      ra.src_base = c->host_dev;
+      ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
+      ra.src_expert_stride = c->store.expert_stride;
+      ra.src_slot_stride = 0;
+      ra.by_expert = 1;
+    }
+    {
+      Launch l(c, K_REPACK, c->side);
+      if (launch_repack(ra, S, nmiss, c->side) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (cudaEventRecord(c->ev_up[j], c->side) != cudaSuccess ||
+        cudaStreamWaitEvent(st, c->ev_up[j], 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  };
 
   if (!need_host) {
-    // single stage guaranteed; everything stays on the device
-    ra.src_base = c->host_dev;
-    ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
-    ra.src_expert_stride = c->store.expert_stride;
-    ra.src_slot_stride = 0;
-    ra.by_expert = 1;
-    ra.stage = 0;
-    MOE_LAUNCH(K_REPACK, launch_repack(ra, S, maxU, st));
-    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 2, 0, maxUnits, st));
-    MOE_LAUNCH(K_DOWN, launch_down(fa, 2, 0, maxUnits, st));
-    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+    // pull fill, single stage guaranteed (at most S distinct experts): no host
+    // round trip; the fill overlaps the hit gate/up
+    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
+    int rc = fill_stage(0, maxU, c->ev_plan, 0, false);  // main waits for it from here on
+    if (rc != MOE_OK) return poison(c, rc);
+    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, 0, maxUnits, st));
+    if (dc_ok) {
+      MOE_LAUNCH(K_DOWN, launch_down_combine(fa, c->d_w, c->d_gpu_slot, T, d_out, st));
+    } else {
+      MOE_LAUNCH(K_DOWN, launch_down(fa, 2, 0, maxUnits, st));
+      MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+    }
   } else {
-    // copies may start as soon as the plan exists; stage-0 hits need no copy
-    if (cudaEventRecord(c->ev_plan, st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
     int rc = wait_mailbox(c, c->seq, st);
     if (rc != MOE_OK) return poison(c, rc);
@@ -489,51 +541,24 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     for (int j = 0; j < n_st; ++j) {
       const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
       const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
-      const int nmiss = mhi - mlo;
-      if (nmiss > 0) {
-        ra.stage = j;
-        if (g.fill_mode == MOE_FILL_MEMCPY) {
-          if (cudaStreamWaitEvent(c->side, j == 0 ? c->ev_plan : c->ev_done[j - 1], 0) != cudaSuccess)
-            return poison(c, MOE_ERR_CUDA);
-          {
-            Launch l(c, K_MEMCPY, c->side);
-            const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) +
-                                   (size_t)layer * c->store.layer_stride;
-            for (int i = mlo; i < mhi; ++i) {
-              const MissItem m = c->h_mail_miss[i];
-              if (m.expert < 0 || m.expert >= E) return poison(c, MOE_ERR_CUDA);
-              if (cudaMemcpyAsync(c->d_staging + (size_t)(i - mlo) * c->expert_bytes,
-                                  lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
-                                  cudaMemcpyHostToDevice, c->side) != cudaSuccess)
-                return poison(c, MOE_ERR_CUDA);
-            }
-          }
-          if (cudaEventRecord(c->ev_up[j], c->side) != cudaSuccess ||
-              cudaStreamWaitEvent(st, c->ev_up[j], 0) != cudaSuccess)
-            return poison(c, MOE_ERR_CUDA);
-          ra.src_base = c->d_staging;
-          ra.src_layer_off = 0;
-          ra.src_expert_stride = 0;
-          ra.src_slot_stride = c->expert_bytes;
-          ra.by_expert = 0;
-        } else {
-          ra.src_base = c->host_dev;
-          ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
-          ra.src_expert_stride = c->store.expert_stride;
-          ra.src_slot_stride = 0;
-          ra.by_expert = 1;
-        }
-        MOE_LAUNCH(K_REPACK, launch_repack(ra, S, nmiss, st));
+      if (mhi > mlo) {
+        rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+        if (rc != MOE_OK) return poison(c, rc);
       }
       const int ulo = j == 0 ? hdr.hit_units : c->h_mail_ub[j];
       const int uhi = c->h_mail_ub[j + 1];
       if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, j, uhi - ulo, st));
-      const int dlo = c->h_mail_ub[j];
-      if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
-      if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
-        return poison(c, MOE_ERR_CUDA);
+      if (n_st == 1 && dc_ok) {
+        MOE_LAUNCH(K_DOWN, launch_down_combine(fa, c->d_w, c->d_gpu_slot, T, d_out, st));
+      } else {
+        const int dlo = c->h_mail_ub[j];
+        if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
+        if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
+          return poison(c, MOE_ERR_CUDA);
+      }
     }
-    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+    if (n_st > 1 || !dc_ok)
+      MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
   }
 #undef MOE_LAUNCH
   c->last_layer = layer;
@@ -580,6 +605,8 @@ MOE_API int moe_cache_stats(const moe_cache *cc, int32_t layer, moe_cache_stats_
   if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) poison(c, MOE_ERR_INVALID_ARG);
   out->poisoned = c->poisoned;
   out->last_error = c->last_error;
+  out->cuda_error = c->cuda_error;
+  out->reserved = 0;
   return MOE_OK;
 }
 
@@ -656,8 +683,9 @@ MOE_API int moe_cache_probe_h2d(moe_cache *c, int32_t iters, double *gbps) {
   std::vector<double> v;
   const uint8_t *base = static_cast<const uint8_t *>(c->store.base);
   int rc = MOE_OK;
-  for (int i = 0; i < iters && rc == MOE_OK; ++i) {
-    const int e = i % c->cfg.n_experts;
+  // one untimed pass over the same blocks first (first-touch effects), then timed
+  for (int i = 0; i < 2 * iters && rc == MOE_OK; ++i) {
+    const int e = i % iters % c->cfg.n_experts;
     cudaEventRecord(a, c->side);
     if (cudaMemcpyAsync(c->d_staging, base + (size_t)e * c->store.expert_stride, c->expert_bytes,
                         cudaMemcpyHostToDevice, c->side) != cudaSuccess) {
@@ -667,7 +695,7 @@ MOE_API int moe_cache_probe_h2d(moe_cache *c, int32_t iters, double *gbps) {
     cudaEventRecord(b, c->side);
     rc = wait_stream(c->side, c->cfg.timeout_us);
     float ms = 0.f;
-    if (rc == MOE_OK && cudaEventElapsedTime(&ms, a, b) == cudaSuccess && ms > 0.f)
+    if (i >= iters && rc == MOE_OK && cudaEventElapsedTime(&ms, a, b) == cudaSuccess && ms > 0.f)
       v.push_back((double)c->expert_bytes / (ms * 1e-3) / 1e9);
   }
   cudaEventDestroy(a);

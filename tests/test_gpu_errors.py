@@ -130,6 +130,6 @@ def test_timing_and_launch_count(store):
     t = c.timing()
     c.set_timing(False)
     assert t["plan"]["launches"] == 3 and t["plan"]["ms"] > 0
-    assert c.launch_count() >= 3 * 4
+    assert c.launch_count() >= 3 * 3      # plan, gate/up, down(+combine) at least
     assert c.probe_h2d(5) > 0.1
     c.close()

@@ -79,7 +79,8 @@ def test_struct_layout_matches_header(tmp_path):
 int main(void) {
   printf("%zu %zu %zu %zu\n", sizeof(moe_cache_config), offsetof(moe_cache_config, timeout_us),
          sizeof(moe_host_store), sizeof(moe_cache_stats_t));
-  printf("%zu %zu\n", offsetof(moe_cache_stats_t, poisoned), offsetof(moe_cache_stats_t, last_error));
+  printf("%zu %zu %zu\n", offsetof(moe_cache_stats_t, poisoned), offsetof(moe_cache_stats_t, last_error),
+         offsetof(moe_cache_stats_t, cuda_error));
   return 0;
 }''')
     exe = tmp_path / "layout"
@@ -89,4 +90,5 @@ int main(void) {
     b = [int(v) for v in b.split()]
     assert a == [ctypes.sizeof(moe.MoeCacheConfig), moe.MoeCacheConfig.timeout_us.offset,
                  ctypes.sizeof(moe.MoeHostStore), ctypes.sizeof(moe.MoeCacheStats)]
-    assert b == [moe.MoeCacheStats.poisoned.offset, moe.MoeCacheStats.last_error.offset]
+    assert b == [moe.MoeCacheStats.poisoned.offset, moe.MoeCacheStats.last_error.offset,
+                 moe.MoeCacheStats.cuda_error.offset]
