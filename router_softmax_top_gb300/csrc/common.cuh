@@ -142,6 +142,7 @@ struct PlanArgs {
   MissItem *miss;     // [min(E, T*k)]
   PlanHdr *hdr;
   int32_t *err_flag;  // sticky device error word of the handle
+  int32_t *sync;      // per-call counters [min(E, T*k) + 1], zeroed here
   Mailbox *mailbox;   // device alias of the mapped host mailbox, or null
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;
@@ -197,8 +198,14 @@ struct RepackArgs {
   int stage;  // misses of this stage
 };
 cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t st);
+// Misses of a single-stage call of at most 8 tokens: fill + gate/up + down in
+// one kernel (y of the miss pairs written to FfnArgs::y).  sync: per-call
+// counters zeroed by the plan kernel ([0] queue head, [1 + m] per miss).
+cudaError_t launch_fused_miss(const FfnArgs &a, const RepackArgs &r, int32_t *sync, int grid,
+                              cudaStream_t st);
+bool fused_miss_supported(int H, int F);
 
 enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,
-                  K_GATHER, K_MEMCPY, K_NKINDS };
+                  K_GATHER, K_MEMCPY, K_FUSED, K_NKINDS };
 
 }  // namespace moe

@@ -136,8 +136,9 @@ __device__ __forceinline__ float half_bits(unsigned short v) {
 
 // Stage n input rows of K values (fp32 or bf16) into shared memory and the
 // per-block sums X_b (one warp per block: lane j holds value j, fixed xor tree).
+// l2_only: read through L2 only (inputs written by other CTAs of the same kernel).
 __device__ __forceinline__ void stage_rows(float *xs, float *xsum, const void *x, int x_bf16,
-                                           const int *rows, int n, int K) {
+                                           const int *rows, int n, int K, bool l2_only = false) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nb = K / 32;
   for (int t = 0; t < n; ++t) {
     const int row = rows[t];
@@ -148,7 +149,10 @@ __device__ __forceinline__ void stage_rows(float *xs, float *xsum, const void *x
       const float4 *src =
           reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(x) + (size_t)row * K);
       float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * K);
-      for (int c = tid; c < K / 4; c += kThreads) dst[c] = src[c];
+      if (l2_only)
+        for (int c = tid; c < K / 4; c += kThreads) dst[c] = __ldcg(src + c);
+      else
+        for (int c = tid; c < K / 4; c += kThreads) dst[c] = src[c];
     }
   }
   __syncthreads();
@@ -481,6 +485,196 @@ __global__ void __launch_bounds__(kThreads) fill_kernel(FillJob jb) {
   }
 }
 
+// ------------------------------------------------------ fused miss path
+// For single-stage calls of at most 8 tokens: every missed expert is read once
+// from its source (mapped host store or staging), written into its slot in the
+// tiled layout, and used for compute on the way, so the misses' FFN hides
+// under the transfer.  Work items come from a queue in order: all gate/up
+// tiles (32 rows of gate and of up), then all down tiles; a down tile waits for
+// the gate/up tiles of its expert (a per-miss counter; bounded wait).  Since
+// items are claimed in order by running CTAs, the tiles a down tile waits for
+// are already being processed.  The per-pair arithmetic and its order are
+// those of q4_tile_gemv_kernel and down_combine_kernel.
+struct FusedMissJob {
+  const uint8_t *src_base;
+  uint64_t src_layer_off, src_expert_stride, src_slot_stride;
+  int by_expert;
+  uint8_t *slots;
+  uint64_t slot_stride;
+  SlotLayout lay;
+  const MissItem *miss;
+  const PlanHdr *hdr;
+  const WorkItem *items;
+  const int32_t *perm;
+  const void *x;
+  int x_bf16;
+  int k, H, F;
+  float *h;        // [T*k, F]
+  float *y;        // [T*k, H]
+  int32_t *sync;   // [0] queue head, [1 + m] finished gate/up tiles of miss m
+  int32_t *err;
+  int G;           // tokens per shared-memory input group
+};
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+size_t fused_smem(int nbH, int nbF, int G) {
+  const size_t canon = (size_t)32 * 18 * (2 * nbH > nbF ? 2 * nbH : nbF);
+  const int kmax = 32 * (nbH > nbF ? nbH : nbF), nbmax = nbH > nbF ? nbH : nbF;
+  return canon + sizeof(float) * ((size_t)G * kmax + (size_t)G * nbmax + (size_t)kWarps * 2 * G * 32);
+}
+
+// One block of one row read from the canonical tile in shared memory:
+// returns the 16 nibble bytes and writes the scale bits.
+__device__ __forceinline__ uint4 canon_block(const unsigned char *canon, int row, int b, int nb,
+                                             unsigned short &dbits) {
+  const unsigned short *blk = reinterpret_cast<const unsigned short *>(canon + ((size_t)row * nb + b) * 18);
+  dbits = blk[0];
+  uint32_t v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = (uint32_t)blk[1 + 2 * i] | ((uint32_t)blk[2 + 2 * i] << 16);
+  return make_uint4(v[0], v[1], v[2], v[3]);
+}
+
+__global__ void __launch_bounds__(kThreads) fused_miss_kernel(FusedMissJob j) {
+  const PlanHdr *hd = j.hdr;
+  if (hd->error) return;
+  const int nM = hd->n_stage0_miss, nH = hd->n_hits;
+  const int nbH = j.H / 32, nbF = j.F / 32, tF = j.F / 32, tH = j.H / 32;
+  const int n_a = nM * tF, n_total = n_a + nM * tH;
+  if (n_total == 0) return;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, G = j.G;
+
+  extern __shared__ __align__(128) unsigned char sm[];
+  const size_t canon_bytes = (size_t)32 * 18 * (2 * nbH > nbF ? 2 * nbH : nbF);
+  unsigned char *canon = sm;
+  float *xs = reinterpret_cast<float *>(sm + canon_bytes);
+  const int kmax = 32 * (nbH > nbF ? nbH : nbF), nbmax = nbH > nbF ? nbH : nbF;
+  float *xsum = xs + (size_t)G * kmax;
+  float *red = xsum + (size_t)G * nbmax;  // [warps][2][G][32]
+  __shared__ int s_wk, s_ok;
+  __shared__ int rows[kTokPerUnit];
+
+  for (;;) {
+    if (tid == 0) s_wk = atomicAdd(&j.sync[0], 1);
+    __syncthreads();
+    const int wk = s_wk;
+    if (wk >= n_total) break;
+    const bool is_gu = wk < n_a;
+    const int m = is_gu ? wk / tF : (wk - n_a) / tH;
+    const int t = is_gu ? wk % tF : (wk - n_a) % tH;
+    const MissItem mi = j.miss[m];
+    const WorkItem it = j.items[nH + m];
+    const int n = it.pair_count;
+    const uint8_t *blk = j.by_expert
+                             ? j.src_base + j.src_layer_off + (uint64_t)mi.expert * j.src_expert_stride
+                             : j.src_base + (uint64_t)m * j.src_slot_stride;
+    uint8_t *dst = j.slots + (uint64_t)mi.slot * j.slot_stride;
+    if (!is_gu) {
+      // wait until every gate/up tile of this expert has produced h
+      if (tid == 0) {
+        int ok = 0;
+        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+          if (ld_acquire(&j.sync[1 + m]) >= tF) { ok = 1; break; }
+          __nanosleep(64);
+        }
+        s_ok = ok;
+      }
+      __syncthreads();
+      if (!s_ok) {
+        flag_error(j.err, 3);
+        return;
+      }
+    }
+    const int nb = is_gu ? nbH : nbF;
+    const int nmat = is_gu ? 2 : 1;
+    // canonical rows [32t, 32t+32) of each matrix of this item
+    const MatLayout *L0 = is_gu ? &j.lay.gate : &j.lay.down;
+    const MatLayout *L1 = &j.lay.up;
+    const size_t tile_bytes = (size_t)32 * nb * 18;
+    for (int mm = 0; mm < nmat; ++mm) {
+      const MatLayout *L = mm == 0 ? L0 : L1;
+      const uint8_t *src = blk + L->nib_off + (uint64_t)t * tile_bytes;
+      for (int i = tid; i < (int)(tile_bytes / 16); i += kThreads)
+        cp_async16(canon + mm * tile_bytes + 16 * i, src + 16 * i);
+    }
+    cp_async_commit();
+    if (tid < n) rows[tid] = is_gu ? j.perm[it.pair_begin + tid] / j.k : j.perm[it.pair_begin + tid];
+    __syncthreads();
+    const int K = 32 * nb;
+    for (int g0 = 0; g0 < n; g0 += G) {
+      const int gn = min(G, n - g0);
+      if (is_gu) stage_rows(xs, xsum, j.x, j.x_bf16, rows + g0, gn, K);
+      else stage_rows(xs, xsum, j.h, 0, rows + g0, gn, K, true);
+      if (g0 == 0) {
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        __syncthreads();
+      }
+      float acc0[kTokPerUnit], acc1[kTokPerUnit];
+#pragma unroll
+      for (int q = 0; q < kTokPerUnit; ++q) { acc0[q] = 0.f; acc1[q] = 0.f; }
+#pragma unroll 1
+      for (int b = warp; b < nb; b += kWarps) {
+        float f0[32], f1[32];
+        unsigned short d0b, d1b = 0;
+        const uint4 q0 = canon_block(canon, lane, b, nb, d0b);
+        decode_block(q0, f0);
+        uint4 q1 = make_uint4(0, 0, 0, 0);
+        if (is_gu) {
+          q1 = canon_block(canon + tile_bytes, lane, b, nb, d1b);
+          decode_block(q1, f1);
+        }
+        if (g0 == 0) {
+          const uint64_t e = tile_elem(t * 32 + lane, b, nb);
+          reinterpret_cast<uint4 *>(dst + L0->nib_off)[e] = q0;
+          reinterpret_cast<unsigned short *>(dst + L0->sc_off)[e] = d0b;
+          if (is_gu) {
+            reinterpret_cast<uint4 *>(dst + L1->nib_off)[e] = q1;
+            reinterpret_cast<unsigned short *>(dst + L1->sc_off)[e] = d1b;
+          }
+        }
+        const float d0 = half_bits(d0b), d1 = half_bits(d1b);
+#pragma unroll
+        for (int q = 0; q < kTokPerUnit; ++q) {
+          if (q < gn) {
+            const float *xb = xs + (size_t)q * K + 32 * b;
+            const float xsb = xsum[q * nb + b];
+            acc0[q] = block_term(f0, d0, xb, xsb, acc0[q]);
+            if (is_gu) acc1[q] = block_term(f1, d1, xb, xsb, acc1[q]);
+          }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kTokPerUnit; ++q) {
+        if (q < gn) {
+          red[((warp * 2 + 0) * G + q) * 32 + lane] = acc0[q];
+          red[((warp * 2 + 1) * G + q) * 32 + lane] = acc1[q];
+        }
+      }
+      __syncthreads();
+      for (int q = warp; q < gn; q += kWarps) {
+        float g = 0.f, v = 0.f;
+        for (int w = 0; w < kWarps; ++w) {
+          g += red[((w * 2 + 0) * G + q) * 32 + lane];
+          if (is_gu) v += red[((w * 2 + 1) * G + q) * 32 + lane];
+        }
+        const int pair = j.perm[it.pair_begin + g0 + q];
+        if (is_gu) j.h[(size_t)pair * j.F + t * 32 + lane] = g / (1.f + expf(-g)) * v;
+        else j.y[(size_t)pair * j.H + t * 32 + lane] = g;
+      }
+      __syncthreads();
+    }
+    if (is_gu && tid == 0) {
+      __threadfence();
+      atomicAdd(&j.sync[1 + m], 1);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- combine
 __global__ void combine_kernel(const float *y, const float *w, const PlanHdr *hdr, int T, int k,
                                int H, float *out) {
@@ -583,6 +777,44 @@ cudaError_t launch_combine(const float *y, const float *w, const PlanHdr *hdr, i
   combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(y, w, hdr, T, k, H, out);
   return cudaGetLastError();
 }
+
+cudaError_t launch_fused_miss(const FfnArgs &a, const RepackArgs &r, int32_t *sync, int grid,
+                              cudaStream_t st) {
+  FusedMissJob j;
+  j.src_base = r.src_base;
+  j.src_layer_off = r.src_layer_off;
+  j.src_expert_stride = r.src_expert_stride;
+  j.src_slot_stride = r.src_slot_stride;
+  j.by_expert = r.by_expert;
+  j.slots = r.slots;
+  j.slot_stride = r.slot_stride;
+  j.lay = r.lay;
+  j.miss = r.miss;
+  j.hdr = r.hdr;
+  j.items = a.items;
+  j.perm = a.perm;
+  j.x = a.x;
+  j.x_bf16 = a.x_bf16;
+  j.k = a.k;
+  j.H = a.H;
+  j.F = a.F;
+  j.h = a.h;
+  j.y = a.y;
+  j.sync = sync;
+  j.err = a.err;
+  int G = a.max_tok;
+  while (G > 1 && fused_smem(a.H / 32, a.F / 32, G) > 200 * 1024) --G;
+  j.G = G;
+  const size_t smem = fused_smem(a.H / 32, a.F / 32, G);
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static size_t cur = 0;
+  const cudaError_t e = ensure_dyn_smem(fused_miss_kernel, smem, cur);
+  if (e != cudaSuccess) return e;
+  fused_miss_kernel<<<grid, kThreads, smem, st>>>(j);
+  return cudaGetLastError();
+}
+
+bool fused_miss_supported(int H, int F) { return fused_smem(H / 32, F / 32, 1) <= 200 * 1024; }
 
 cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t st) {
   if (max_miss <= 0) return cudaSuccess;

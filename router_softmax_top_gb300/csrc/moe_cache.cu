@@ -64,6 +64,7 @@ struct moe_cache {
   WorkUnit *d_units = nullptr;
   MissItem *d_miss = nullptr;
   PlanHdr *d_hdr = nullptr;
+  int32_t *d_sync = nullptr;
   uint8_t *d_staging = nullptr;
   int staging_blocks = 0;
 
@@ -88,9 +89,9 @@ struct moe_cache {
 
 namespace {
 
-const char *const kKindNames[K_NKINDS] = {"plan",      "repack",    "q4_gateup_gemv", "q4_down_gemv",
-                                          "combine",   "gemm_gateup", "gemm_down",    "gather",
-                                          "h2d_memcpy"};
+const char *const kKindNames[K_NKINDS] = {"plan",        "repack",    "q4_gateup_gemv", "q4_down_gemv",
+                                          "combine",     "gemm_gateup", "gemm_down",    "gather",
+                                          "h2d_memcpy",  "fused_miss"};
 
 int poison(moe_cache *c, int code) {
   if (!c->poisoned) {
@@ -210,6 +211,7 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_units);
   cudaFree(c->d_miss);
   cudaFree(c->d_hdr);
+  cudaFree(c->d_sync);
   cudaFree(c->d_staging);
   if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
   if (c->h_err) cudaFreeHost(c->h_err);
@@ -334,6 +336,7 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_units, c->maxUnits) == cudaSuccess;
   ok = ok && dalloc(&c->d_miss, c->maxU) == cudaSuccess;
   ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
+  ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 33) == cudaSuccess;
   if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
     c->staging_blocks = std::min(S, c->maxU);
     ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess;
@@ -434,6 +437,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.miss = c->d_miss;
   pa.hdr = c->d_hdr;
   pa.err_flag = c->d_err;
+  pa.sync = c->d_sync;
   pa.mailbox = need_host ? c->d_mail : nullptr;
   pa.mailbox_stage_cap = c->mail_stage_cap;
   pa.seq = c->seq;
@@ -517,9 +521,59 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     return MOE_OK;
   };
 
-  if (!need_host) {
-    // pull fill, single stage guaranteed (at most S distinct experts): no host
-    // round trip; the fill overlaps the hit gate/up
+  const bool fused_ok = T <= kTokPerUnit && fused_miss_supported(g.hidden, g.ffn);
+
+  // misses of a single-stage call through the fused kernel on the side stream
+  // (after `after`), the main stream waiting for it before the combine
+  auto fused_stage0 = [&](cudaEvent_t after, int nmiss_max, bool copies) -> int {
+    if (cudaStreamWaitEvent(c->side, after, 0) != cudaSuccess) return MOE_ERR_CUDA;
+    if (g.fill_mode == MOE_FILL_MEMCPY) {
+      if (copies) {
+        Launch l(c, K_MEMCPY, c->side);
+        const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) +
+                               (size_t)layer * c->store.layer_stride;
+        for (int i = 0; i < nmiss_max; ++i) {
+          const MissItem m = c->h_mail_miss[i];
+          if (m.expert < 0 || m.expert >= E) return MOE_ERR_CUDA;
+          if (cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
+                              lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
+                              cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        }
+      }
+      ra.src_base = c->d_staging;
+      ra.src_layer_off = 0;
+      ra.src_expert_stride = 0;
+      ra.src_slot_stride = c->expert_bytes;
+      ra.by_expert = 0;
+    } else {
+      ra.src_base = c->host_dev;
+      ra.src_layer_off = (uint64_t)layer * c->store.layer_stride;
+      ra.src_expert_stride = c->store.expert_stride;
+      ra.src_slot_stride = 0;
+      ra.by_expert = 1;
+    }
+    ra.stage = 0;
+    {
+      Launch l(c, K_FUSED, c->side);
+      const int grid = std::max(1, std::min(96, nmiss_max * (g.ffn / 32 + g.hidden / 32)));
+      if (launch_fused_miss(fa, ra, c->d_sync, grid, c->side) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (cudaEventRecord(c->ev_up[0], c->side) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  };
+
+  if (!need_host && fused_ok) {
+    // pull fill, single stage guaranteed, few tokens: misses read once from the
+    // host store and computed on the way; hits computed beside them
+    int rc = fused_stage0(c->ev_plan, maxU, false);
+    if (rc != MOE_OK) return poison(c, rc);
+    MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
+    MOE_LAUNCH(K_DOWN, launch_down(fa, 0, 0, maxUnits, st));
+    if (cudaStreamWaitEvent(st, c->ev_up[0], 0) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+  } else if (!need_host) {
+    // pull fill, single stage guaranteed: the fill overlaps the hit gate/up
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
     int rc = fill_stage(0, maxU, c->ev_plan, 0, false);  // main waits for it from here on
     if (rc != MOE_OK) return poison(c, rc);
@@ -538,27 +592,38 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
     const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss;
     if (n_st < 1 || n_st > c->maxStages - 1) return poison(c, MOE_ERR_CUDA);
-    for (int j = 0; j < n_st; ++j) {
-      const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
-      const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
-      if (mhi > mlo) {
-        rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+    if (n_st == 1 && fused_ok) {
+      if (nM > 0) {
+        rc = fused_stage0(c->ev_plan, nM, true);
         if (rc != MOE_OK) return poison(c, rc);
       }
-      const int ulo = j == 0 ? hdr.hit_units : c->h_mail_ub[j];
-      const int uhi = c->h_mail_ub[j + 1];
-      if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, j, uhi - ulo, st));
-      if (n_st == 1 && dc_ok) {
-        MOE_LAUNCH(K_DOWN, launch_down_combine(fa, c->d_w, c->d_gpu_slot, T, d_out, st));
-      } else {
-        const int dlo = c->h_mail_ub[j];
-        if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
-        if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
-          return poison(c, MOE_ERR_CUDA);
-      }
-    }
-    if (n_st > 1 || !dc_ok)
+      MOE_LAUNCH(K_DOWN, launch_down(fa, 0, 0, std::max(1, hdr.hit_units), st));
+      if (nM > 0 && cudaStreamWaitEvent(st, c->ev_up[0], 0) != cudaSuccess)
+        return poison(c, MOE_ERR_CUDA);
       MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+    } else {
+      for (int j = 0; j < n_st; ++j) {
+        const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
+        const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
+        if (mhi > mlo) {
+          rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+          if (rc != MOE_OK) return poison(c, rc);
+        }
+        const int ulo = j == 0 ? hdr.hit_units : c->h_mail_ub[j];
+        const int uhi = c->h_mail_ub[j + 1];
+        if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, j, uhi - ulo, st));
+        if (n_st == 1 && dc_ok) {
+          MOE_LAUNCH(K_DOWN, launch_down_combine(fa, c->d_w, c->d_gpu_slot, T, d_out, st));
+        } else {
+          const int dlo = c->h_mail_ub[j];
+          if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
+          if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
+            return poison(c, MOE_ERR_CUDA);
+        }
+      }
+      if (n_st > 1 || !dc_ok)
+        MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
+    }
   }
 #undef MOE_LAUNCH
   c->last_layer = layer;

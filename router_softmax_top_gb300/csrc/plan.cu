@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     e_stage[e] = -1;
   }
   for (int i = tid; i < NW * E; i += NT) wcnt[i] = 0;
+  for (int i = tid; i <= (E < P ? E : P); i += NT) a.sync[i] = 0;
   if (tid < 8) scal[tid] = 0;
   const unsigned long long now = *a.clock + 1ull;
   __syncthreads();
@@ -430,6 +431,178 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   }
 }
 
+
+// Single-warp plan for small calls: at most 32 (token, pick) pairs, at most 256
+// slots, and no more distinct experts possible than slots (one stage).  Same
+// rule and outputs as plan_kernel, with warp-synchronous code only (small
+// code: this kernel runs once per layer call, mostly from a cold instruction
+// cache).
+constexpr int kSmallMaxSlots = 256;
+
+__global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
+  const unsigned F = 0xffffffffu;
+  const int E = a.E, S = a.S, k = a.k, T = a.T, P = T * k;
+  const int lane = threadIdx.x;
+  __shared__ int s_bad;
+  __shared__ uint32_t s_pinned[kSmallMaxSlots / 32];
+  if (lane == 0) s_bad = 0;
+  if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
+  a.sync[lane] = 0;  // P <= 32: 33 counters
+  if (lane == 0) a.sync[32] = 0;
+  __syncwarp();
+  for (int t = 0; t < T; ++t) {
+    if (E <= 256) route_token<8>(a.logits + (size_t)t * E, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+    else route_token<32>(a.logits + (size_t)t * E, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+  }
+  __syncwarp();
+  if (s_bad) {
+    write_error(a);
+    return;
+  }
+  const unsigned long long now = *a.clock + 1ull;
+
+  // distinct experts: one leader lane per expert
+  const bool act = lane < P;
+  const int e = act ? a.ids[lane] : -1 - lane;
+  const unsigned same = __match_any_sync(F, e);
+  const int leader = __ffs(same) - 1;
+  const bool lead = act && leader == lane;
+  const int cnt = __popc(same);
+  const int es0 = lead ? a.expert_slot[e] : -1;
+  const bool hit = lead && es0 >= 0, miss = lead && es0 < 0;
+  const unsigned hmask = __ballot_sync(F, hit), mmask = __ballot_sync(F, miss);
+  const int nH = __popc(hmask), nM = __popc(mmask), nU = nH + nM;
+  int hr = 0, mr = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int ej = __shfl_sync(F, e, j);
+    hr += ((hmask >> j) & 1u) && ej < e;
+    mr += ((mmask >> j) & 1u) && ej < e;
+  }
+  const int my_hit = __shfl_sync(F, hit ? 1 : 0, leader);
+  const int pick_hits = __popc(__ballot_sync(F, act && my_hit));
+  if (hit) atomicOr(&s_pinned[es0 >> 5], 1u << (es0 & 31));
+  __syncwarp();
+
+  // stage-0 victims: empty slots (by index), then unpinned slots by (stamp, index)
+  const int nch = (S + 31) / 32;
+  unsigned long long key[kSmallMaxSlots / 32];
+#pragma unroll
+  for (int c = 0; c < kSmallMaxSlots / 32; ++c) {
+    key[c] = ~0ull;
+    const int sl = c * 32 + lane;
+    if (c < nch && sl < S && !((s_pinned[c] >> lane) & 1u)) {
+      const int se = a.slot_expert[sl];
+      key[c] = se < 0 ? (unsigned long long)sl
+                      : (1ull << 62) | ((unsigned long long)a.slot_stamp[sl] << 11) | (unsigned)sl;
+    }
+  }
+  int my_victim = -1;  // lane r holds the victim of miss rank r
+  for (int r = 0; r < nM; ++r) {
+    unsigned long long best = ~0ull;
+#pragma unroll
+    for (int c = 0; c < kSmallMaxSlots / 32; ++c) best = key[c] < best ? key[c] : best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(F, best, o);
+      best = other < best ? other : best;
+    }
+    const int sl = (int)(best & 2047ull);
+    if (lane == (sl & 31)) {
+#pragma unroll
+      for (int c = 0; c < kSmallMaxSlots / 32; ++c)
+        if (c == (sl >> 5)) key[c] = ~0ull;
+    }
+    if (lane == r) my_victim = sl;
+  }
+  const int vslot = __shfl_sync(F, my_victim, miss ? mr : 0);
+  const int my_slot = hit ? es0 : (miss ? vslot : -1);
+  const int evicted = miss ? a.slot_expert[vslot] : -1;
+  const int n_evict = __popc(__ballot_sync(F, miss && evicted >= 0));
+  __syncwarp();
+
+  // new state
+  if (miss) {
+    a.slot_expert[vslot] = e;
+    a.expert_slot[e] = vslot;
+    a.slot_stamp[vslot] = now;
+    if (evicted >= 0) a.expert_slot[evicted] = -1;
+    a.miss[mr] = MissItem{e, vslot, evicted, 0};
+  }
+  if (hit) a.slot_stamp[es0] = now;
+
+  // per-pair slot and stage
+  const int pslot = __shfl_sync(F, my_slot, leader);
+  if (act) {
+    a.gpu_slot[lane] = pslot;
+    a.stage[lane] = 0;
+  }
+
+  // work items (hits ascending, then misses ascending), units, perm
+  const int item = hit ? hr : (miss ? nH + mr : -1);
+  const int ucount = (cnt + kTokPerUnit - 1) / kTokPerUnit;
+  int pb = 0, ub = 0, hit_units = 0, n_units = 0;
+  for (int j = 0; j < 32; ++j) {
+    const int ij = __shfl_sync(F, item, j);
+    const int cj = __shfl_sync(F, cnt, j);
+    const int uj = (cj + kTokPerUnit - 1) / kTokPerUnit;
+    if (ij < 0) continue;
+    if (ij < item) { pb += cj; ub += uj; }
+    if (ij < nH) hit_units += uj;
+    n_units += uj;
+  }
+  if (lead) {
+    a.items[item] = WorkItem{e, my_slot, 0, miss ? 1 : 0, pb, cnt};
+    for (int j = 0; j < ucount; ++j)
+      a.units[ub + j] = WorkUnit{item, pb + j * kTokPerUnit, min(kTokPerUnit, cnt - j * kTokPerUnit), 0};
+  }
+  const int ppb = __shfl_sync(F, pb, leader);
+  if (act) a.perm[ppb + __popc(same & ((1u << lane) - 1u))] = lane;
+  if (lane == 0) {
+    a.unit_begin[0] = 0;
+    a.unit_begin[1] = n_units;
+    PlanHdr h = {};
+    h.n_unique = nU;
+    h.n_hits = nH;
+    h.n_miss = nM;
+    h.n_stage0_miss = nM;
+    h.n_stages = 1;
+    h.n_units = n_units;
+    h.n_evict = n_evict;
+    h.pick_hits = pick_hits;
+    h.pick_misses = P - pick_hits;
+    h.hit_units = hit_units;
+    *a.hdr = h;
+    *a.clock = now;
+    uint64_t *st = a.stats;
+    st[0] += 1;
+    st[1] += (uint64_t)pick_hits;
+    st[2] += (uint64_t)(P - pick_hits);
+    st[3] += (uint64_t)nH;
+    st[4] += (uint64_t)nM;
+    st[5] += (uint64_t)n_evict;
+    st[6] += (uint64_t)nM * a.expert_bytes;
+    st[7] += 1;
+    if (a.mailbox) {
+      a.mailbox->hdr = h;
+      int32_t *mub = reinterpret_cast<int32_t *>(a.mailbox + 1);
+      mub[0] = 0;
+      mub[1] = n_units;
+    }
+  }
+  if (a.mailbox) {
+    int32_t *mub = reinterpret_cast<int32_t *>(a.mailbox + 1);
+    MissItem *mm = reinterpret_cast<MissItem *>(mub + a.mailbox_stage_cap);
+    if (miss) mm[mr] = MissItem{e, vslot, evicted, 0};
+    __threadfence_system();
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_system();
+      a.mailbox->seq = a.seq;
+      __threadfence_system();
+    }
+  }
+}
+
 }  // namespace
 
 size_t plan_smem_bytes(int E, int S) {
@@ -442,7 +615,16 @@ size_t plan_smem_bytes(int E, int S) {
   return b + 64;
 }
 
+bool plan_small_ok(int T, int E, int k, int S) {
+  const int P = T * k;
+  return P <= 32 && S <= kSmallMaxSlots && (E < P ? E : P) <= S;
+}
+
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
+  if (plan_small_ok(a.T, a.E, a.k, a.S)) {
+    plan_small_kernel<<<1, 32, 0, st>>>(a);
+    return cudaGetLastError();
+  }
   const size_t smem = plan_smem_bytes(a.E, a.S);
   static size_t cur = 0;
   const cudaError_t e = ensure_dyn_smem(plan_kernel, smem, cur);
