@@ -574,22 +574,6 @@ __global__ void __launch_bounds__(kThreads) fused_miss_kernel(FusedMissJob j) {
                              ? j.src_base + j.src_layer_off + (uint64_t)mi.expert * j.src_expert_stride
                              : j.src_base + (uint64_t)m * j.src_slot_stride;
     uint8_t *dst = j.slots + (uint64_t)mi.slot * j.slot_stride;
-    if (!is_gu) {
-      // wait until every gate/up tile of this expert has produced h
-      if (tid == 0) {
-        int ok = 0;
-        for (uint32_t i = 0; i < kSpinLimit; ++i) {
-          if (ld_acquire(&j.sync[1 + m]) >= tF) { ok = 1; break; }
-          __nanosleep(64);
-        }
-        s_ok = ok;
-      }
-      __syncthreads();
-      if (!s_ok) {
-        flag_error(j.err, 3);
-        return;
-      }
-    }
     const int nb = is_gu ? nbH : nbF;
     const int nmat = is_gu ? 2 : 1;
     // canonical rows [32t, 32t+32) of each matrix of this item
@@ -603,6 +587,23 @@ __global__ void __launch_bounds__(kThreads) fused_miss_kernel(FusedMissJob j) {
         cp_async16(canon + mm * tile_bytes + 16 * i, src + 16 * i);
     }
     cp_async_commit();
+    if (!is_gu) {
+      // the tile is on its way; h of this expert needs all its gate/up tiles
+      if (tid == 0) {
+        int ok = 0;
+        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+          if (ld_acquire(&j.sync[1 + m]) >= tF) { ok = 1; break; }
+          __nanosleep(64);
+        }
+        s_ok = ok;
+      }
+      __syncthreads();
+      if (!s_ok) {
+        flag_error(j.err, 3);
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        return;
+      }
+    }
     if (tid < n) rows[tid] = is_gu ? j.perm[it.pair_begin + tid] / j.k : j.perm[it.pair_begin + tid];
     __syncthreads();
     const int K = 32 * nb;

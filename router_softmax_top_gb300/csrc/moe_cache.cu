@@ -556,7 +556,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     ra.stage = 0;
     {
       Launch l(c, K_FUSED, c->side);
-      const int grid = std::max(1, std::min(96, nmiss_max * (g.ffn / 32 + g.hidden / 32)));
+      const int grid = std::max(1, std::min(128, nmiss_max * (g.ffn / 32 + g.hidden / 32)));
       if (launch_fused_miss(fa, ra, c->d_sync, grid, c->side) != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (cudaEventRecord(c->ev_up[0], c->side) != cudaSuccess) return MOE_ERR_CUDA;

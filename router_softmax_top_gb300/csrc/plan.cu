@@ -445,6 +445,16 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const int lane = threadIdx.x;
   __shared__ int s_bad;
   __shared__ uint32_t s_pinned[kSmallMaxSlots / 32];
+  __shared__ int s_se[kSmallMaxSlots];
+  __shared__ unsigned long long s_st[kSmallMaxSlots];
+  __shared__ int s_es[kMaxExperts];
+  // the whole per-layer state in one round of loads, issued before the router
+  for (int i = lane; i < S; i += 32) {
+    s_se[i] = a.slot_expert[i];
+    s_st[i] = a.slot_stamp[i];
+  }
+  for (int i = lane; i < E; i += 32) s_es[i] = a.expert_slot[i];
+  const unsigned long long now = *a.clock + 1ull;
   if (lane == 0) s_bad = 0;
   if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
   a.sync[lane] = 0;  // P <= 32: 33 counters
@@ -459,7 +469,6 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     write_error(a);
     return;
   }
-  const unsigned long long now = *a.clock + 1ull;
 
   // distinct experts: one leader lane per expert
   const bool act = lane < P;
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const int leader = __ffs(same) - 1;
   const bool lead = act && leader == lane;
   const int cnt = __popc(same);
-  const int es0 = lead ? a.expert_slot[e] : -1;
+  const int es0 = lead ? s_es[e] : -1;
   const bool hit = lead && es0 >= 0, miss = lead && es0 < 0;
   const unsigned hmask = __ballot_sync(F, hit), mmask = __ballot_sync(F, miss);
   const int nH = __popc(hmask), nM = __popc(mmask), nU = nH + nM;
@@ -491,9 +500,9 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     key[c] = ~0ull;
     const int sl = c * 32 + lane;
     if (c < nch && sl < S && !((s_pinned[c] >> lane) & 1u)) {
-      const int se = a.slot_expert[sl];
+      const int se = s_se[sl];
       key[c] = se < 0 ? (unsigned long long)sl
-                      : (1ull << 62) | ((unsigned long long)a.slot_stamp[sl] << 11) | (unsigned)sl;
+                      : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
     }
   }
   int my_victim = -1;  // lane r holds the victim of miss rank r
@@ -516,7 +525,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   }
   const int vslot = __shfl_sync(F, my_victim, miss ? mr : 0);
   const int my_slot = hit ? es0 : (miss ? vslot : -1);
-  const int evicted = miss ? a.slot_expert[vslot] : -1;
+  const int evicted = miss ? s_se[vslot] : -1;
   const int n_evict = __popc(__ballot_sync(F, miss && evicted >= 0));
   __syncwarp();
 
