@@ -185,6 +185,33 @@ int moe_cache_probe_h2d(moe_cache *c, int32_t iters, double *gbps);
 /* Bytes of one expert block (3 * F * H / 32 * 18) and of one device slot. */
 uint64_t moe_expert_bytes(int32_t hidden, int32_t ffn);
 
+/*
+ * One expert's Q4_0 SwiGLU FFN on up to 8 tokens, allocating nothing.
+ * (No counterpart on the pages: an addition for callers that cannot allocate.)
+ * Callers that cannot call cudaMalloc -- code inside a CUDA graph being
+ * captured, real-time or signal-handling paths that must not block on an
+ * allocator, plugins that do not own the process's memory pool -- pass their
+ * inputs and outputs and get y without any per-call or per-handle allocation:
+ * the only intermediate (h, the tokens' SwiGLU activations, and two work
+ * counters) lives in a fixed array compiled into the library, 128 KiB + 256 B
+ * on every GPU that loads it, held until the process exits.
+ *   d_expert_block: one canonical expert block [gate | up | down] (layout as
+ *                   above), in device memory or mapped pinned host memory,
+ *                   16-byte aligned, 3 * ffn * hidden / 32 * 18 bytes.
+ *   d_x: device fp32 [n_tokens, hidden]; d_y: device fp32 [n_tokens, hidden],
+ *        overwritten with y_t = W_down (silu(W_gate x_t) * (W_up x_t)).
+ * Limits: 0 <= n_tokens <= 8 (0 = no-op), hidden and ffn multiples of 64 and
+ * <= 4096; beyond them MOE_ERR_UNSUPPORTED.  Null or misaligned pointers:
+ * MOE_ERR_INVALID_ARG.  Stream-ordered on cuda_stream.
+ * All calls on a device share the fixed array and its contents persist between
+ * calls (the counters are cleared at the start of each call): calls that
+ * overlap on the GPU race and must be serialised by the caller.  The first
+ * call on each device looks up the array's device address (with that device
+ * current); make that first call before any stream capture.
+ */
+int moe_expert_ffn_static(const void *d_expert_block, int32_t hidden, int32_t ffn,
+                          const float *d_x, int32_t n_tokens, float *d_y, void *cuda_stream);
+
 /* Number of kernel launches the library issued since init (all streams). */
 uint64_t moe_cache_launch_count(const moe_cache *c);
 

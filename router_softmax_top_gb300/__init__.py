@@ -32,7 +32,7 @@ MOE_FILL_PULL = 1
 EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_stats",
            "moe_layer_last_plan", "moe_cache_set_timing", "moe_cache_timing",
            "moe_cache_probe_h2d", "moe_expert_bytes", "moe_cache_launch_count",
-           "moe_cache_destroy", "moe_strerror")
+           "moe_cache_destroy", "moe_strerror", "moe_expert_ffn_static")
 
 
 class MoeCacheConfig(ctypes.Structure):
@@ -106,6 +106,8 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_destroy.argtypes = [vp]
         L.moe_strerror.restype = ctypes.c_char_p
         L.moe_strerror.argtypes = [ctypes.c_int]
+        L.moe_expert_ffn_static.restype = ctypes.c_int
+        L.moe_expert_ffn_static.argtypes = [vp, i32, i32, vp, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -158,6 +160,15 @@ def moe_cache_stats(handle, layer: int = -1) -> dict:
 
 def moe_cache_destroy(handle) -> None:
     lib().moe_cache_destroy(handle)
+
+
+def moe_expert_ffn_static(d_expert_block: int, hidden: int, ffn: int, d_x: int, n_tokens: int,
+                          d_y: int, stream=None) -> int:
+    """One expert's FFN on up to 8 tokens with no allocation (for callers that cannot
+    allocate, e.g. during graph capture); returns the status code."""
+    return int(lib().moe_expert_ffn_static(ctypes.c_void_p(d_expert_block), hidden, ffn,
+                                           ctypes.c_void_p(d_x), n_tokens, ctypes.c_void_p(d_y),
+                                           _stream_handle(stream)))
 
 
 # ------------------------------------------------------- tensor-level API
