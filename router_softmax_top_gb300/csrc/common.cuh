@@ -16,6 +16,7 @@ constexpr int kPlanThreads = 256;
 constexpr int kNStat = 9;  // calls, pick_hits, pick_misses, unique_hits, unique_misses,
                            // evictions, bytes_uploaded, stages, staged_calls
 constexpr int kTokPerUnit = 8;  // tokens of one expert handled by one GEMV work unit
+constexpr int kGemmN = 128;     // routed pairs of one expert per tensor-core GEMM tile
 
 // ------------------------------------------------------------ plan records
 // Header of one call's plan, written by the plan kernel into device scratch and
@@ -32,7 +33,8 @@ struct PlanHdr {
   int32_t pick_hits;
   int32_t pick_misses;
   int32_t hit_units;  // GEMV units of the stage-0 hits: [0, hit_units)
-  int32_t pad[5];
+  int32_t hit_gunits; // GEMM units of the stage-0 hits: [0, hit_gunits)
+  int32_t pad[4];
 };
 
 // A work item = one distinct expert of the call.  Items are ordered: stage-0
@@ -139,6 +141,8 @@ struct PlanArgs {
   WorkItem *items;    // [min(E, T*k)]
   WorkUnit *units;    // [min(E,T*k) + T*k/kTokPerUnit + 1]
   int32_t *unit_begin;  // [n_stages + 1] (capacity min(E,T*k) + 2)
+  WorkUnit *gunits;     // GEMM units (up to kGemmN pairs of one item), item order
+  int32_t *gunit_begin; // [n_stages + 1]
   MissItem *miss;     // [min(E, T*k)]
   PlanHdr *hdr;
   int32_t *err_flag;  // sticky device error word of the handle
@@ -204,6 +208,13 @@ cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t
 cudaError_t launch_fused_miss(const FfnArgs &a, const RepackArgs &r, int32_t *sync, int grid,
                               cudaStream_t st);
 bool fused_miss_supported(int H, int F);
+// Tensor-core grouped GEMM (bf16 activations): gate/up -> h16 (bf16), down -> y.
+cudaError_t launch_gemm_gateup(const FfnArgs &a, const __nv_bfloat16 *x, const WorkUnit *gunits,
+                               const int32_t *gunit_begin, __nv_bfloat16 *h16, int range_kind, int stage,
+                               int max_gunits, cudaStream_t st);
+cudaError_t launch_gemm_down(const FfnArgs &a, const __nv_bfloat16 *h16, const WorkUnit *gunits,
+                             const int32_t *gunit_begin, int range_kind, int stage, int max_gunits,
+                             cudaStream_t st);
 
 enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,
                   K_GATHER, K_MEMCPY, K_FUSED, K_NKINDS };

@@ -65,6 +65,10 @@ struct moe_cache {
   MissItem *d_miss = nullptr;
   PlanHdr *d_hdr = nullptr;
   int32_t *d_sync = nullptr;
+  WorkUnit *d_gunits = nullptr;
+  int32_t *d_gunit_begin = nullptr;
+  __nv_bfloat16 *d_h16 = nullptr;
+  int maxGunits = 0;
   uint8_t *d_staging = nullptr;
   int staging_blocks = 0;
 
@@ -212,6 +216,9 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_miss);
   cudaFree(c->d_hdr);
   cudaFree(c->d_sync);
+  cudaFree(c->d_gunits);
+  cudaFree(c->d_gunit_begin);
+  cudaFree(c->d_h16);
   cudaFree(c->d_staging);
   if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
   if (c->h_err) cudaFreeHost(c->h_err);
@@ -337,6 +344,11 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_miss, c->maxU) == cudaSuccess;
   ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
   ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 33) == cudaSuccess;
+  c->maxGunits = c->maxU + (c->maxP + kGemmN - 1) / kGemmN + 1;
+  ok = ok && dalloc(&c->d_gunits, c->maxGunits) == cudaSuccess;
+  ok = ok && dalloc(&c->d_gunit_begin, c->maxStages + 1) == cudaSuccess;
+  if (ok && cfg->gemm_min_tokens > 0 && cfg->act_dtype == 1)
+    ok = dalloc(&c->d_h16, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
   if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
     c->staging_blocks = std::min(S, c->maxU);
     ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess;
@@ -409,7 +421,9 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   const int P = T * k;
   const int maxU = std::min(E, P);
   const int maxUnits = maxU + (P + kTokPerUnit - 1) / kTokPerUnit;
-  const bool need_host = g.fill_mode == MOE_FILL_MEMCPY || maxU > S;
+  const bool use_gemm = g.gemm_min_tokens > 0 && T >= g.gemm_min_tokens && g.act_dtype == 1 &&
+                        c->d_h16 != nullptr;
+  const bool need_host = g.fill_mode == MOE_FILL_MEMCPY || maxU > S || use_gemm;
 
   c->seq += 1;
   if (c->seq == 0) c->seq = 1;
@@ -434,6 +448,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.items = c->d_items;
   pa.units = c->d_units;
   pa.unit_begin = c->d_unit_begin;
+  pa.gunits = c->d_gunits;
+  pa.gunit_begin = c->d_gunit_begin;
   pa.miss = c->d_miss;
   pa.hdr = c->d_hdr;
   pa.err_flag = c->d_err;
@@ -584,6 +600,31 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       MOE_LAUNCH(K_DOWN, launch_down(fa, 2, 0, maxUnits, st));
       MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
     }
+  } else if (use_gemm) {
+    // tensor-core grouped GEMM; stage-0 hits start before the copies are issued
+    const int maxG = std::min(c->maxGunits, maxU + (P + kGemmN - 1) / kGemmN + 1);
+    const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(d_x);
+    MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(fa, xb, c->d_gunits, c->d_gunit_begin, c->d_h16, 0, 0, maxG, st));
+    int rc = wait_mailbox(c, c->seq, st);
+    if (rc != MOE_OK) return poison(c, rc);
+    const PlanHdr hdr = c->h_mail->hdr;
+    if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
+    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss;
+    if (n_st < 1 || n_st > c->maxStages - 1) return poison(c, MOE_ERR_CUDA);
+    for (int j = 0; j < n_st; ++j) {
+      const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
+      const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
+      if (mhi > mlo) {
+        rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+        if (rc != MOE_OK) return poison(c, rc);
+      }
+      const int sg = std::min(maxG, S + (P + kGemmN - 1) / kGemmN + 1);  // units of one stage, bound
+      MOE_LAUNCH(K_GEMM_GATEUP,
+                 launch_gemm_gateup(fa, xb, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
+      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fa, c->d_h16, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
+      if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+    }
+    MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
   } else {
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
     int rc = wait_mailbox(c, c->seq, st);

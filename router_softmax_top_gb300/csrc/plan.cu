@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   long long *itm = take64(E + 1);  // per item: pairs | units << 32, then its exclusive scan
   long long *ws64 = take64(NW + 2);
   int *cnt = take(E), *es0 = take(E), *code = take(E), *e_slot = take(E), *e_stage = take(E);
-  int *M = take(E), *new_es = take(E), *item_of = take(E);
+  int *M = take(E), *new_es = take(E), *item_of = take(E), *gitm = take(E + 1);
   int *se0 = take(S), *vpos = take(S), *occ0 = take(S), *touched = take(S), *victim = take(S);
   int *wcnt = take(NW * E);
   int *ws = take(NW + 2);
@@ -311,9 +311,15 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     itm[it] = (long long)cnt[e] | (units << 32);
   }
   __syncthreads();
+  for (int e = tid; e < E; e += NT) {
+    const int it = item_of[e];
+    if (it >= 0) gitm[it] = (cnt[e] + kGemmN - 1) / kGemmN;
+  }
   const long long tot_iu = block_scan_array<long long>(itm, nU, ws64);
   const int n_units = (int)(tot_iu >> 32);
   if (tid == 0) itm[nU] = tot_iu;
+  const int n_gunits = block_scan_array<int>(gitm, nU, ws);
+  if (tid == 0) gitm[nU] = n_gunits;
   __syncthreads();
 
   // ---- H. items, units, stage ranges; perm = stable counting sort by item
@@ -338,12 +344,23 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
       u.stage = w.stage;
       a.units[u0 + j] = u;
     }
+    const int g0 = gitm[it], ngu = (cnt[e] + kGemmN - 1) / kGemmN;
+    for (int j = 0; j < ngu; ++j) {
+      WorkUnit u;
+      u.item = it;
+      u.pair_begin = w.pair_begin + j * kGemmN;
+      u.pair_count = min(kGemmN, cnt[e] - j * kGemmN);
+      u.stage = w.stage;
+      a.gunits[g0 + j] = u;
+    }
   }
   for (int j = tid; j <= n_stages; j += NT) {
     const int first_item = (j == 0) ? 0 : min(nU, nH + n0 + (j - 1) * S);
     a.unit_begin[j] = (int)(itm[first_item] >> 32);
+    a.gunit_begin[j] = gitm[first_item];
   }
   const int hit_units = (int)(itm[nH] >> 32);
+  const int hit_gunits = gitm[nH];
 
   const int chunk = (P + NW - 1) / NW;
   const int c0 = warp * chunk, c1 = min(P, c0 + chunk);
@@ -399,6 +416,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     h.pick_hits = pick_hits;
     h.pick_misses = P - pick_hits;
     h.hit_units = hit_units;
+    h.hit_gunits = hit_gunits;
     *a.hdr = h;
     *a.clock = now;
     uint64_t *st = a.stats;
@@ -563,12 +581,15 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     a.items[item] = WorkItem{e, my_slot, 0, miss ? 1 : 0, pb, cnt};
     for (int j = 0; j < ucount; ++j)
       a.units[ub + j] = WorkUnit{item, pb + j * kTokPerUnit, min(kTokPerUnit, cnt - j * kTokPerUnit), 0};
+    a.gunits[item] = WorkUnit{item, pb, cnt, 0};  // at most 32 pairs: one GEMM unit per item
   }
   const int ppb = __shfl_sync(F, pb, leader);
   if (act) a.perm[ppb + __popc(same & ((1u << lane) - 1u))] = lane;
   if (lane == 0) {
     a.unit_begin[0] = 0;
     a.unit_begin[1] = n_units;
+    a.gunit_begin[0] = 0;
+    a.gunit_begin[1] = nU;
     PlanHdr h = {};
     h.n_unique = nU;
     h.n_hits = nH;
@@ -580,6 +601,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     h.pick_hits = pick_hits;
     h.pick_misses = P - pick_hits;
     h.hit_units = hit_units;
+    h.hit_gunits = nH;
     *a.hdr = h;
     *a.clock = now;
     uint64_t *st = a.stats;
@@ -618,7 +640,7 @@ size_t plan_smem_bytes(int E, int S) {
   auto r8 = [](size_t n) { return 8 * ((n + 1) / 2 * 2); };
   auto r4 = [](size_t n) { return 4 * ((n + 3) / 4 * 4); };
   size_t b = r8(S) + r8(E + 1) + r8(NW + 2);
-  b += 8 * r4(E);
+  b += 8 * r4(E) + r4(E + 1);
   b += 5 * r4(S);
   b += r4((size_t)NW * E) + r4(NW + 2) + r4(8);
   return b + 64;
