@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--fill", default="memcpy", choices=["memcpy", "pull"])
-    ap.add_argument("--workload", default="decode", choices=["decode"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--cpu-sample-steps", type=int, default=4)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -197,11 +197,113 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ prefill
+def prefill_config(sh, fill):
+    return {
+        "workload": (f"prefill: {sh.L} MoE layers, {sh.E} experts/layer, top-{sh.k}, hidden {sh.H}, "
+                     f"expert FFN {sh.F}, Q4_0 experts in pinned host RAM, {sh.S} slots/layer, "
+                     f"512 tokens per batch through the tensor-core grouped GEMM, Zipf({sh.zipf}) routing "
+                     f"with {int(sh.sticky * 100)}% of picks copied from the previous token, bf16 "
+                     f"activations N(0,1)"),
+        "layers": sh.L, "experts": sh.E, "top_k": sh.k, "hidden": sh.H, "ffn": sh.F,
+        "slots_per_layer": sh.S, "tokens_per_step": 512, "fill_mode": fill,
+        "l2": "inputs larger than L2: each batch streams the stage-wise expert weights and activations "
+              "(~1 GB per layer-batch) through HBM",
+    }
+
+
+def run_prefill(args):
+    import torch
+
+    import router_softmax_top_gb300 as moe
+    sh = synth.PREFILL
+    T = 512
+    W, K = max(3, args.warmup), args.steps
+    torch.cuda.set_device(0)
+    eb = sh.expert_bytes
+    store = torch.empty(sh.L * sh.E * eb, dtype=torch.uint8, pin_memory=True)
+    synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
+    nb = W + 2 * K
+    _, logits_h, x_h = synth.batch_inputs(sh, nb, T, seed=0, act="bf16")
+    logits_d = torch.from_numpy(logits_h).cuda()
+    x_d = torch.from_numpy(x_h.view(np.int16)).cuda().view(torch.bfloat16)
+    out_d = torch.empty((sh.L, T, sh.H), dtype=torch.float32, device="cuda")
+    fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
+    cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
+                         slots_per_layer=sh.S, max_tokens=T, store=store, act_dtype="bf16",
+                         fill_mode=fill, gemm_min_tokens=64, timeout_us=60_000_000)
+    h2d_gbps = cache.probe_h2d(24)
+    fwd = moe.lib().moe_layer_forward
+    sh_ = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+    def run(b0, b1):
+        for b in range(b0, b1):
+            for l in range(sh.L):
+                rc = fwd(cache.handle, l, ctypes.c_void_p(logits_d[b, l].data_ptr()),
+                         ctypes.c_void_p(x_d[b, l].data_ptr()), T, ctypes.c_void_p(out_d[l].data_ptr()), sh_)
+                if rc != 0:
+                    raise moe.MoeError(rc, f"moe_layer_forward batch {b} layer {l}")
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    run(0, W)
+    torch.cuda.synchronize()
+    st1 = cache.stats(-1)
+    clocks = ClockSampler(0)
+    clocks.start()
+    e0.record()
+    run(W, W + K)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    clk = clocks.stop()
+    st2 = cache.stats(-1)
+    cache.set_timing(True)
+    run(W + K, W + 2 * K)
+    torch.cuda.synchronize()
+    kt = cache.timing()
+    cache.set_timing(False)
+    st3 = cache.stats(-1)
+    hbm_peak, bf16_peak, peak_kind = measured_peaks()
+    d = {k2: st2[k2] - st1[k2] for k2 in ("pick_hits", "pick_misses", "unique_hits", "unique_misses")}
+    dk = {k2: st3[k2] - st2[k2] for k2 in ("pick_hits", "pick_misses", "unique_hits", "unique_misses")}
+    pairs_k = dk["pick_hits"] + dk["pick_misses"]
+    flops_gu = pairs_k * 2.0 * 2 * sh.H * sh.F
+    flops_dn = pairs_k * 2.0 * sh.H * sh.F
+    g_gu = kt.get("gemm_gateup", {"ms": 0.0, "launches": 0})
+    g_dn = kt.get("gemm_down", {"ms": 0.0, "launches": 0})
+    ach = flops_gu / (g_gu["ms"] * 1e-3) / 1e12 if g_gu["ms"] else 0.0
+    roof = {"kernel": "gemm_gateup", "bound": "tensor", "achieved": ach, "peak": bf16_peak,
+            "unit": "TFLOP/s", "frac": ach / bf16_peak, "traffic": None, "peak_source": peak_kind,
+            "launches": g_gu["launches"], "avg_launch_us": 1e3 * g_gu["ms"] / max(1, g_gu["launches"]),
+            "down_tflops": flops_dn / (g_dn["ms"] * 1e-3) / 1e12 if g_dn["ms"] else 0.0}
+    flops = (d["pick_hits"] + d["pick_misses"]) * 2.0 * 3 * sh.H * sh.F
+    t_roof = (max(flops / (bf16_peak * 1e12), d["unique_hits"] * eb / (hbm_peak * 1e9)) +
+              d["unique_misses"] * eb / (h2d_gbps * 1e9))
+    value = K * T / (ms * 1e-3)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic", "config": prefill_config(sh, args.fill),
+            "hit_rate": {"pick": d["pick_hits"] / max(1, d["pick_hits"] + d["pick_misses"]),
+                         "unique": d["unique_hits"] / max(1, d["unique_hits"] + d["unique_misses"])},
+            "roofline": roof,
+            "step_roofline": {"bound": "max(tensor, hbm) + h2d", "t_roof_ms": 1e3 * t_roof, "t_meas_ms": ms,
+                              "frac": t_roof / (ms * 1e-3), "h2d_gbs_measured": h2d_gbps,
+                              "tflop_per_batch": flops / K / 1e12},
+            "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kt.items()
+                        if v["launches"]},
+            "clocks": clk}
+    cache.close()
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------ our arm
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.workload == "prefill":
+        run_prefill(args)
         return
     import torch
     import torch.distributed as dist

@@ -7,9 +7,11 @@
 // One CTA computes one output tile: 128 output features (rows of W) x up to
 // kGemmN routed pairs of one expert, looping over the input dimension in
 // chunks of 64.  Roles (8 warps):
-//   warps 0-3  dequantise the Q4_0 rows of the tile chunk (slot, tiled layout)
-//              to bf16, w = (q - 8) * d rounded to bf16, into shared memory in
-//              the 128-byte-swizzled K-major layout the MMA reads;
+//   warp 7     brings the chunk's Q4_0 tile into shared memory with bulk
+//              copies (4 contiguous runs of nibbles and of scales per matrix);
+//   warps 0-3  dequantise it to bf16, w = (q - 8) * bf16(d) rounded to bf16,
+//              built with bf16x2 operations from the nibble bits, into shared
+//              memory in the 128-byte-swizzled K-major layout the MMA reads;
 //   warps 4-5  gather the pairs' input rows (bf16) with cp.async into the same
 //              layout;
 //   warp 6     one thread issues the MMAs (gate and up share the inputs and
@@ -124,9 +126,19 @@ __device__ __forceinline__ bool gunit_range(const PlanHdr *h, const int32_t *gb,
   return true;
 }
 
+constexpr int kRawStages = 4;  // raw Q4_0 chunks in flight (bulk copies)
+
 template <int NMAT>
-constexpr size_t gemm_stage_bytes() {
+constexpr size_t gemm_stage_bytes() {  // bf16 A (per matrix) + B tiles of one K chunk
   return (size_t)NMAT * kGemmM * 128 + (size_t)kGemmN * 128;
+}
+template <int NMAT>
+constexpr size_t raw_stage_bytes() {   // Q4_0 of one chunk: 4 row tiles x 2 blocks, per matrix
+  return (size_t)NMAT * (4 * 1024 + 4 * 128);
+}
+template <int NMAT>
+constexpr size_t gemm_smem_bytes() {
+  return kStages * gemm_stage_bytes<NMAT>() + kRawStages * raw_stage_bytes<NMAT>() + 1024;
 }
 
 template <int NMAT>
@@ -137,15 +149,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
   if (gu >= hi) return;
   const WorkUnit wu = j.gunits[gu];
   const WorkItem it = j.items[wu.item];
-  const int n = wu.pair_count;  // 1..kGemmN
+  const int n = wu.pair_count;                       // 1..kGemmN
+  const int nr = (n + 15) & ~15;                     // MMA N: pairs rounded up to 16
   const int m0 = blockIdx.x * kGemmM;
-  const int nb = j.nb, n_chunks = nb / 2;  // 64 inputs = 2 blocks per chunk
+  const int rt0 = m0 >> 5, n_rt = min(4, (j.R >> 5) - rt0);  // valid 32-row tiles
+  const int nb = j.nb, n_chunks = nb / 2;            // 64 inputs = 2 blocks per chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char *sm =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], done;
+  unsigned char *raw = sm + kStages * gemm_stage_bytes<NMAT>();
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], rfull[kRawStages], rempty[kRawStages], done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_rows[kGemmN];
   __shared__ int s_fail;
@@ -156,6 +171,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
     for (int s = 0; s < kStages; ++s) {
       g_mbar_init(&full[s], kProducers);
       g_mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < kRawStages; ++s) {
+      g_mbar_init(&rfull[s], 1);
+      g_mbar_init(&rempty[s], 128);
     }
     g_mbar_init(&done, 1);
     s_fail = 0;
@@ -173,60 +192,106 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
   const uint32_t tmem = tmem_base;
   const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
 
-  if (warp < 4) {
-    // ---- A producers: row r of the tile, both matrices
-    const int r = tid;               // 0..127
-    const int row = m0 + r;
-    const bool valid = row < j.R;
-    const int rt = row >> 5, ln = row & 31;
+  if (warp == 7) {
+    // ---- raw Q4_0 loader: per chunk and matrix, 4 contiguous 1 KB nibble runs
+    // (32 rows x blocks 2c, 2c+1 of one row tile) and 4 runs of 128 B scales
+    if (lane == 0) {
+      for (int c = 0; c < n_chunks; ++c) {
+        const int s = c % kRawStages;
+        if (c >= kRawStages && !g_mbar_wait(&rempty[s], (uint32_t)((c / kRawStages) - 1) & 1u)) {
+          s_fail = 1;
+          break;
+        }
+        unsigned char *rs = raw + (size_t)s * raw_stage_bytes<NMAT>();
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(gsa(&rfull[s])),
+                     "r"((uint32_t)(NMAT * n_rt * (1024 + 128)))
+                     : "memory");
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+          const MatLayout &L = m == 0 ? j.m0 : j.m1;
+          for (int q = 0; q < n_rt; ++q) {
+            const uint64_t e = ((uint64_t)(rt0 + q) * nb + 2 * c) * 32;
+            unsigned char *dn = rs + m * (4 * 1024 + 4 * 128) + q * 1024;
+            unsigned char *ds = rs + m * (4 * 1024 + 4 * 128) + 4 * 1024 + q * 128;
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
+                    gsa(dn)),
+                "l"(slot + L.nib_off + e * 16), "r"(gsa(&rfull[s]))
+                : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 128, [%2];" ::"r"(
+                    gsa(ds)),
+                "l"(slot + L.sc_off + e * 2), "r"(gsa(&rfull[s]))
+                : "memory");
+          }
+        }
+      }
+    }
+  } else if (warp < 4) {
+    // ---- dequant: row r of the tile, both matrices, raw smem -> swizzled bf16
+    const int r = tid;
+    const bool valid = (r >> 5) < n_rt;
     for (int c = 0; c < n_chunks; ++c) {
-      const int s = c % kStages;
+      const int s = c % kStages, rsi = c % kRawStages;
       if (c >= kStages && !g_mbar_wait(&empty[s], (uint32_t)((c / kStages) - 1) & 1u)) { s_fail = 1; break; }
+      if (!g_mbar_wait(&rfull[rsi], (uint32_t)(c / kRawStages) & 1u)) { s_fail = 1; break; }
+      const unsigned char *rs = raw + (size_t)rsi * raw_stage_bytes<NMAT>();
       unsigned char *st = sm + (size_t)s * gemm_stage_bytes<NMAT>();
 #pragma unroll
       for (int m = 0; m < NMAT; ++m) {
-        const MatLayout &L = m == 0 ? j.m0 : j.m1;
         unsigned char *a = st + (size_t)m * kGemmM * 128;
 #pragma unroll
         for (int bi = 0; bi < 2; ++bi) {
           uint4 q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
           float d = 0.f;
           if (valid) {
-            const uint64_t e = tile_elem(row, 2 * c + bi, nb);
-            q = reinterpret_cast<const uint4 *>(slot + L.nib_off)[e];
-            d = __half2float(__ushort_as_half(reinterpret_cast<const unsigned short *>(slot + L.sc_off)[e]));
+            const unsigned char *rm = rs + m * (4 * 1024 + 4 * 128);
+            q = *reinterpret_cast<const uint4 *>(rm + (r >> 5) * 1024 + bi * 512 + (r & 31) * 16);
+            d = __half2float(__ushort_as_half(
+                *reinterpret_cast<const unsigned short *>(rm + 4 * 1024 + (r >> 5) * 128 + bi * 64 + (r & 31) * 2)));
           }
+          // two nibbles side by side under the bf16 exponent of 128: 0x4300|q is
+          // 128 + q exactly; minus 136 gives q - 8 exactly; times d rounds once
+          const __nv_bfloat162 d2 = __float2bfloat162_rn(d);
+          const __nv_bfloat162 k136 = __float2bfloat162_rn(136.f);
           const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-          // values 0..15: low nibbles of bytes 0..15; values 16..31: high nibbles
-          uint32_t lo_pk[8], hi_pk[8];
+          uint32_t lo_pk[8], hi_pk[8];  // values 0..15 (low nibbles), 16..31 (high nibbles)
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
+            const uint32_t p01 = __byte_perm(w[i], 0u, 0x4140u);  // bytes 4i, 4i+1 in the two halves
+            const uint32_t p23 = __byte_perm(w[i], 0u, 0x4342u);  // bytes 4i+2, 4i+3
+            const uint32_t v[4] = {(p01 & 0x000F000Fu) | 0x43004300u, (p23 & 0x000F000Fu) | 0x43004300u,
+                                   ((p01 >> 4) & 0x000F000Fu) | 0x43004300u,
+                                   ((p23 >> 4) & 0x000F000Fu) | 0x43004300u};
+            __nv_bfloat162 o[4];
 #pragma unroll
-            for (int b2 = 0; b2 < 2; ++b2) {
-              const uint32_t by0 = (w[i] >> (16 * b2)) & 0xFFu, by1 = (w[i] >> (16 * b2 + 8)) & 0xFFu;
-              lo_pk[2 * i + b2] = pack_bf16((float)((int)(by0 & 15u) - 8) * d, (float)((int)(by1 & 15u) - 8) * d);
-              hi_pk[2 * i + b2] = pack_bf16((float)((int)(by0 >> 4) - 8) * d, (float)((int)(by1 >> 4) - 8) * d);
-            }
+            for (int z = 0; z < 4; ++z)
+              o[z] = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&v[z]), k136), d2);
+            lo_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[0]);
+            lo_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[1]);
+            hi_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[2]);
+            hi_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[3]);
           }
-          // 16-byte chunks 4bi..4bi+3 of this row: values 8cc..8cc+7 of the block
           *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 0)) = make_uint4(lo_pk[0], lo_pk[1], lo_pk[2], lo_pk[3]);
           *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 1)) = make_uint4(lo_pk[4], lo_pk[5], lo_pk[6], lo_pk[7]);
           *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 2)) = make_uint4(hi_pk[0], hi_pk[1], hi_pk[2], hi_pk[3]);
           *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 3)) = make_uint4(hi_pk[4], hi_pk[5], hi_pk[6], hi_pk[7]);
         }
       }
+      g_mbar_arrive(&rempty[rsi]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       g_mbar_arrive(&full[s]);
     }
   } else if (warp < 6) {
-    // ---- B producers: 64 threads gather the pairs' input rows, 8 chunks each
+    // ---- gather the pairs' input rows (nr rows, zero padding past n) with
+    // cp.async; a chunk is published once it landed
     const int t = tid - 128;  // 0..63
     const int K = 32 * nb;
     for (int c = 0; c < n_chunks; ++c) {
       const int s = c % kStages;
       if (c >= kStages && !g_mbar_wait(&empty[s], (uint32_t)((c / kStages) - 1) & 1u)) { s_fail = 1; break; }
       unsigned char *bsm = sm + (size_t)s * gemm_stage_bytes<NMAT>() + (size_t)NMAT * kGemmM * 128;
-      for (int i = t; i < kGemmN * 8; i += 64) {
+      for (int i = t; i < nr * 8; i += 64) {
         const int rr = i >> 3, cc = i & 7;
         unsigned char *dst = bsm + sw128_off(rr, cc);
         const int src_row = s_rows[rr];
@@ -237,14 +302,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
           *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
         }
       }
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      g_mbar_arrive(&full[s]);
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      // publish the previous chunk: its copies have landed once at most one
+      // group (this one) is pending.  Publishing one behind (not kStages - 1)
+      // keeps the publication of chunk c independent of the MMA of chunk c - 1.
+      if (c >= 1) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        g_mbar_arrive(&full[(c - 1) % kStages]);
+      }
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (n_chunks >= 1) g_mbar_arrive(&full[(n_chunks - 1) % kStages]);
   } else if (warp == 6) {
     // ---- MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(kGemmM, kGemmN);
+      const uint32_t idesc = idesc_bf16(kGemmM, nr);
       bool ok = true;
       for (int c = 0; c < n_chunks && ok; ++c) {
         const int s = c % kStages;
@@ -275,7 +349,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int row = m0 + tid;
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      for (int c0 = 0; c0 < kGemmN; c0 += 16) {
+      for (int c0 = 0; c0 < nr; c0 += 16) {
         float g[16], u[16];
         tmem_ld16(lane_addr + c0, g);
         if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
@@ -305,7 +379,7 @@ template <int NMAT>
 cudaError_t launch_gemm_t(const GemmJob &j, int max_gunits, cudaStream_t st) {
   if (max_gunits <= 0) return cudaSuccess;
   if (j.nb % 2) return cudaErrorInvalidValue;
-  const size_t smem = kStages * gemm_stage_bytes<NMAT>() + 1024;
+  const size_t smem = gemm_smem_bytes<NMAT>();
   static size_t cur = 0;
   const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT>, smem, cur);
   if (e != cudaSuccess) return e;
