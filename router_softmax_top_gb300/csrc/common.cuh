@@ -2,6 +2,7 @@
 // of the C ABI).
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is fetched from the driver)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -146,7 +147,8 @@ struct PlanArgs {
   MissItem *miss;     // [min(E, T*k)]
   PlanHdr *hdr;
   int32_t *err_flag;  // sticky device error word of the handle
-  int32_t *sync;      // per-call counters [min(E, T*k) + 1], zeroed here
+  int32_t *sync;      // per-call counters, the first sync_n zeroed here
+  int sync_n;
   Mailbox *mailbox;   // device alias of the mapped host mailbox, or null
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;
@@ -208,15 +210,36 @@ cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t
 cudaError_t launch_fused_miss(const FfnArgs &a, const RepackArgs &r, int32_t *sync, int grid,
                               cudaStream_t st);
 bool fused_miss_supported(int H, int F);
-// Tensor-core grouped GEMM (bf16 activations): gate/up -> h16 (bf16), down -> y.
-cudaError_t launch_gemm_gateup(const FfnArgs &a, const __nv_bfloat16 *x, const WorkUnit *gunits,
-                               const int32_t *gunit_begin, __nv_bfloat16 *h16, int range_kind, int stage,
+// Tensor-core grouped GEMM (bf16 activations).  The activations of the routed
+// pairs are first copied into pair-sorted order (xs[pos] = x[perm[pos] / k]),
+// so that the rows of one GEMM unit are contiguous and a TMA tensor copy loads
+// them; gate/up writes h16 in the same sorted order, and down writes y by pair.
+// GemmMaps: 2-D tensor maps (bf16, [rows][K], 128-byte swizzle) over one
+// sorted buffer, with boxes of 64 columns x 16, 32, 64 and 128 rows.
+struct GemmMaps {
+  CUtensorMap box[4];
+};
+cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps *out);
+cudaError_t launch_gather_sorted(const __nv_bfloat16 *x, const int32_t *perm, int P, int k, int H,
+                                 __nv_bfloat16 *xs, cudaStream_t st);
+cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const WorkUnit *gunits,
+                               const int32_t *gunit_begin, __nv_bfloat16 *h16s, int range_kind, int stage,
                                int max_gunits, cudaStream_t st);
-cudaError_t launch_gemm_down(const FfnArgs &a, const __nv_bfloat16 *h16, const WorkUnit *gunits,
+cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const WorkUnit *gunits,
                              const int32_t *gunit_begin, int range_kind, int stage, int max_gunits,
                              cudaStream_t st);
 
+// Whole expert FFN + combine of a single-stage call of at most 8 tokens with the
+// pull fill, in one persistent launch (misses read from the mapped host store
+// and written into their slots on the way).  g, u: [T*k, F] scratch.  sync:
+// [0], [1] queue heads, [2 + i] per work item, [cbase + t * H/32 + r] per token
+// and row tile (zeroed by the plan kernel).
+bool decode_layer_supported(int H, int F, int T);
+cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
+                                float *g, float *u, float *out, int32_t *sync, int cbase, int T, int n_sms,
+                                cudaStream_t st);
+
 enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,
-                  K_GATHER, K_MEMCPY, K_FUSED, K_NKINDS };
+                  K_GATHER, K_MEMCPY, K_FUSED, K_DECODE, K_NKINDS };
 
 }  // namespace moe

@@ -1,0 +1,543 @@
+// Decode layer kernel: the whole expert FFN and the weighted combine of one
+// single-stage layer call of at most 8 tokens in one persistent launch, for
+// the pull fill (the host store is read in place through its mapped address).
+//
+// Missed experts are read once from the host store over the host link and
+// written into their slots on the way ("Multi-GPU LLM Calculator: VRAM Split
+// and RAM Offload", "RAM offload": weights stream from host RAM when they do
+// not fit); cached experts are read from their slots in HBM; both are computed
+// by the same CTAs.  Work items are 32-row tiles of gate or of up, and groups
+// of up to 4 consecutive 32-row tiles of down (one input staging for 128 output
+// rows), of one expert.  Two queues hold them in dependency order: misses
+// (gate/up tiles, then down groups) and hits (likewise).  When the call has
+// misses, 24 CTAs serve the miss queue, so the host link is busy from the
+// start and no hit waits behind a tile in flight on it, then turn to the hit
+// queue; the other CTAs serve the hit queue only (a CTA's GPU-scope fence
+// also waits for its copies in flight, so a host read there would hold up
+// the publication of hit outputs).  A down group waits for the gate/up tiles
+// of its expert, which come earlier in the same queue; a CTA claims items only
+// while it runs, processes them in claim order, and takes from its second
+// queue only once its first is exhausted, so every waited-for tile is held by
+// a running CTA that reaches it.  Each CTA keeps its next items loading (bulk
+// copies, a producer warp) while its compute warps work, and a publisher warp
+// makes finished outputs visible and counts them.
+//
+// gate and up are stored separately (g, u); a down tile forms h = silu(g) * u
+// while staging its input, with the same expression the other kernels use.
+// The weighted sum over a token's picks is done by whichever down tile of
+// that token and row tile finishes last (a per-(token, tile) counter): it adds
+// the k stored y rows in ascending pick order ("The idea: cache the hot
+// experts on the GPU", step 4).  Every value is reduced in the canonical order
+// of the Q4_0 GEMV kernels, so results are bitwise those of the
+// tile-GEMV + combine path.
+#include "q4_math.cuh"
+
+namespace moe {
+namespace {
+
+using namespace q4;
+
+constexpr uint64_t kDecodeWaitNs = 2000000000ull;  // bounded waits: 2 s
+constexpr int kPubSlots = 4;
+constexpr int kDecodeThreads = kThreads + 64;     // 8 compute warps, producer, publisher
+constexpr int kHitQueue = 1 << 30;                 // claim code flag: item of the hit queue
+constexpr int kMissCtas = 48;                      // CTAs that serve the miss queue first
+
+struct DecodeJob {
+  const uint8_t *host;     // device alias of this layer's experts in the mapped host store
+  uint64_t expert_stride;  // bytes between experts in the store
+  uint8_t *slots;          // layer's slot 0
+  uint64_t slot_stride;
+  SlotLayout lay;
+  const PlanHdr *hdr;
+  const WorkItem *items;   // hits [0, nH), then misses
+  const int32_t *perm;
+  const float *w;
+  const void *x;
+  int x_bf16;
+  int T, k, H, F;
+  int DG;                  // 32-row down tiles per down item (1, 2 or 4)
+  float *g, *u;            // [T*k, F]
+  float *y;                // [T*k, H]
+  float *out;              // [T, H]
+  int32_t *sync;           // [0] miss queue head, [1] hit queue head, [2 + i] gate/up tiles done of
+                           // work item i, [cbase + t * H/32 + r] picks done of token t, row tile r
+  int cbase;
+  int32_t *err;
+};
+
+__device__ __forceinline__ uint64_t now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A claimed item: work item, matrix (0 gate, 1 up, 2 down), first 32-row tile
+// and number of tiles, source.
+struct Work {
+  int iu, mat, tile, nt;
+  bool miss;
+};
+struct QueueShape {
+  int nH, nM, tF, tH, DG, dG;  // dG = down items per expert
+  __device__ int misses() const { return nM * (2 * tF + dG); }
+  __device__ int hits() const { return nH * (2 * tF + dG); }
+};
+// Queue position -> item.  Each queue: all gate/up tiles, then all down groups.
+__device__ __forceinline__ Work decode_claim(int code, const QueueShape &q) {
+  Work w;
+  const bool hitq = code & kHitQueue;
+  const int pos = code & (kHitQueue - 1);
+  const int n_exp = hitq ? q.nH : q.nM, base = hitq ? 0 : q.nH;
+  const int A = n_exp * 2 * q.tF;
+  w.miss = !hitq;
+  if (pos < A) {
+    w.iu = base + pos / (2 * q.tF);
+    const int r = pos % (2 * q.tF);
+    w.mat = r / q.tF;
+    w.tile = r % q.tF;
+    w.nt = 1;
+  } else {
+    const int i = pos - A;
+    w.iu = base + i / q.dG;
+    w.mat = 2;
+    w.tile = (i % q.dG) * q.DG;
+    w.nt = min(q.DG, q.tH - w.tile);
+  }
+  return w;
+}
+
+__host__ __device__ inline size_t decode_slot_bytes(int H, int F, int DG) {
+  const size_t gu = (size_t)32 * (H / 32) * 18, dn = (size_t)DG * 32 * (F / 32) * 18;
+  return gu > dn ? gu : dn;  // canonical and tiled forms have the same size
+}
+// Down tiles per item: the most of 4, 2, 1 whose bytes fit a gate/up tile's
+// (one is always allowed).
+int decode_down_group(int H, int F) {
+  const size_t gu = (size_t)32 * (H / 32) * 18, dn = (size_t)32 * (F / 32) * 18;
+  for (int g = 4; g > 1; g /= 2)
+    if (g * dn <= gu) return g;
+  return 1;
+}
+size_t decode_smem(int H, int F, int T, int NB) {
+  return (size_t)NB * decode_slot_bytes(H, F, decode_down_group(H, F)) +
+         sizeof(float) * ((size_t)T * H + (size_t)T * (H / 32) + (size_t)T * F + (size_t)T * (F / 32) +
+                          (size_t)kWarps * T * 32);
+}
+constexpr size_t kDecodeSmemCap = 226 * 1024;
+
+// Compute warps (0-7) synchronise among themselves with a named barrier; the
+// producer (warp 8) and publisher (warp 9) run beside them on mbarriers.
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      const uint64_t t = now_ns();
+      if (t0 == 0) t0 = t;
+      else if (t - t0 > kDecodeWaitNs) return false;
+    }
+  }
+  return false;
+}
+
+// Block b of row `row` of the item's tiles (row = 32 * tile-in-item + lane):
+// nibbles and scale bits; a miss also writes the block's tiled form into its
+// slot (fill on the way).
+__device__ __forceinline__ void load_block(const unsigned char *buf, bool miss, int nt, int row, int b, int nb,
+                                           uint8_t *slot, const MatLayout &L, int tile0, uint4 &qv,
+                                           unsigned short &db) {
+  if (miss) {
+    qv = canon_block(buf, row, b, nb, db);
+    const uint64_t e = tile_elem(tile0 * 32 + row, b, nb);
+    reinterpret_cast<uint4 *>(slot + L.nib_off)[e] = qv;
+    reinterpret_cast<unsigned short *>(slot + L.sc_off)[e] = db;
+  } else {
+    const int i = ((row >> 5) * nb + b) * 32 + (row & 31);
+    qv = reinterpret_cast<const uint4 *>(buf)[i];
+    db = reinterpret_cast<const unsigned short *>(buf + (size_t)nt * nb * 512)[i];
+  }
+}
+
+template <int NB, int TMAX>
+__global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const DecodeJob j) {
+  const PlanHdr *hd = j.hdr;
+  if (hd->error) return;
+  QueueShape qs;
+  qs.nH = hd->n_hits;
+  qs.nM = hd->n_stage0_miss;
+  qs.tF = j.F / 32;
+  qs.tH = j.H / 32;
+  qs.DG = j.DG;
+  qs.dG = (qs.tH + j.DG - 1) / j.DG;
+  const int T = j.T, nbH = j.H / 32, nbF = j.F / 32, tH = qs.tH;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t slot_bytes = decode_slot_bytes(j.H, j.F, j.DG);
+
+  extern __shared__ __align__(128) unsigned char sm[];
+  unsigned char *ring = sm;
+  float *xs = reinterpret_cast<float *>(sm + NB * slot_bytes);  // [T][H]: the call's inputs
+  float *xsum = xs + (size_t)T * j.H;                           // [T][H/32]
+  float *hs = xsum + (size_t)T * nbH;                           // [T][F]: one down item's inputs
+  float *hsum = hs + (size_t)T * j.F;                           // [T][F/32]
+  float *red = hsum + (size_t)T * nbF;                          // [warps][T][32]
+  __shared__ __align__(8) uint64_t full[NB], empty[NB], pub[kPubSlots], pubfree[kPubSlots], published;
+  __shared__ int s_item[NB], s_pub[kPubSlots];
+  __shared__ int s_ok, s_ok_down;  // decisions of thread 0, each read after a barrier
+
+  auto mat_of = [&](int mat) -> const MatLayout & {
+    return mat == 0 ? j.lay.gate : mat == 1 ? j.lay.up : j.lay.down;
+  };
+  if (tid == 0) {
+    for (int s = 0; s < NB; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int p = 0; p < kPubSlots; ++p) {
+      mbar_init(&pub[p], kThreads);
+      mbar_init(&pubfree[p], 1);
+    }
+    mbar_init(&published, 1);
+    fence_mbar_init();
+    s_ok = 1;
+    s_ok_down = 1;
+  }
+  __syncthreads();
+
+  if (warp == kWarps) {
+    // ---- producer: claim items in order, bulk-copy each one's tiles into the ring
+    if (lane == 0) {
+      // miss CTAs serve the miss queue, then help with the hits; hit CTAs never
+      // take a miss item: a GPU-scope fence waits for the CTA's copies in
+      // flight, and one from the host link would hold up the hit outputs
+      const int n_miss_ctas = qs.nM ? min((int)gridDim.x / 3, kMissCtas) : 0;
+      const bool hit_first = (int)blockIdx.x >= n_miss_ctas;
+      bool second = false, sequential = !hit_first;
+      for (int c = 0;; ++c) {
+        const int s = c % NB;
+        if (c >= NB && !ring_wait(&empty[s], (uint32_t)((c / NB) - 1) & 1u)) {
+          // the compute warps stopped: no copy may still be landing when the CTA exits
+          flag_error(j.err, 3);
+          for (int c2 = c - NB; c2 < c; ++c2) (void)ring_wait(&full[c2 % NB], (uint32_t)(c2 / NB) & 1u);
+          break;
+        }
+        // a miss CTA claims its next item only once the previous one is
+        // published: no publication then waits for a read in flight on the host
+        // link, and a hit item it takes is never queued behind a miss
+        if (sequential && c >= 1 && !ring_wait(&published, (uint32_t)(c - 1) & 1u)) {
+          flag_error(j.err, 3);
+          s_item[s] = -1;
+          mbar_arrive(&full[s]);
+          break;
+        }
+        int code = -1;
+        for (;;) {
+          const bool hitq = hit_first != second;
+          const int size = hitq ? qs.hits() : qs.misses();
+          const int pos = size > 0 ? atomicAdd(&j.sync[hitq ? 1 : 0], 1) : size;
+          if (pos < size) {
+            code = pos | (hitq ? kHitQueue : 0);
+            break;
+          }
+          if (second || hit_first) break;
+          second = true;
+        }
+        if (code < 0) {
+          s_item[s] = -1;
+          mbar_arrive(&full[s]);
+          break;
+        }
+        if (code & kHitQueue) sequential = false;  // HBM reads only from here on
+        s_item[s] = code;
+        const Work wk = decode_claim(code, qs);
+        const WorkItem it = j.items[wk.iu];
+        const MatLayout &L = mat_of(wk.mat);
+        const int nb = L.nb;
+        unsigned char *dst = ring + (size_t)s * slot_bytes;
+        if (wk.miss) {
+          // canonical rows [32 tile, 32 (tile + nt)) of the matrix: one contiguous run
+          const uint32_t bytes = (uint32_t)(32 * nb * 18);
+          mbar_expect_tx(&full[s], bytes * wk.nt);
+          bulk_g2s(dst, j.host + (uint64_t)it.expert * j.expert_stride + L.nib_off + (uint64_t)wk.tile * bytes,
+                   bytes * wk.nt, &full[s]);
+        } else {
+          // tiled slot planes: nibbles [tiles][nb][32][16 B], then scales [tiles][nb][32]
+          const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
+          const uint32_t bn = (uint32_t)nb * 512, bs = (uint32_t)nb * 64;
+          mbar_expect_tx(&full[s], (bn + bs) * wk.nt);
+          bulk_g2s(dst, slot + L.nib_off + (uint64_t)wk.tile * bn, bn * wk.nt, &full[s]);
+          bulk_g2s(dst + (size_t)bn * wk.nt, slot + L.sc_off + (uint64_t)wk.tile * bs, bs * wk.nt, &full[s]);
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == kWarps + 1) {
+    // ---- publisher: after an item's outputs are stored, make them visible and
+    // count them; the last down tile of a (token, row tile) does its combine
+    for (int c = 0;; ++c) {
+      const int p = c % kPubSlots;
+      int ok = 1;
+      if (lane == 0) ok = ring_wait(&pub[p], (uint32_t)(c / kPubSlots) & 1u) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        if (lane == 0) flag_error(j.err, 3);
+        break;
+      }
+      (void)mbar_try_wait(&pub[p], (uint32_t)(c / kPubSlots) & 1u);  // completed phase: acquire
+      const int code = s_pub[p];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pubfree[p]);
+      if (code < 0) break;
+      const Work wk = decode_claim(code, qs);
+      const WorkItem it = j.items[wk.iu];
+      if (wk.mat != 2) {
+        if (lane == 0) {
+          __threadfence();
+          atomicAdd(&j.sync[2 + wk.iu], 1);
+        }
+      } else {
+        // bit (tt * 8 + i): pick i of this item completed row tile tile + tt
+        unsigned done_mask = 0;
+        if (lane == 0) {
+          __threadfence();
+          for (int tt = 0; tt < wk.nt; ++tt)
+            for (int i = 0; i < it.pair_count; ++i) {
+              const int t = j.perm[it.pair_begin + i] / j.k;
+              if (atomicAdd(&j.sync[j.cbase + t * tH + wk.tile + tt], 1) == j.k - 1) done_mask |= 1u << (tt * 8 + i);
+            }
+        }
+        done_mask = __shfl_sync(0xffffffffu, done_mask, 0);
+        if (done_mask) {
+          __threadfence();
+          // weighted sum over the picks of each completed (token, row tile), ascending
+          for (int tt = 0; tt < wk.nt; ++tt)
+            for (int i = 0; i < it.pair_count; ++i) {
+              if (!(done_mask >> (tt * 8 + i) & 1u)) continue;
+              const int t = j.perm[it.pair_begin + i] / j.k, r = (wk.tile + tt) * 32 + lane;
+              float o = 0.f;
+              for (int q = 0; q < j.k; ++q) o = fmaf(j.w[t * j.k + q], __ldcg(j.y + ((size_t)t * j.k + q) * j.H + r), o);
+              j.out[(size_t)t * j.H + r] = o;
+            }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&published);
+    }
+    return;
+  }
+
+  // ---- compute warps: the call's inputs once (the staging of stage_rows)
+  for (int t = 0; t < T; ++t) {
+    if (j.x_bf16) {
+      const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(j.x) + (size_t)t * j.H;
+      for (int c = tid; c < j.H; c += kThreads) xs[t * j.H + c] = __bfloat162float(src[c]);
+    } else {
+      const float4 *src = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(j.x) + (size_t)t * j.H);
+      float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * j.H);
+      for (int c = tid; c < j.H / 4; c += kThreads) dst[c] = src[c];
+    }
+  }
+  compute_sync();
+  for (int i = warp; i < T * nbH; i += kWarps) {
+    float v = xs[(size_t)i * 32 + lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) xsum[i] = v;
+  }
+  compute_sync();
+
+  int c = 0;
+  for (;; ++c) {
+    const int s = c % NB;
+    const uint32_t parity = (uint32_t)(c / NB) & 1u;
+    // one thread waits (bounded) and shares the decision, so that every
+    // compute thread leaves the loop together
+    if (tid == 0) s_ok = ring_wait(&full[s], parity) ? 1 : 0;
+    compute_sync();
+    if (!s_ok) {
+      flag_error(j.err, 3);
+      break;
+    }
+    (void)mbar_try_wait(&full[s], parity);  // completed phase: each thread's acquire of the tiles
+    const int code = s_item[s];
+    if (code < 0) break;
+    const Work wk = decode_claim(code, qs);
+    const WorkItem it = j.items[wk.iu];
+    const MatLayout &L = mat_of(wk.mat);
+    const bool is_down = wk.mat == 2;
+    const int nb = L.nb, K = 32 * nb, n = it.pair_count;
+    const unsigned char *buf = ring + (size_t)s * slot_bytes;
+    uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
+    const float *in = is_down ? hs : xs;
+    const float *insum = is_down ? hsum : xsum;
+
+    if (is_down) {
+      // h of this expert needs all of its gate and up tiles
+      if (tid == 0) {
+        int ok = 0;
+        uint64_t t0 = 0;
+        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+          if (ld_acquire(&j.sync[2 + wk.iu]) >= 2 * qs.tF) { ok = 1; break; }
+          __nanosleep(32);
+          if ((i & 63u) == 63u) {
+            const uint64_t t = now_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > kDecodeWaitNs) break;
+          }
+        }
+        s_ok_down = ok;
+      }
+      compute_sync();
+      if (!s_ok_down) {
+        flag_error(j.err, 3);
+        break;
+      }
+      // h = silu(g) * u of the pairs (written by other CTAs: read through L2)
+      for (int q = 0; q < n; ++q) {
+        const size_t base = (size_t)j.perm[it.pair_begin + q] * j.F;
+        for (int c2 = tid; c2 < K; c2 += kThreads) {
+          const float gv = __ldcg(j.g + base + c2), uv = __ldcg(j.u + base + c2);
+          hs[q * K + c2] = gv / (1.f + expf(-gv)) * uv;
+        }
+      }
+      compute_sync();
+      for (int i = warp; i < n * nb; i += kWarps) {
+        float v = hs[(size_t)i * 32 + lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) hsum[i] = v;
+      }
+      compute_sync();
+    }
+    // input row of pick q: its token (gate/up) or its own staged h (down)
+    int qrow[TMAX];
+#pragma unroll
+    for (int q = 0; q < TMAX; ++q) qrow[q] = q < n ? (is_down ? q : j.perm[it.pair_begin + q] / j.k) : 0;
+
+    for (int tt = 0; tt < wk.nt; ++tt) {
+      const int row = tt * 32 + lane;
+      // blocks warp, warp + 8, ... in ascending order, two at a time; each is
+      // added exactly as block_term adds it
+      float acc[TMAX];
+#pragma unroll
+      for (int q = 0; q < TMAX; ++q) acc[q] = 0.f;
+#pragma unroll 1
+      for (int b = warp; b < nb; b += 2 * kWarps) {
+        const int b2 = b + kWarps;
+        const bool two = b2 < nb;
+        uint4 q0, q1 = make_uint4(0, 0, 0, 0);
+        unsigned short d0b, d1b = 0;
+        load_block(buf, wk.miss, wk.nt, row, b, nb, slot, L, wk.tile, q0, d0b);
+        if (two) load_block(buf, wk.miss, wk.nt, row, b2, nb, slot, L, wk.tile, q1, d1b);
+        float f0[32], f1[32];
+        decode_block(q0, f0);
+        decode_block(q1, f1);
+        const float d0 = half_bits(d0b), d1 = half_bits(d1b);
+#pragma unroll
+        for (int q = 0; q < TMAX; ++q) {
+          if (q < n) {
+            const float *xr = in + (size_t)qrow[q] * K;
+            const float t0 = dot32(f0, xr + 32 * b);
+            const float t1 = two ? dot32(f1, xr + 32 * b2) : 0.f;
+            acc[q] = fmaf(d0, fmaf(256.f, t0, -136.f * insum[qrow[q] * nb + b]), acc[q]);
+            if (two) acc[q] = fmaf(d1, fmaf(256.f, t1, -136.f * insum[qrow[q] * nb + b2]), acc[q]);
+          }
+        }
+      }
+      if (tt > 0) compute_sync();  // the previous tile's sums have been read
+#pragma unroll
+      for (int q = 0; q < TMAX; ++q)
+        if (q < n) red[(warp * T + q) * 32 + lane] = acc[q];
+      compute_sync();
+      if (tt == wk.nt - 1 && tid == 0) mbar_arrive(&empty[s]);  // the tiles are no longer read
+      for (int q = warp; q < n; q += kWarps) {
+        float v = 0.f;
+        for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
+        const int pair = j.perm[it.pair_begin + q];
+        if (is_down) j.y[(size_t)pair * j.H + (wk.tile + tt) * 32 + lane] = v;
+        else (wk.mat == 0 ? j.g : j.u)[(size_t)pair * j.F + wk.tile * 32 + lane] = v;
+      }
+    }
+    // hand the item to the publisher once every compute thread's stores are issued
+    const int p = c % kPubSlots;
+    if (tid == 0) {
+      if (c >= kPubSlots && !ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u)) flag_error(j.err, 3);
+      s_pub[p] = code;
+    }
+    mbar_arrive(&pub[p]);
+  }
+  // end of the publisher's list
+  {
+    const int p = c % kPubSlots;
+    if (tid == 0) {
+      if (c >= kPubSlots) (void)ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u);
+      s_pub[p] = -1;
+    }
+    mbar_arrive(&pub[p]);
+  }
+}
+
+}  // namespace
+
+bool decode_layer_supported(int H, int F, int T) {
+  if (T < 1 || T > kTokPerUnit || H % 32 || F % 32) return false;
+  return decode_smem(H, F, T, 2) <= kDecodeSmemCap;
+}
+
+cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
+                                float *g, float *u, float *out, int32_t *sync, int cbase, int T, int n_sms,
+                                cudaStream_t st) {
+  if (!decode_layer_supported(a.H, a.F, T)) return cudaErrorInvalidValue;
+  DecodeJob j;
+  j.host = host_layer;
+  j.expert_stride = expert_stride;
+  j.slots = const_cast<uint8_t *>(a.slots);
+  j.slot_stride = a.slot_stride;
+  j.lay = a.lay;
+  j.hdr = a.hdr;
+  j.items = a.items;
+  j.perm = a.perm;
+  j.w = w;
+  j.x = a.x;
+  j.x_bf16 = a.x_bf16;
+  j.T = T;
+  j.k = a.k;
+  j.H = a.H;
+  j.F = a.F;
+  j.DG = decode_down_group(a.H, a.F);
+  j.g = g;
+  j.u = u;
+  j.y = a.y;
+  j.out = out;
+  j.sync = sync;
+  j.cbase = cbase;
+  j.err = a.err;
+  // three items in flight per CTA when they fit, else two
+  const bool nb3 = decode_smem(a.H, a.F, T, 3) <= kDecodeSmemCap;
+  const size_t smem = decode_smem(a.H, a.F, T, nb3 ? 3 : 2);
+  cudaError_t e;
+  if (T == 1 && nb3) {
+    static size_t cur = 0;
+    if ((e = ensure_dyn_smem(decode_layer_kernel<3, 1>, smem, cur)) != cudaSuccess) return e;
+    decode_layer_kernel<3, 1><<<n_sms, kDecodeThreads, smem, st>>>(j);
+  } else if (T == 1) {
+    static size_t cur = 0;
+    if ((e = ensure_dyn_smem(decode_layer_kernel<2, 1>, smem, cur)) != cudaSuccess) return e;
+    decode_layer_kernel<2, 1><<<n_sms, kDecodeThreads, smem, st>>>(j);
+  } else if (nb3) {
+    static size_t cur = 0;
+    if ((e = ensure_dyn_smem(decode_layer_kernel<3, kTokPerUnit>, smem, cur)) != cudaSuccess) return e;
+    decode_layer_kernel<3, kTokPerUnit><<<n_sms, kDecodeThreads, smem, st>>>(j);
+  } else {
+    static size_t cur = 0;
+    if ((e = ensure_dyn_smem(decode_layer_kernel<2, kTokPerUnit>, smem, cur)) != cudaSuccess) return e;
+    decode_layer_kernel<2, kTokPerUnit><<<n_sms, kDecodeThreads, smem, st>>>(j);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -6,31 +6,43 @@
 //
 // One CTA computes one output tile: 128 output features (rows of W) x up to
 // kGemmN routed pairs of one expert, looping over the input dimension in
-// chunks of 64.  Roles (8 warps):
-//   warp 7     brings the chunk's Q4_0 tile into shared memory with bulk
-//              copies (4 contiguous runs of nibbles and of scales per matrix);
-//   warps 0-3  dequantise it to bf16, w = (q - 8) * bf16(d) rounded to bf16,
-//              built with bf16x2 operations from the nibble bits, into shared
-//              memory in the 128-byte-swizzled K-major layout the MMA reads;
-//   warps 4-5  gather the pairs' input rows (bf16) with cp.async into the same
-//              layout;
-//   warp 6     one thread issues the MMAs (gate and up share the inputs and
-//              accumulate into two TMEM regions) and commits each stage back to
-//              the producers;
-//   warps 0-3  finally read the accumulators from TMEM: gate/up -> h =
-//              silu(g) * u rounded to bf16; down -> y in fp32.
-// Stages are guarded by mbarriers; every wait is bounded and, on timeout, sets
-// the handle's error word, frees TMEM and returns.
+// chunks of 64.  The pairs' activations were copied beforehand into
+// pair-sorted order, so the tile's B operand is a contiguous row range that a
+// TMA tensor copy lands directly in the 128-byte-swizzled K-major layout.
+// Roles (11 warps):
+//   warp 9     brings each chunk's Q4_0 weights into a raw ring with bulk
+//              copies (per matrix, 4 contiguous runs of nibbles and of scales);
+//   warp 10    brings each chunk's activation rows into a 6-deep ring with
+//              TMA tensor copies;
+//   warps 0-7  dequantise the raw chunk to bf16, w = (q - 8) * bf16(d) rounded
+//              to bf16, built with bf16x2 operations from the nibble bits, into
+//              the swizzled K-major layout the MMA reads;
+//   warp 8     one thread issues the MMAs (gate and up share the activations
+//              and accumulate into two TMEM regions) and commits each stage
+//              back to its producers;
+//   warps 0-7  finally read the accumulators from TMEM: gate/up -> h =
+//              silu(g) * u rounded to bf16 (pair-sorted rows); down -> y in
+//              fp32 (rows by pair).
+// Stages are guarded by mbarriers; every wait is bounded and gives up early
+// once another role has failed; on failure the CTA waits for its copies and
+// MMAs in flight, sets the handle's error word, frees TMEM and returns.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int kGemmM = 128;   // output features per tile
-constexpr int kGemmK = 64;    // input features per pipeline stage (128 bytes of bf16)
-constexpr int kStages = 3;
-constexpr int kGemmThreads = 256;
+constexpr int kGemmM = 128;    // output features per tile
+constexpr int kGemmK = 64;     // input features per pipeline stage (128 bytes of bf16)
+constexpr int kAStages = 2;    // dequantised weight tiles
+constexpr int kBStages = 6;    // activation tiles
+constexpr int kRawStages = 4;  // raw Q4_0 chunks
+constexpr int kDqThreads = 256;
+constexpr int kMmaWarp = 8, kRawWarp = 9, kBWarp = 10;
+constexpr int kGemmThreads = 352;
 constexpr uint32_t kGemmSpin = 1u << 26;
+constexpr uint64_t kGemmWaitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t gsa(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -40,15 +52,33 @@ __device__ __forceinline__ void g_mbar_init(uint64_t *bar, uint32_t count) {
 __device__ __forceinline__ void g_mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(gsa(bar)) : "memory");
 }
-__device__ __forceinline__ bool g_mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ uint64_t g_now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool g_mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(gsa(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `bar` with the given parity: gives up (false)
+// after kGemmWaitNs of wall time or kGemmSpin polls, or as soon as another role
+// of the CTA has failed (fail != nullptr).
+__device__ __forceinline__ bool g_mbar_wait(uint64_t *bar, uint32_t parity, const int *fail) {
+  uint64_t t0 = 0;
   for (uint32_t i = 0; i < kGemmSpin; ++i) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(gsa(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
+    if (g_mbar_test(bar, parity)) return true;
+    if ((i & 255u) == 255u) {
+      if (fail && *reinterpret_cast<const volatile int *>(fail)) return false;
+      const uint64_t now = g_now_ns();
+      if (t0 == 0) t0 = now;
+      else if (now - t0 > kGemmWaitNs) return false;
+    }
   }
   return false;
 }
@@ -94,9 +124,24 @@ __device__ __forceinline__ uint32_t sw128_off(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<const uint32_t *>(&v);
+
+// TMA tensor copy of one 2-D box (x = column, y = row) into shared memory,
+// completing on `bar` with the box's byte count.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(gsa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(gsa(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   gsa(dst)),
+               "l"(src), "r"(bytes), "r"(gsa(bar))
+               : "memory");
+}
+__device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(gsa(bar)), "r"(bytes) : "memory");
 }
 
 struct GemmJob {
@@ -104,16 +149,14 @@ struct GemmJob {
   uint64_t slot_stride;
   MatLayout m0, m1;  // gate, up (NMAT 2) or down (NMAT 1)
   int R, nb;         // output rows, input 32-blocks
-  const __nv_bfloat16 *x;  // input rows [*, 32 nb] bf16
-  int x_div;               // input row of pair p is p / x_div
   const int32_t *perm;
   const WorkItem *items;
   const WorkUnit *gunits;
   const int32_t *gunit_begin;
   const PlanHdr *hdr;
   int range_kind, stage;
-  __nv_bfloat16 *h16;  // gate/up output [pairs, R]
-  float *y;            // down output [pairs, R]
+  __nv_bfloat16 *h16s;  // gate/up output [sorted pairs, R]
+  float *y;             // down output [pairs, R]
   int32_t *err;
 };
 
@@ -126,62 +169,112 @@ __device__ __forceinline__ bool gunit_range(const PlanHdr *h, const int32_t *gb,
   return true;
 }
 
-constexpr int kRawStages = 4;  // raw Q4_0 chunks in flight (bulk copies)
-
+constexpr size_t kBTileBytes = (size_t)kGemmN * 128;  // one chunk of up to 128 activation rows
 template <int NMAT>
-constexpr size_t gemm_stage_bytes() {  // bf16 A (per matrix) + B tiles of one K chunk
-  return (size_t)NMAT * kGemmM * 128 + (size_t)kGemmN * 128;
-}
+constexpr size_t a_stage_bytes() { return (size_t)NMAT * kGemmM * 128; }
 template <int NMAT>
-constexpr size_t raw_stage_bytes() {   // Q4_0 of one chunk: 4 row tiles x 2 blocks, per matrix
+constexpr size_t raw_stage_bytes() {  // Q4_0 of one chunk: 4 row tiles x 2 blocks, per matrix
   return (size_t)NMAT * (4 * 1024 + 4 * 128);
 }
 template <int NMAT>
 constexpr size_t gemm_smem_bytes() {
-  return kStages * gemm_stage_bytes<NMAT>() + kRawStages * raw_stage_bytes<NMAT>() + 1024;
+  return kAStages * a_stage_bytes<NMAT>() + kBStages * kBTileBytes + kRawStages * raw_stage_bytes<NMAT>() + 1024;
+}
+
+// Dequantise block bi (32 inputs) of row r of one matrix from the raw chunk
+// into the swizzled bf16 tile `a` (row r, 16-byte chunks 4 bi .. 4 bi + 3).
+__device__ __forceinline__ void dequant_block(const unsigned char *rm, unsigned char *a, int r, int bi, bool valid) {
+  uint4 q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
+  float d = 0.f;
+  if (valid) {
+    q = *reinterpret_cast<const uint4 *>(rm + (r >> 5) * 1024 + bi * 512 + (r & 31) * 16);
+    d = __half2float(__ushort_as_half(
+        *reinterpret_cast<const unsigned short *>(rm + 4 * 1024 + (r >> 5) * 128 + bi * 64 + (r & 31) * 2)));
+  }
+  // two nibbles side by side under the bf16 exponent of 128: 0x4300|q is
+  // 128 + q exactly; minus 136 gives q - 8 exactly; times d rounds once
+  const __nv_bfloat162 d2 = __float2bfloat162_rn(d);
+  const __nv_bfloat162 k136 = __float2bfloat162_rn(136.f);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t lo_pk[8], hi_pk[8];  // values 0..15 (low nibbles), 16..31 (high nibbles)
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t p01 = __byte_perm(w[i], 0u, 0x4140u);  // bytes 4i, 4i+1 in the two halves
+    const uint32_t p23 = __byte_perm(w[i], 0u, 0x4342u);  // bytes 4i+2, 4i+3
+    const uint32_t v[4] = {(p01 & 0x000F000Fu) | 0x43004300u, (p23 & 0x000F000Fu) | 0x43004300u,
+                           ((p01 >> 4) & 0x000F000Fu) | 0x43004300u, ((p23 >> 4) & 0x000F000Fu) | 0x43004300u};
+    __nv_bfloat162 o[4];
+#pragma unroll
+    for (int z = 0; z < 4; ++z) o[z] = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&v[z]), k136), d2);
+    lo_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[0]);
+    lo_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[1]);
+    hi_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[2]);
+    hi_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[3]);
+  }
+  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 0)) = make_uint4(lo_pk[0], lo_pk[1], lo_pk[2], lo_pk[3]);
+  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 1)) = make_uint4(lo_pk[4], lo_pk[5], lo_pk[6], lo_pk[7]);
+  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 2)) = make_uint4(hi_pk[0], hi_pk[1], hi_pk[2], hi_pk[3]);
+  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 3)) = make_uint4(hi_pk[4], hi_pk[5], hi_pk[6], hi_pk[7]);
+}
+
+// Waits (bounded) until the last min(issued, stages) copies a loader issued
+// into a ring of `stages` barriers have landed, so no copy is in flight when
+// the CTA leaves; a no-op once all of them were consumed.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int issued) {
+  for (int c = issued - stages < 0 ? 0 : issued - stages; c < issued; ++c)
+    (void)g_mbar_wait(&full[c % stages], (uint32_t)(c / stages) & 1u, nullptr);
 }
 
 template <int NMAT>
-__global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    umma_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmJob j) {
   int lo, hi;
   if (!gunit_range(j.hdr, j.gunit_begin, j.range_kind, j.stage, lo, hi)) return;
   const int gu = lo + (int)blockIdx.y;
   if (gu >= hi) return;
   const WorkUnit wu = j.gunits[gu];
   const WorkItem it = j.items[wu.item];
-  const int n = wu.pair_count;                       // 1..kGemmN
-  const int nr = (n + 15) & ~15;                     // MMA N: pairs rounded up to 16
+  const int n = wu.pair_count;                 // 1..kGemmN
+  const int nr = (n + 15) & ~15;               // MMA N: pairs rounded up to 16
+  const int bsel = nr <= 16 ? 0 : nr <= 32 ? 1 : nr <= 64 ? 2 : 3;
+  const uint32_t b_bytes = (uint32_t)(16 << bsel) * 128u;  // activation box of 16 << bsel rows
   const int m0 = blockIdx.x * kGemmM;
   const int rt0 = m0 >> 5, n_rt = min(4, (j.R >> 5) - rt0);  // valid 32-row tiles
-  const int nb = j.nb, n_chunks = nb / 2;            // 64 inputs = 2 blocks per chunk
+  const int nb = j.nb, n_chunks = nb / 2;      // 64 inputs = 2 blocks per chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char *sm =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char *raw = sm + kStages * gemm_stage_bytes<NMAT>();
-  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], rfull[kRawStages], rempty[kRawStages], done;
+  unsigned char *sa_base = sm;
+  unsigned char *sb_base = sa_base + kAStages * a_stage_bytes<NMAT>();
+  unsigned char *raw = sb_base + kBStages * kBTileBytes;
+  __shared__ __align__(8) uint64_t afull[kAStages], aempty[kAStages], bfull[kBStages], bempty[kBStages],
+      rfull[kRawStages], rempty[kRawStages], done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_rows[kGemmN];
   __shared__ int s_fail;
 
   constexpr uint32_t kCols = NMAT == 2 ? 2 * kGemmN : kGemmN;  // TMEM columns (power of 2)
-  constexpr int kProducers = 128 + 64;                       // dequant + gather threads
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      g_mbar_init(&full[s], kProducers);
-      g_mbar_init(&empty[s], 1);
+    for (int s = 0; s < kAStages; ++s) {
+      g_mbar_init(&afull[s], kDqThreads);
+      g_mbar_init(&aempty[s], 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      g_mbar_init(&bfull[s], 1);
+      g_mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < kRawStages; ++s) {
       g_mbar_init(&rfull[s], 1);
-      g_mbar_init(&rempty[s], 128);
+      g_mbar_init(&rempty[s], kDqThreads);
     }
     g_mbar_init(&done, 1);
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (tid < kGemmN) s_rows[tid] = tid < n ? j.perm[wu.pair_begin + tid] : -1;
-  if (warp == 7) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(gsa(&tmem_base)),
                  "r"(kCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -192,191 +285,147 @@ __global__ void __launch_bounds__(kGemmThreads, 1) umma_gemm_kernel(GemmJob j) {
   const uint32_t tmem = tmem_base;
   const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
 
-  if (warp == 7) {
-    // ---- raw Q4_0 loader: per chunk and matrix, 4 contiguous 1 KB nibble runs
-    // (32 rows x blocks 2c, 2c+1 of one row tile) and 4 runs of 128 B scales
+  if (warp == kRawWarp) {
+    // ---- raw Q4_0 loader: per chunk and matrix, n_rt contiguous 1 KB nibble
+    // runs (32 rows x blocks 2c, 2c+1 of one row tile) and n_rt 128 B scale runs
     if (lane == 0) {
-      for (int c = 0; c < n_chunks; ++c) {
+      int c = 0;
+      for (; c < n_chunks; ++c) {
         const int s = c % kRawStages;
-        if (c >= kRawStages && !g_mbar_wait(&rempty[s], (uint32_t)((c / kRawStages) - 1) & 1u)) {
+        if (c >= kRawStages && !g_mbar_wait(&rempty[s], (uint32_t)((c / kRawStages) - 1) & 1u, &s_fail)) {
           s_fail = 1;
           break;
         }
         unsigned char *rs = raw + (size_t)s * raw_stage_bytes<NMAT>();
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(gsa(&rfull[s])),
-                     "r"((uint32_t)(NMAT * n_rt * (1024 + 128)))
-                     : "memory");
+        expect_tx(&rfull[s], (uint32_t)(NMAT * n_rt * (1024 + 128)));
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
           const MatLayout &L = m == 0 ? j.m0 : j.m1;
           for (int q = 0; q < n_rt; ++q) {
             const uint64_t e = ((uint64_t)(rt0 + q) * nb + 2 * c) * 32;
-            unsigned char *dn = rs + m * (4 * 1024 + 4 * 128) + q * 1024;
-            unsigned char *ds = rs + m * (4 * 1024 + 4 * 128) + 4 * 1024 + q * 128;
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 1024, [%2];" ::"r"(
-                    gsa(dn)),
-                "l"(slot + L.nib_off + e * 16), "r"(gsa(&rfull[s]))
-                : "memory");
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], 128, [%2];" ::"r"(
-                    gsa(ds)),
-                "l"(slot + L.sc_off + e * 2), "r"(gsa(&rfull[s]))
-                : "memory");
+            unsigned char *dm = rs + m * (4 * 1024 + 4 * 128);
+            bulk_load(dm + q * 1024, slot + L.nib_off + e * 16, 1024, &rfull[s]);
+            bulk_load(dm + 4 * 1024 + q * 128, slot + L.sc_off + e * 2, 128, &rfull[s]);
           }
         }
       }
+      drain_ring(rfull, kRawStages, c);
     }
-  } else if (warp < 4) {
-    // ---- dequant: row r of the tile, both matrices, raw smem -> swizzled bf16
-    const int r = tid;
-    const bool valid = (r >> 5) < n_rt;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int s = c % kStages, rsi = c % kRawStages;
-      if (c >= kStages && !g_mbar_wait(&empty[s], (uint32_t)((c / kStages) - 1) & 1u)) { s_fail = 1; break; }
-      if (!g_mbar_wait(&rfull[rsi], (uint32_t)(c / kRawStages) & 1u)) { s_fail = 1; break; }
-      const unsigned char *rs = raw + (size_t)rsi * raw_stage_bytes<NMAT>();
-      unsigned char *st = sm + (size_t)s * gemm_stage_bytes<NMAT>();
-#pragma unroll
-      for (int m = 0; m < NMAT; ++m) {
-        unsigned char *a = st + (size_t)m * kGemmM * 128;
-#pragma unroll
-        for (int bi = 0; bi < 2; ++bi) {
-          uint4 q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
-          float d = 0.f;
-          if (valid) {
-            const unsigned char *rm = rs + m * (4 * 1024 + 4 * 128);
-            q = *reinterpret_cast<const uint4 *>(rm + (r >> 5) * 1024 + bi * 512 + (r & 31) * 16);
-            d = __half2float(__ushort_as_half(
-                *reinterpret_cast<const unsigned short *>(rm + 4 * 1024 + (r >> 5) * 128 + bi * 64 + (r & 31) * 2)));
-          }
-          // two nibbles side by side under the bf16 exponent of 128: 0x4300|q is
-          // 128 + q exactly; minus 136 gives q - 8 exactly; times d rounds once
-          const __nv_bfloat162 d2 = __float2bfloat162_rn(d);
-          const __nv_bfloat162 k136 = __float2bfloat162_rn(136.f);
-          const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-          uint32_t lo_pk[8], hi_pk[8];  // values 0..15 (low nibbles), 16..31 (high nibbles)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t p01 = __byte_perm(w[i], 0u, 0x4140u);  // bytes 4i, 4i+1 in the two halves
-            const uint32_t p23 = __byte_perm(w[i], 0u, 0x4342u);  // bytes 4i+2, 4i+3
-            const uint32_t v[4] = {(p01 & 0x000F000Fu) | 0x43004300u, (p23 & 0x000F000Fu) | 0x43004300u,
-                                   ((p01 >> 4) & 0x000F000Fu) | 0x43004300u,
-                                   ((p23 >> 4) & 0x000F000Fu) | 0x43004300u};
-            __nv_bfloat162 o[4];
-#pragma unroll
-            for (int z = 0; z < 4; ++z)
-              o[z] = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&v[z]), k136), d2);
-            lo_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[0]);
-            lo_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[1]);
-            hi_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[2]);
-            hi_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[3]);
-          }
-          *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 0)) = make_uint4(lo_pk[0], lo_pk[1], lo_pk[2], lo_pk[3]);
-          *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 1)) = make_uint4(lo_pk[4], lo_pk[5], lo_pk[6], lo_pk[7]);
-          *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 2)) = make_uint4(hi_pk[0], hi_pk[1], hi_pk[2], hi_pk[3]);
-          *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 3)) = make_uint4(hi_pk[4], hi_pk[5], hi_pk[6], hi_pk[7]);
+  } else if (warp == kBWarp) {
+    // ---- activation loader: rows [pair_begin, pair_begin + box) of the sorted
+    // buffer, columns [64 c, 64 c + 64), one TMA tensor copy per chunk
+    if (lane == 0) {
+      const CUtensorMap *map = &maps.box[bsel];
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+      int c = 0;
+      for (; c < n_chunks; ++c) {
+        const int s = c % kBStages;
+        if (c >= kBStages && !g_mbar_wait(&bempty[s], (uint32_t)((c / kBStages) - 1) & 1u, &s_fail)) {
+          s_fail = 1;
+          break;
         }
+        expect_tx(&bfull[s], b_bytes);
+        tma_load_2d(sb_base + (size_t)s * kBTileBytes, map, c * kGemmK, wu.pair_begin, &bfull[s]);
       }
-      g_mbar_arrive(&rempty[rsi]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      g_mbar_arrive(&full[s]);
+      drain_ring(bfull, kBStages, c);
     }
-  } else if (warp < 6) {
-    // ---- gather the pairs' input rows (nr rows, zero padding past n) with
-    // cp.async; a chunk is published once it landed
-    const int t = tid - 128;  // 0..63
-    const int K = 32 * nb;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int s = c % kStages;
-      if (c >= kStages && !g_mbar_wait(&empty[s], (uint32_t)((c / kStages) - 1) & 1u)) { s_fail = 1; break; }
-      unsigned char *bsm = sm + (size_t)s * gemm_stage_bytes<NMAT>() + (size_t)NMAT * kGemmM * 128;
-      for (int i = t; i < nr * 8; i += 64) {
-        const int rr = i >> 3, cc = i & 7;
-        unsigned char *dst = bsm + sw128_off(rr, cc);
-        const int src_row = s_rows[rr];
-        if (src_row >= 0) {
-          const __nv_bfloat16 *src = j.x + (size_t)(src_row / j.x_div) * K + c * kGemmK + cc * 8;
-          asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(gsa(dst)), "l"(src) : "memory");
-        } else {
-          *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      // publish the previous chunk: its copies have landed once at most one
-      // group (this one) is pending.  Publishing one behind (not kStages - 1)
-      // keeps the publication of chunk c independent of the MMA of chunk c - 1.
-      if (c >= 1) {
-        asm volatile("cp.async.wait_group 1;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        g_mbar_arrive(&full[(c - 1) % kStages]);
-      }
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (n_chunks >= 1) g_mbar_arrive(&full[(n_chunks - 1) % kStages]);
-  } else if (warp == 6) {
+  } else if (warp == kMmaWarp) {
     // ---- MMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kGemmM, nr);
-      bool ok = true;
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        const int s = c % kStages;
-        if (!g_mbar_wait(&full[s], (uint32_t)(c / kStages) & 1u)) { ok = false; s_fail = 1; break; }
+      for (int c = 0; c < n_chunks; ++c) {
+        const int sa = c % kAStages, sb = c % kBStages;
+        if (!g_mbar_wait(&afull[sa], (uint32_t)(c / kAStages) & 1u, &s_fail) ||
+            !g_mbar_wait(&bfull[sb], (uint32_t)(c / kBStages) & 1u, &s_fail)) {
+          s_fail = 1;
+          break;
+        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        unsigned char *st = sm + (size_t)s * gemm_stage_bytes<NMAT>();
-        const uint32_t b_addr = gsa(st + (size_t)NMAT * kGemmM * 128);
+        const uint32_t b_addr = gsa(sb_base + (size_t)sb * kBTileBytes);
+        const uint32_t a_base = gsa(sa_base + (size_t)sa * a_stage_bytes<NMAT>());
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
-          const uint32_t a_addr = gsa(st + (size_t)m * kGemmM * 128);
+          const uint32_t a_addr = a_base + (uint32_t)(m * kGemmM * 128);
 #pragma unroll
           for (int ks = 0; ks < kGemmK / 16; ++ks)
             umma(tmem + (uint32_t)(m * kGemmN), sw128_desc(a_addr + ks * 32), sw128_desc(b_addr + ks * 32), idesc,
                  (c > 0 || ks > 0) ? 1u : 0u);
         }
-        umma_commit(&empty[s]);
+        umma_commit(&aempty[sa]);
+        umma_commit(&bempty[sb]);
       }
-      if (ok) umma_commit(&done);
+      umma_commit(&done);  // also on failure: `done` then tracks the MMAs in flight
+    }
+  } else {
+    // ---- dequant (warps 0-7): gate/up: thread = (matrix, row), both blocks;
+    // down: thread = (block, row)
+    const int r = tid & 127, hi_half = tid >> 7;
+    const bool valid = (r >> 5) < n_rt;
+    for (int c = 0; c < n_chunks; ++c) {
+      const int sa = c % kAStages, rsi = c % kRawStages;
+      if (c >= kAStages && !g_mbar_wait(&aempty[sa], (uint32_t)((c / kAStages) - 1) & 1u, &s_fail)) {
+        s_fail = 1;
+        break;
+      }
+      if (!g_mbar_wait(&rfull[rsi], (uint32_t)(c / kRawStages) & 1u, &s_fail)) {
+        s_fail = 1;
+        break;
+      }
+      const unsigned char *rs = raw + (size_t)rsi * raw_stage_bytes<NMAT>();
+      unsigned char *st = sa_base + (size_t)sa * a_stage_bytes<NMAT>();
+      if (NMAT == 2) {
+        const unsigned char *rm = rs + hi_half * (4 * 1024 + 4 * 128);
+        unsigned char *a = st + (size_t)hi_half * kGemmM * 128;
+        dequant_block(rm, a, r, 0, valid);
+        dequant_block(rm, a, r, 1, valid);
+      } else {
+        dequant_block(rs, st, r, hi_half, valid);
+      }
+      g_mbar_arrive(&rempty[rsi]);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      g_mbar_arrive(&afull[sa]);
     }
   }
 
-  // ---- epilogue (warps 0-3 own TMEM lanes 0-127 = the tile's rows)
-  if (warp < 4) {
-    const bool ok = !s_fail && g_mbar_wait(&done, 0);
-    if (!ok) {
-      s_fail = 1;
-    } else {
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int row = m0 + tid;
-      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      for (int c0 = 0; c0 < nr; c0 += 16) {
-        float g[16], u[16];
-        tmem_ld16(lane_addr + c0, g);
-        if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
-        if (row < j.R) {
+  // ---- epilogue (warps 0-7): warp w reads TMEM lanes 32 (w % 4) .. + 31 (the
+  // tile's rows) and the 16-column groups of parity w / 4
+  const bool ok = warp < 8 && g_mbar_wait(&done, 0, &s_fail) && !s_fail;
+  if (warp < 8 && ok) {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const int q = warp & 3, half = warp >> 2;
+    const int row = m0 + q * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+    for (int c0 = half * 16; c0 < nr; c0 += 32) {
+      float g[16], u[16];
+      tmem_ld16(lane_addr + c0, g);
+      if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
+      if (row < j.R) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int col = c0 + i;
-            if (col < n) {
-              const int pair = s_rows[col];
-              if (NMAT == 2)
-                j.h16[(size_t)pair * j.R + row] = __float2bfloat16_rn(g[i] / (1.f + expf(-g[i])) * u[i]);
-              else
-                j.y[(size_t)pair * j.R + row] = g[i];
-            }
+        for (int i = 0; i < 16; ++i) {
+          const int col = c0 + i;
+          if (col < n) {
+            if (NMAT == 2)
+              j.h16s[(size_t)(wu.pair_begin + col) * j.R + row] = __float2bfloat16_rn(g[i] / (1.f + expf(-g[i])) * u[i]);
+            else
+              j.y[(size_t)s_rows[col] * j.R + row] = g[i];
           }
         }
       }
     }
+  } else if (warp < 8 && !ok) {
+    s_fail = 1;
   }
+  // MMAs in flight must finish before TMEM is freed: `done` is committed on
+  // every path of the issuer
+  if (s_fail && warp == 0) (void)g_mbar_wait(&done, 0, nullptr);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (s_fail && tid == 0 && j.err) atomicExch(j.err, 4);
-  if (warp == 7) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+  if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
 }
 
 template <int NMAT>
-cudaError_t launch_gemm_t(const GemmJob &j, int max_gunits, cudaStream_t st) {
+cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmJob &j, int max_gunits, cudaStream_t st) {
   if (max_gunits <= 0) return cudaSuccess;
   if (j.nb % 2) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes<NMAT>();
@@ -384,60 +433,98 @@ cudaError_t launch_gemm_t(const GemmJob &j, int max_gunits, cudaStream_t st) {
   const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT>, smem, cur);
   if (e != cudaSuccess) return e;
   dim3 grid((j.R + kGemmM - 1) / kGemmM, max_gunits);
-  umma_gemm_kernel<NMAT><<<grid, kGemmThreads, smem, st>>>(j);
+  umma_gemm_kernel<NMAT><<<grid, kGemmThreads, smem, st>>>(maps, j);
   return cudaGetLastError();
+}
+
+// xs[pos] = x[perm[pos] / k], 16 bytes per thread
+__global__ void gather_sorted_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm, int P, int k,
+                                     int H8, uint4 *__restrict__ xs) {
+  const int total = P * H8;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += gridDim.x * blockDim.x) {
+    const int pos = i / H8, c = i - pos * H8;
+    xs[i] = x[(size_t)(perm[pos] / k) * H8 + c];
+  }
+}
+
+GemmJob base_job(const FfnArgs &a, const WorkUnit *gunits, const int32_t *gunit_begin, int range_kind, int stage) {
+  GemmJob j;
+  j.slots = a.slots;
+  j.slot_stride = a.slot_stride;
+  j.perm = a.perm;
+  j.items = a.items;
+  j.gunits = gunits;
+  j.gunit_begin = gunit_begin;
+  j.hdr = a.hdr;
+  j.range_kind = range_kind;
+  j.stage = stage;
+  j.h16s = nullptr;
+  j.y = nullptr;
+  j.err = a.err;
+  return j;
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_gateup(const FfnArgs &a, const __nv_bfloat16 *x, const WorkUnit *gunits,
-                               const int32_t *gunit_begin, __nv_bfloat16 *h16, int range_kind, int stage,
+cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps *out) {
+  using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || K % kGemmK || rows <= 0) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(__nv_bfloat16)};
+  const cuuint32_t elem[2] = {1, 1};
+  for (int i = 0; i < 4; ++i) {
+    const cuuint32_t box[2] = {(cuuint32_t)kGemmK, (cuuint32_t)(16 << i)};
+    const CUresult r = encode(&out->box[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16 *>(base), dims,
+                              strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_gather_sorted(const __nv_bfloat16 *x, const int32_t *perm, int P, int k, int H,
+                                 __nv_bfloat16 *xs, cudaStream_t st) {
+  if (P <= 0) return cudaSuccess;
+  if (H % 8) return cudaErrorInvalidValue;
+  const int H8 = H / 8, total = P * H8;
+  const int grid = std::min((total + 255) / 256, 152 * 8);
+  gather_sorted_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(x), perm, P, k, H8,
+                                             reinterpret_cast<uint4 *>(xs));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const WorkUnit *gunits,
+                               const int32_t *gunit_begin, __nv_bfloat16 *h16s, int range_kind, int stage,
                                int max_gunits, cudaStream_t st) {
-  GemmJob j;
-  j.slots = a.slots;
-  j.slot_stride = a.slot_stride;
+  GemmJob j = base_job(a, gunits, gunit_begin, range_kind, stage);
   j.m0 = a.lay.gate;
   j.m1 = a.lay.up;
   j.R = a.F;
   j.nb = a.H / 32;
-  j.x = x;
-  j.x_div = a.k;
-  j.perm = a.perm;
-  j.items = a.items;
-  j.gunits = gunits;
-  j.gunit_begin = gunit_begin;
-  j.hdr = a.hdr;
-  j.range_kind = range_kind;
-  j.stage = stage;
-  j.h16 = h16;
-  j.y = nullptr;
-  j.err = a.err;
-  return launch_gemm_t<2>(j, max_gunits, st);
+  j.h16s = h16s;
+  return launch_gemm_t<2>(xs_maps, j, max_gunits, st);
 }
 
-cudaError_t launch_gemm_down(const FfnArgs &a, const __nv_bfloat16 *h16, const WorkUnit *gunits,
+cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const WorkUnit *gunits,
                              const int32_t *gunit_begin, int range_kind, int stage, int max_gunits,
                              cudaStream_t st) {
-  GemmJob j;
-  j.slots = a.slots;
-  j.slot_stride = a.slot_stride;
+  GemmJob j = base_job(a, gunits, gunit_begin, range_kind, stage);
   j.m0 = a.lay.down;
   j.m1 = a.lay.down;
   j.R = a.H;
   j.nb = a.F / 32;
-  j.x = h16;
-  j.x_div = 1;
-  j.perm = a.perm;
-  j.items = a.items;
-  j.gunits = gunits;
-  j.gunit_begin = gunit_begin;
-  j.hdr = a.hdr;
-  j.range_kind = range_kind;
-  j.stage = stage;
-  j.h16 = nullptr;
   j.y = a.y;
-  j.err = a.err;
-  return launch_gemm_t<1>(j, max_gunits, st);
+  return launch_gemm_t<1>(h16s_maps, j, max_gunits, st);
 }
 
 }  // namespace moe

@@ -64,10 +64,14 @@ struct moe_cache {
   WorkUnit *d_units = nullptr;
   MissItem *d_miss = nullptr;
   PlanHdr *d_hdr = nullptr;
-  int32_t *d_sync = nullptr;
+  int32_t *d_sync = nullptr;  // per-call counters: queue head, per item, per (token, row tile)
+  float *d_u = nullptr;         // up outputs of the decode layer kernel [maxP, F] (gate outputs use d_h)
+  int n_sms = 0;
   WorkUnit *d_gunits = nullptr;
   int32_t *d_gunit_begin = nullptr;
-  __nv_bfloat16 *d_h16 = nullptr;
+  __nv_bfloat16 *d_h16 = nullptr;  // gate/up output of the GEMM path, pair-sorted rows [maxP, F]
+  __nv_bfloat16 *d_xs = nullptr;   // activations in pair-sorted order [maxP, H]
+  GemmMaps xs_maps, h16_maps;
   int maxGunits = 0;
   uint8_t *d_staging = nullptr;
   int staging_blocks = 0;
@@ -95,7 +99,7 @@ namespace {
 
 const char *const kKindNames[K_NKINDS] = {"plan",        "repack",    "q4_gateup_gemv", "q4_down_gemv",
                                           "combine",     "gemm_gateup", "gemm_down",    "gather",
-                                          "h2d_memcpy",  "fused_miss"};
+                                          "h2d_memcpy",  "fused_miss",  "decode_layer"};
 
 int poison(moe_cache *c, int code) {
   if (!c->poisoned) {
@@ -216,9 +220,11 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_miss);
   cudaFree(c->d_hdr);
   cudaFree(c->d_sync);
+  cudaFree(c->d_u);
   cudaFree(c->d_gunits);
   cudaFree(c->d_gunit_begin);
   cudaFree(c->d_h16);
+  cudaFree(c->d_xs);
   cudaFree(c->d_staging);
   if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
   if (c->h_err) cudaFreeHost(c->h_err);
@@ -301,7 +307,9 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
     delete c;
     return code;
   };
-  if (cudaGetDevice(&c->device) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
 
   // host store: pinned and mapped
   cudaPointerAttributes pa;
@@ -343,12 +351,18 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_units, c->maxUnits) == cudaSuccess;
   ok = ok && dalloc(&c->d_miss, c->maxU) == cudaSuccess;
   ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
-  ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 33) == cudaSuccess;
+  ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 2 + (size_t)cfg->max_tokens * (cfg->hidden / 32)) == cudaSuccess;
+  ok = ok && dalloc(&c->d_u, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
   c->maxGunits = c->maxU + (c->maxP + kGemmN - 1) / kGemmN + 1;
   ok = ok && dalloc(&c->d_gunits, c->maxGunits) == cudaSuccess;
   ok = ok && dalloc(&c->d_gunit_begin, c->maxStages + 1) == cudaSuccess;
-  if (ok && cfg->gemm_min_tokens > 0 && cfg->act_dtype == 1)
-    ok = dalloc(&c->d_h16, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
+  if (ok && cfg->gemm_min_tokens > 0 && cfg->act_dtype == 1) {
+    ok = dalloc(&c->d_h16, (size_t)c->maxP * cfg->ffn) == cudaSuccess &&
+         dalloc(&c->d_xs, (size_t)c->maxP * cfg->hidden) == cudaSuccess;
+    if (ok && (make_gemm_maps(c->d_xs, cfg->hidden, c->maxP, &c->xs_maps) != cudaSuccess ||
+               make_gemm_maps(c->d_h16, cfg->ffn, c->maxP, &c->h16_maps) != cudaSuccess))
+      return fail(MOE_ERR_CUDA);
+  }
   if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
     c->staging_blocks = std::min(S, c->maxU);
     ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess;
@@ -454,6 +468,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.hdr = c->d_hdr;
   pa.err_flag = c->d_err;
   pa.sync = c->d_sync;
+  const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
+  pa.sync_n = 2 + maxU + (use_decode ? T * (g.hidden / 32) : 0);
   pa.mailbox = need_host ? c->d_mail : nullptr;
   pa.mailbox_stage_cap = c->mail_stage_cap;
   pa.seq = c->seq;
@@ -579,7 +595,13 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     return MOE_OK;
   };
 
-  if (!need_host && fused_ok) {
+  if (use_decode) {
+    // pull fill, single stage, few tokens: the whole layer in one launch after
+    // the plan (misses from the mapped host store, hits from their slots)
+    const uint8_t *host_layer = static_cast<const uint8_t *>(c->host_dev) + (size_t)layer * c->store.layer_stride;
+    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, c->d_w, c->d_h, c->d_u,
+                                             static_cast<float *>(d_out), c->d_sync, 2 + maxU, T, c->n_sms, st));
+  } else if (!need_host && fused_ok) {
     // pull fill, single stage guaranteed, few tokens: misses read once from the
     // host store and computed on the way; hits computed beside them
     int rc = fused_stage0(c->ev_plan, maxU, false);
@@ -604,7 +626,9 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     // tensor-core grouped GEMM; stage-0 hits start before the copies are issued
     const int maxG = std::min(c->maxGunits, maxU + (P + kGemmN - 1) / kGemmN + 1);
     const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(d_x);
-    MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(fa, xb, c->d_gunits, c->d_gunit_begin, c->d_h16, 0, 0, maxG, st));
+    MOE_LAUNCH(K_GATHER, launch_gather_sorted(xb, c->d_perm, P, k, g.hidden, c->d_xs, st));
+    MOE_LAUNCH(K_GEMM_GATEUP,
+               launch_gemm_gateup(fa, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 0, 0, maxG, st));
     int rc = wait_mailbox(c, c->seq, st);
     if (rc != MOE_OK) return poison(c, rc);
     const PlanHdr hdr = c->h_mail->hdr;
@@ -620,8 +644,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       }
       const int sg = std::min(maxG, S + (P + kGemmN - 1) / kGemmN + 1);  // units of one stage, bound
       MOE_LAUNCH(K_GEMM_GATEUP,
-                 launch_gemm_gateup(fa, xb, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
-      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fa, c->d_h16, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
+                 launch_gemm_gateup(fa, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
+      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fa, c->h16_maps, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
       if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
     }
     MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));

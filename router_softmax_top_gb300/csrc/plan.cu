@@ -192,7 +192,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     e_stage[e] = -1;
   }
   for (int i = tid; i < NW * E; i += NT) wcnt[i] = 0;
-  for (int i = tid; i <= (E < P ? E : P); i += NT) a.sync[i] = 0;
+  for (int i = tid; i < a.sync_n; i += NT) a.sync[i] = 0;
   if (tid < 8) scal[tid] = 0;
   const unsigned long long now = *a.clock + 1ull;
   __syncthreads();
@@ -475,8 +475,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const unsigned long long now = *a.clock + 1ull;
   if (lane == 0) s_bad = 0;
   if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
-  a.sync[lane] = 0;  // P <= 32: 33 counters
-  if (lane == 0) a.sync[32] = 0;
+  for (int i = lane; i < a.sync_n; i += 32) a.sync[i] = 0;
   __syncwarp();
   for (int t = 0; t < T; ++t) {
     if (E <= 256) route_token<8>(a.logits + (size_t)t * E, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
