@@ -173,11 +173,14 @@ def moe_expert_ffn_static(d_expert_block: int, hidden: int, ffn: int, d_x: int, 
 
 # ------------------------------------------------------- tensor-level API
 class MoECache:
-    """One cache over a pinned host store, for PyTorch tensors.
+    """One cache over a host store, for PyTorch tensors.
 
-    store: a CPU uint8 tensor (pinned, e.g. ``torch.empty(n, dtype=torch.uint8,
-    pin_memory=True)``) or a (host address, nbytes) pair, holding canonical Q4_0
-    expert blocks [layer][expert] (block = gate | up | down)."""
+    store: a CPU uint8 tensor or a (host address, nbytes) pair, holding
+    canonical Q4_0 expert blocks [layer][expert] (block = gate | up | down).
+    Ordinary memory is pinned and mapped by the library (cudaHostRegister) for
+    the lifetime of the cache; already pinned memory is used as it is.  On a
+    Grace host, ordinary (e.g. mmap'd) memory registered this way reads over
+    the host link faster and more steadily than a cudaHostAlloc buffer."""
 
     def __init__(self, *, n_layers, n_experts, top_k, hidden, ffn, slots_per_layer, max_tokens,
                  store, weight_mode=0, act_dtype="f32", fill_mode=MOE_FILL_MEMCPY,

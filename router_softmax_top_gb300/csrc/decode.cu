@@ -161,13 +161,17 @@ __device__ __forceinline__ void load_block(const unsigned char *buf, bool miss, 
   }
 }
 
+// Launched as a programmatic dependent of the plan kernel: everything before
+// griddepcontrol.wait (barriers, the staged inputs) overlaps the plan; nothing
+// the plan writes is read before it.
+__device__ __forceinline__ void wait_plan() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <int NB, int TMAX>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const DecodeJob j) {
   const PlanHdr *hd = j.hdr;
-  if (hd->error) return;
   QueueShape qs;
-  qs.nH = hd->n_hits;
-  qs.nM = hd->n_stage0_miss;
+  qs.nH = 0;
+  qs.nM = 0;
   qs.tF = j.F / 32;
   qs.tH = j.H / 32;
   qs.DG = j.DG;
@@ -208,6 +212,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
 
   if (warp == kWarps) {
     // ---- producer: claim items in order, bulk-copy each one's tiles into the ring
+    wait_plan();
+    if (hd->error) return;
+    qs.nH = hd->n_hits;
+    qs.nM = hd->n_stage0_miss;
     if (lane == 0) {
       // miss CTAs serve the miss queue, then help with the hits; hit CTAs never
       // take a miss item: a GPU-scope fence waits for the CTA's copies in
@@ -278,6 +286,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
   if (warp == kWarps + 1) {
     // ---- publisher: after an item's outputs are stored, make them visible and
     // count them; the last down tile of a (token, row tile) does its combine
+    wait_plan();
+    if (hd->error) return;
+    qs.nH = hd->n_hits;
+    qs.nM = hd->n_stage0_miss;
     for (int c = 0;; ++c) {
       const int p = c % kPubSlots;
       int ok = 1;
@@ -349,6 +361,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
     if (lane == 0) xsum[i] = v;
   }
   compute_sync();
+  wait_plan();
+  if (hd->error) return;
+  qs.nH = hd->n_hits;
+  qs.nM = hd->n_stage0_miss;
 
   int c = 0;
   for (;; ++c) {
@@ -519,25 +535,24 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   // three items in flight per CTA when they fit, else two
   const bool nb3 = decode_smem(a.H, a.F, T, 3) <= kDecodeSmemCap;
   const size_t smem = decode_smem(a.H, a.F, T, nb3 ? 3 : 2);
-  cudaError_t e;
-  if (T == 1 && nb3) {
-    static size_t cur = 0;
-    if ((e = ensure_dyn_smem(decode_layer_kernel<3, 1>, smem, cur)) != cudaSuccess) return e;
-    decode_layer_kernel<3, 1><<<n_sms, kDecodeThreads, smem, st>>>(j);
-  } else if (T == 1) {
-    static size_t cur = 0;
-    if ((e = ensure_dyn_smem(decode_layer_kernel<2, 1>, smem, cur)) != cudaSuccess) return e;
-    decode_layer_kernel<2, 1><<<n_sms, kDecodeThreads, smem, st>>>(j);
-  } else if (nb3) {
-    static size_t cur = 0;
-    if ((e = ensure_dyn_smem(decode_layer_kernel<3, kTokPerUnit>, smem, cur)) != cudaSuccess) return e;
-    decode_layer_kernel<3, kTokPerUnit><<<n_sms, kDecodeThreads, smem, st>>>(j);
-  } else {
-    static size_t cur = 0;
-    if ((e = ensure_dyn_smem(decode_layer_kernel<2, kTokPerUnit>, smem, cur)) != cudaSuccess) return e;
-    decode_layer_kernel<2, kTokPerUnit><<<n_sms, kDecodeThreads, smem, st>>>(j);
-  }
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_sms);
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  auto go = [&](auto kern, size_t &cur) -> cudaError_t {
+    const cudaError_t e = ensure_dyn_smem(kern, smem, cur);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, kern, j);
+  };
+  static size_t c31 = 0, c21 = 0, c38 = 0, c28 = 0;
+  if (T == 1) return nb3 ? go(decode_layer_kernel<3, 1>, c31) : go(decode_layer_kernel<2, 1>, c21);
+  return nb3 ? go(decode_layer_kernel<3, kTokPerUnit>, c38) : go(decode_layer_kernel<2, kTokPerUnit>, c28);
 }
 
 }  // namespace moe

@@ -86,27 +86,37 @@ __device__ void route_token(const float *row, int E, int k, int weight_mode, int
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
 
+  // k rounds: the largest remaining value, ties to the lower id.  A value's
+  // key orders like the float (-0 taken as +0); one warp max over keys, then
+  // one warp min over the ids holding that key.
+  uint32_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const uint32_t b = __float_as_uint(v[i] == 0.f ? 0.f : v[i]);
+    key[i] = (i * 32 + lane < E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
+  }
   uint32_t taken = 0;
   float my_p = 0.f;
   int my_id = -1;
   for (int q = 0; q < k; ++q) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t bk = 0;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = i * 32 + lane;
-      if (e < E && !((taken >> i) & 1u)) {
-        if (v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
-      }
-    }
+    for (int i = 0; i < VPL; ++i)
+      if (i * 32 + lane < E && !((taken >> i) & 1u) && key[i] > bk) bk = key[i];
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    uint32_t bi = 0xffffffffu;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == q) { my_p = expf(bv - m) / z; my_id = bi; }
+    for (int i = 0; i < VPL; ++i)
+      if (i * 32 + lane < E && !((taken >> i) & 1u) && key[i] == mk && (uint32_t)(i * 32 + lane) < bi)
+        bi = (uint32_t)(i * 32 + lane);
+    const int id = (int)__reduce_min_sync(0xffffffffu, bi);
+    if ((id & 31) == lane) taken |= 1u << (id >> 5);
+    // the chosen value, from its owner lane
+    float ov = 0.f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) ov = (i == (id >> 5)) ? v[i] : ov;
+    const float bvv = __shfl_sync(0xffffffffu, ov, id & 31);
+    if (lane == q) { my_p = expf(bvv - m) / z; my_id = id; }
   }
   float sum = lane < k ? my_p : 0.f;
 #pragma unroll
@@ -159,6 +169,7 @@ __device__ __forceinline__ MissItem miss_record(int i, int n0, int S, const int 
 }
 
 __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");  // see plan_small_kernel
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int E = a.E, S = a.S, k = a.k, T = a.T;
   const int P = T * k;
@@ -458,6 +469,9 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
 constexpr int kSmallMaxSlots = 256;
 
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
+  // a dependent launched programmatically may start its plan-independent
+  // prologue now; it reads the plan only after this grid has completed
+  asm volatile("griddepcontrol.launch_dependents;");
   const unsigned F = 0xffffffffu;
   const int E = a.E, S = a.S, k = a.k, T = a.T, P = T * k;
   const int lane = threadIdx.x;
@@ -466,6 +480,8 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ int s_se[kSmallMaxSlots];
   __shared__ unsigned long long s_st[kSmallMaxSlots];
   __shared__ int s_es[kMaxExperts];
+  __shared__ unsigned long long s_pack[kMaxExperts];
+  __shared__ unsigned long long s_key[kSmallMaxSlots];
   // the whole per-layer state in one round of loads, issued before the router
   for (int i = lane; i < S; i += 32) {
     s_se[i] = a.slot_expert[i];
@@ -498,47 +514,86 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const bool hit = lead && es0 >= 0, miss = lead && es0 < 0;
   const unsigned hmask = __ballot_sync(F, hit), mmask = __ballot_sync(F, miss);
   const int nH = __popc(hmask), nM = __popc(mmask), nU = nH + nM;
-  int hr = 0, mr = 0;
-  for (int j = 0; j < 32; ++j) {
-    const int ej = __shfl_sync(F, e, j);
-    hr += ((hmask >> j) & 1u) && ej < e;
-    mr += ((mmask >> j) & 1u) && ej < e;
-  }
   const int my_hit = __shfl_sync(F, hit ? 1 : 0, leader);
   const int pick_hits = __popc(__ballot_sync(F, act && my_hit));
   if (hit) atomicOr(&s_pinned[es0 >> 5], 1u << (es0 & 31));
-  __syncwarp();
 
-  // stage-0 victims: empty slots (by index), then unpinned slots by (stamp, index)
-  const int nch = (S + 31) / 32;
-  unsigned long long key[kSmallMaxSlots / 32];
+  // per-expert packed counts, 8 bits each: [hit leaders][miss leaders]
+  // [hit pairs][miss pairs][hit units][miss units]; their prefix over expert
+  // ids gives every leader its item rank, pair offset and unit offset in the
+  // item order (hits ascending, then misses ascending)
+  const int ucount = (cnt + kTokPerUnit - 1) / kTokPerUnit;
+  const int csz = (E + 31) / 32;  // experts per lane in the scan
+  for (int i = lane; i < csz * 32; i += 32) s_pack[i] = 0ull;
+  __syncwarp();
+  if (lead)
+    s_pack[e] = hit ? (1ull | ((uint64_t)cnt << 16) | ((uint64_t)ucount << 32))
+                    : ((1ull << 8) | ((uint64_t)cnt << 24) | ((uint64_t)ucount << 40));
+  __syncwarp();
+  uint64_t part = 0;
+  for (int i = 0; i < csz; ++i) part += s_pack[lane * csz + i];
+  uint64_t incl = part;
 #pragma unroll
-  for (int c = 0; c < kSmallMaxSlots / 32; ++c) {
-    key[c] = ~0ull;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint64_t y = __shfl_up_sync(F, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint64_t total = __shfl_sync(F, incl, 31);
+  const int src = lead ? e / csz : 0;
+  uint64_t before = __shfl_sync(F, incl - part, src);  // exclusive prefix of my expert's chunk
+  if (lead)
+    for (int i = src * csz; i < e; ++i) before += s_pack[i];
+  auto field = [](uint64_t v, int f) { return (int)((v >> (8 * f)) & 0xffull); };
+  const int tot_hit_pairs = field(total, 2), tot_hit_units = field(total, 4);
+  const int hr = field(before, 0), mr = field(before, 1);
+
+  // stage-0 victims: empty slots (by index), then unpinned slots by (stamp, index);
+  // miss rank r takes the r-th smallest key
+  __syncwarp();
+  unsigned long long key = ~0ull;
+  for (int c = 0; c * 32 < S; ++c) {
     const int sl = c * 32 + lane;
-    if (c < nch && sl < S && !((s_pinned[c] >> lane) & 1u)) {
+    if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
       const int se = s_se[sl];
-      key[c] = se < 0 ? (unsigned long long)sl
-                      : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
+      const unsigned long long kk =
+          se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
+      key = kk < key ? kk : key;
     }
+  }
+  // lanes hold their smallest remaining key; keys beyond one per lane stay in s_key
+  const int kpl = (S + 31) / 32;
+  if (kpl > 1) {
+    for (int c = 0; c < kpl; ++c) {
+      const int sl = c * 32 + lane;
+      unsigned long long kk = ~0ull;
+      if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
+        const int se = s_se[sl];
+        kk = se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
+      }
+      s_key[sl] = kk;
+    }
+    __syncwarp();
   }
   int my_victim = -1;  // lane r holds the victim of miss rank r
   for (int r = 0; r < nM; ++r) {
-    unsigned long long best = ~0ull;
-#pragma unroll
-    for (int c = 0; c < kSmallMaxSlots / 32; ++c) best = key[c] < best ? key[c] : best;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(F, best, o);
-      best = other < best ? other : best;
-    }
+    const unsigned hi = __reduce_min_sync(F, (unsigned)(key >> 32));
+    const unsigned lo = __reduce_min_sync(F, (unsigned)(key >> 32) == hi ? (unsigned)key : 0xffffffffu);
+    const unsigned long long best = ((unsigned long long)hi << 32) | lo;
     const int sl = (int)(best & 2047ull);
-    if (lane == (sl & 31)) {
-#pragma unroll
-      for (int c = 0; c < kSmallMaxSlots / 32; ++c)
-        if (c == (sl >> 5)) key[c] = ~0ull;
-    }
     if (lane == r) my_victim = sl;
+    if (lane == (sl & 31)) {
+      // the owner drops the taken key and exposes its next smallest
+      if (kpl == 1) {
+        key = ~0ull;
+      } else {
+        s_key[sl] = ~0ull;
+        key = ~0ull;
+        for (int c = 0; c < kpl; ++c) {
+          const unsigned long long kk = s_key[c * 32 + lane];
+          key = kk < key ? kk : key;
+        }
+      }
+    }
   }
   const int vslot = __shfl_sync(F, my_victim, miss ? mr : 0);
   const int my_slot = hit ? es0 : (miss ? vslot : -1);
@@ -565,17 +620,9 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
 
   // work items (hits ascending, then misses ascending), units, perm
   const int item = hit ? hr : (miss ? nH + mr : -1);
-  const int ucount = (cnt + kTokPerUnit - 1) / kTokPerUnit;
-  int pb = 0, ub = 0, hit_units = 0, n_units = 0;
-  for (int j = 0; j < 32; ++j) {
-    const int ij = __shfl_sync(F, item, j);
-    const int cj = __shfl_sync(F, cnt, j);
-    const int uj = (cj + kTokPerUnit - 1) / kTokPerUnit;
-    if (ij < 0) continue;
-    if (ij < item) { pb += cj; ub += uj; }
-    if (ij < nH) hit_units += uj;
-    n_units += uj;
-  }
+  const int pb = hit ? field(before, 2) : tot_hit_pairs + field(before, 3);
+  const int ub = hit ? field(before, 4) : tot_hit_units + field(before, 5);
+  const int n_units = tot_hit_units + field(total, 5);
   if (lead) {
     a.items[item] = WorkItem{e, my_slot, 0, miss ? 1 : 0, pb, cnt};
     for (int j = 0; j < ucount; ++j)
@@ -599,19 +646,19 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     h.n_evict = n_evict;
     h.pick_hits = pick_hits;
     h.pick_misses = P - pick_hits;
-    h.hit_units = hit_units;
+    h.hit_units = tot_hit_units;
     h.hit_gunits = nH;
     *a.hdr = h;
     *a.clock = now;
-    uint64_t *st = a.stats;
-    st[0] += 1;
-    st[1] += (uint64_t)pick_hits;
-    st[2] += (uint64_t)(P - pick_hits);
-    st[3] += (uint64_t)nH;
-    st[4] += (uint64_t)nM;
-    st[5] += (uint64_t)n_evict;
-    st[6] += (uint64_t)nM * a.expert_bytes;
-    st[7] += 1;
+    unsigned long long *st = reinterpret_cast<unsigned long long *>(a.stats);
+    atomicAdd(st + 0, 1ull);
+    atomicAdd(st + 1, (unsigned long long)pick_hits);
+    atomicAdd(st + 2, (unsigned long long)(P - pick_hits));
+    atomicAdd(st + 3, (unsigned long long)nH);
+    atomicAdd(st + 4, (unsigned long long)nM);
+    atomicAdd(st + 5, (unsigned long long)n_evict);
+    atomicAdd(st + 6, (unsigned long long)nM * a.expert_bytes);
+    atomicAdd(st + 7, 1ull);
     if (a.mailbox) {
       a.mailbox->hdr = h;
       int32_t *mub = reinterpret_cast<int32_t *>(a.mailbox + 1);
