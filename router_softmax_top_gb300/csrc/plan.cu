@@ -54,23 +54,26 @@ __device__ V block_scan_array(V *a, int n, V *ws) {
   return total;
 }
 
-// Router for one token, VPL logits per lane (value e = i*32 + lane).
+// One token's logits, VPL per lane (value e = i*32 + lane; -inf past E).
 template <int VPL>
-__device__ void route_token(const float *row, int E, int k, int weight_mode, int32_t *ids,
-                            float *w, int *bad_flag) {
+__device__ __forceinline__ void load_logits(const float *row, int E, float v[VPL]) {
   const int lane = threadIdx.x & 31;
-  float v[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) v[i] = (i * 32 + lane < E) ? row[i * 32 + lane] : -INFINITY;
+}
+
+// Router for one token from its loaded logits.
+template <int VPL>
+__device__ void route_values(const float v[VPL], int E, int k, int weight_mode, int32_t *ids, float *w,
+                             int *bad_flag) {
+  const int lane = threadIdx.x & 31;
   bool bad = false;
   float m = -INFINITY;
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    const int e = i * 32 + lane;
-    v[i] = -INFINITY;
-    if (e < E) {
-      const float x = row[e];
-      if (!isfinite(x)) bad = true;
-      v[i] = x;
-      m = fmaxf(m, x);
+    if (i * 32 + lane < E) {
+      if (!isfinite(v[i])) bad = true;
+      m = fmaxf(m, v[i]);
     }
   }
   if (__any_sync(0xffffffffu, bad)) {
@@ -125,6 +128,15 @@ __device__ void route_token(const float *row, int E, int k, int weight_mode, int
     ids[lane] = my_id;
     w[lane] = weight_mode == 1 ? my_p / sum : my_p;
   }
+}
+
+// Router for one token, VPL logits per lane.
+template <int VPL>
+__device__ void route_token(const float *row, int E, int k, int weight_mode, int32_t *ids,
+                            float *w, int *bad_flag) {
+  float v[VPL];
+  load_logits<VPL>(row, E, v);
+  route_values<VPL>(v, E, k, weight_mode, ids, w, bad_flag);
 }
 
 template <int VPL>
@@ -209,7 +221,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   __syncthreads();
   {
     int *bad = &scal[0];
-    if (E <= 256) route_all<8>(a, bad);
+    if (E <= 128) route_all<4>(a, bad);
+    else if (E <= 256) route_all<8>(a, bad);
     else route_all<32>(a, bad);
   }
   __syncthreads();
@@ -482,7 +495,10 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ int s_es[kMaxExperts];
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
-  // the whole per-layer state in one round of loads, issued before the router
+  // the first token's logits and the whole per-layer state in one round of loads
+  float lg4[4], lg8[8];
+  if (E <= 128) load_logits<4>(a.logits, E, lg4);
+  else if (E <= 256) load_logits<8>(a.logits, E, lg8);
   for (int i = lane; i < S; i += 32) {
     s_se[i] = a.slot_expert[i];
     s_st[i] = a.slot_stamp[i];
@@ -494,8 +510,16 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   for (int i = lane; i < a.sync_n; i += 32) a.sync[i] = 0;
   __syncwarp();
   for (int t = 0; t < T; ++t) {
-    if (E <= 256) route_token<8>(a.logits + (size_t)t * E, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
-    else route_token<32>(a.logits + (size_t)t * E, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+    const float *row = a.logits + (size_t)t * E;
+    if (E <= 128) {
+      if (t > 0) load_logits<4>(row, E, lg4);
+      route_values<4>(lg4, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+    } else if (E <= 256) {
+      if (t > 0) load_logits<8>(row, E, lg8);
+      route_values<8>(lg8, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+    } else {
+      route_token<32>(row, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+    }
   }
   __syncwarp();
   if (s_bad) {
