@@ -149,6 +149,8 @@ struct PlanArgs {
   int32_t *err_flag;  // sticky device error word of the handle
   int32_t *sync;      // per-call counters, the first sync_n zeroed here
   int sync_n;
+  int32_t *route_bad; // device word for the grid router's non-finite flag (zero between calls)
+  int routed;         // set by launch_plan when route_kernel produced ids and w
   Mailbox *mailbox;   // device alias of the mapped host mailbox, or null
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;

@@ -66,6 +66,7 @@ struct moe_cache {
   PlanHdr *d_hdr = nullptr;
   int32_t *d_sync = nullptr;  // per-call counters: queue head, per item, per (token, row tile)
   float *d_u = nullptr;         // up outputs of the decode layer kernel [maxP, F] (gate outputs use d_h)
+  int32_t *d_route_bad = nullptr;  // non-finite-logit flag of the grid router
   int n_sms = 0;
   WorkUnit *d_gunits = nullptr;
   int32_t *d_gunit_begin = nullptr;
@@ -221,6 +222,7 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_hdr);
   cudaFree(c->d_sync);
   cudaFree(c->d_u);
+  cudaFree(c->d_route_bad);
   cudaFree(c->d_gunits);
   cudaFree(c->d_gunit_begin);
   cudaFree(c->d_h16);
@@ -353,6 +355,8 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
   ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 2 + (size_t)cfg->max_tokens * (cfg->hidden / 32)) == cudaSuccess;
   ok = ok && dalloc(&c->d_u, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
+  ok = ok && dalloc(&c->d_route_bad, 1) == cudaSuccess &&
+       cudaMemsetAsync(c->d_route_bad, 0, sizeof(int32_t), (cudaStream_t)cuda_stream) == cudaSuccess;
   c->maxGunits = c->maxU + (c->maxP + kGemmN - 1) / kGemmN + 1;
   ok = ok && dalloc(&c->d_gunits, c->maxGunits) == cudaSuccess;
   ok = ok && dalloc(&c->d_gunit_begin, c->maxStages + 1) == cudaSuccess;
@@ -468,6 +472,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.hdr = c->d_hdr;
   pa.err_flag = c->d_err;
   pa.sync = c->d_sync;
+  pa.route_bad = c->d_route_bad;
+  pa.routed = 0;
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
   pa.sync_n = 2 + maxU + (use_decode ? T * (g.hidden / 32) : 0);
   pa.mailbox = need_host ? c->d_mail : nullptr;

@@ -139,6 +139,16 @@ __device__ void route_token(const float *row, int E, int k, int weight_mode, int
   route_values<VPL>(v, E, k, weight_mode, ids, w, bad_flag);
 }
 
+// Routing of a large call as its own grid: one warp per token; a non-finite
+// logit sets *bad (read and cleared by plan_kernel).
+template <int VPL>
+__global__ void __launch_bounds__(256) route_kernel(const float *logits, int T, int E, int k, int weight_mode,
+                                                  int32_t *ids, float *w, int *bad) {
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  route_token<VPL>(logits + (size_t)t * E, E, k, weight_mode, ids + (size_t)t * k, w + (size_t)t * k, bad);
+}
+
 template <int VPL>
 __device__ void route_all(const PlanArgs &a, int *bad_flag) {
   const int warp = threadIdx.x >> 5;
@@ -219,7 +229,13 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   if (tid < 8) scal[tid] = 0;
   const unsigned long long now = *a.clock + 1ull;
   __syncthreads();
-  {
+  if (a.routed) {
+    // ids and weights come from route_kernel (earlier on the stream)
+    if (tid == 0) {
+      scal[0] = *a.route_bad;
+      *a.route_bad = 0;
+    }
+  } else {
     int *bad = &scal[0];
     if (E <= 128) route_all<4>(a, bad);
     else if (E <= 256) route_all<8>(a, bad);
@@ -480,6 +496,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
 // code: this kernel runs once per layer call, mostly from a cold instruction
 // cache).
 constexpr int kSmallMaxSlots = 256;
+constexpr int kRouteGridMin = 64;  // calls with more tokens route in their own grid
 
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   // a dependent launched programmatically may start its plan-independent
@@ -721,10 +738,25 @@ bool plan_small_ok(int T, int E, int k, int S) {
   return P <= 32 && S <= kSmallMaxSlots && (E < P ? E : P) <= S;
 }
 
-cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st) {
-  if (plan_small_ok(a.T, a.E, a.k, a.S)) {
-    plan_small_kernel<<<1, 32, 0, st>>>(a);
+cudaError_t launch_plan(const PlanArgs &a_in, cudaStream_t st) {
+  if (plan_small_ok(a_in.T, a_in.E, a_in.k, a_in.S)) {
+    plan_small_kernel<<<1, 32, 0, st>>>(a_in);
     return cudaGetLastError();
+  }
+  PlanArgs a = a_in;
+  a.routed = 0;
+  if (a.T > kRouteGridMin && a.route_bad) {
+    // many tokens: route them grid-wide first (one warp per token)
+    const dim3 grid((a.T + 7) / 8);
+    if (a.E <= 128)
+      route_kernel<4><<<grid, 256, 0, st>>>(a.logits, a.T, a.E, a.k, a.weight_mode, a.ids, a.w, a.route_bad);
+    else if (a.E <= 256)
+      route_kernel<8><<<grid, 256, 0, st>>>(a.logits, a.T, a.E, a.k, a.weight_mode, a.ids, a.w, a.route_bad);
+    else
+      route_kernel<32><<<grid, 256, 0, st>>>(a.logits, a.T, a.E, a.k, a.weight_mode, a.ids, a.w, a.route_bad);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    a.routed = 1;
   }
   const size_t smem = plan_smem_bytes(a.E, a.S);
   static size_t cur = 0;

@@ -79,6 +79,36 @@ def test_non_finite_logit_poisons(store, fill_mode, bad):
     c.close()
 
 
+@pytest.mark.parametrize("fill_mode", [0, 1])
+def test_non_finite_logit_large_call_poisons(store, fill_mode):
+    # more than 64 tokens: routing runs in its own grid and reports through a
+    # device flag that the plan kernel reads
+    import numpy as np
+    import torch
+    T = 100
+    c = _cache(store, fill_mode=fill_mode, max_tokens=T)
+    rng = np.random.default_rng(7)
+    lg = torch.from_numpy(rng.standard_normal((T, TINY.E)).astype(np.float32)).cuda()
+    x = torch.from_numpy(rng.standard_normal((T, TINY.H)).astype(np.float32)).cuda()
+    out = torch.empty((T, TINY.H), device="cuda")
+    c.forward(0, lg, x, out)
+    before = c.stats(0)
+    lg2 = lg.clone()
+    lg2[77, 5] = float("nan")
+    rc = c.forward_rc(0, lg2, x, out)
+    if rc == moe.MOE_OK:
+        rc = c.sync()
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    st = c.stats(0)
+    assert st["poisoned"] == 1 and st["calls"] == before["calls"]
+    c.close()
+    # a fresh handle on the same device routes large calls normally again
+    c = _cache(store, fill_mode=fill_mode, max_tokens=T)
+    c.forward(0, lg, x, out)
+    assert c.stats(0)["calls"] == 1 and c.stats(0)["poisoned"] == 0
+    c.close()
+
+
 def test_timeout_on_host_wait_poisons(store):
     # a host wait limit shorter than any kernel launch: the mailbox wait gives up
     import torch
