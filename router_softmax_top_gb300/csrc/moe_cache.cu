@@ -53,6 +53,8 @@ struct moe_cache {
 
   // persistent device state
   uint8_t *d_slots = nullptr;
+  uint8_t *d_stage_buf = nullptr;  // 2 x S blocks (slot layout): stages >= 1 of staged calls
+  cudaEvent_t ev_fin = nullptr;
   int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
   uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
 
@@ -203,6 +205,8 @@ cudaError_t dalloc(T **p, size_t n) {
 
 void free_all(moe_cache *c) {
   cudaFree(c->d_slots);
+  cudaFree(c->d_stage_buf);
+  if (c->ev_fin) cudaEventDestroy(c->ev_fin);
   cudaFree(c->d_slot_expert);
   cudaFree(c->d_expert_slot);
   cudaFree(c->d_slot_stamp);
@@ -336,6 +340,11 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   // device memory
   const size_t slot_bytes = (size_t)L * S * c->lay.stride;
   bool ok = cudaMalloc(&c->d_slots, slot_bytes) == cudaSuccess;
+  // staged calls (more distinct experts than slots) are possible: stages >= 1
+  // alternate between two stage buffers, so that a stage's fill overlaps the
+  // previous stage's compute
+  if (ok && std::min(E, cfg->max_tokens * cfg->top_k) > S)
+    ok = cudaMalloc(&c->d_stage_buf, (size_t)2 * S * c->lay.stride) == cudaSuccess;
   ok = ok && dalloc(&c->d_slot_expert, (size_t)L * S) == cudaSuccess;
   ok = ok && dalloc(&c->d_expert_slot, (size_t)L * E) == cudaSuccess;
   ok = ok && dalloc(&c->d_slot_stamp, (size_t)L * S) == cudaSuccess;
@@ -396,7 +405,13 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   c->d_err = static_cast<int32_t *>(dm);
 
   // streams and events
-  if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  // the side stream carries the fills: highest priority, so that its kernels
+  // get SMs ahead of the compute kernels they overlap
+  int prio_lo = 0, prio_hi = 0;
+  if (cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi) != cudaSuccess ||
+      cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_hi) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_fin, cudaEventDisableTiming) != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
   if (cudaEventCreateWithFlags(&c->ev_plan, cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
   c->ev_up.resize(c->maxStages);
   c->ev_done.resize(c->maxStages);
@@ -518,11 +533,24 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   if (cudaEventRecord(c->ev_plan, st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
   const bool dc_ok = down_combine_supported(g.ffn, k);
 
-  // fill of stage j's misses on the side stream, after `after` (recorded on st);
-  // the main stream then waits for it.  src_host: pull from the mapped store.
-  auto fill_stage = [&](int j, int nmiss, cudaEvent_t after, int mlo, bool from_mailbox) -> int {
+  // Where stage j's misses live: stage 0 in their slots; later stages (whose
+  // i-th miss takes slot i) alternately in the two stage buffers, so that the
+  // fill of stage j + 1 overlaps the compute of stage j.
+  uint8_t *const layer_slots = c->d_slots + (size_t)layer * S * c->lay.stride;
+  auto stage_base = [&](int j) -> uint8_t * {
+    return (j == 0 || !c->d_stage_buf) ? layer_slots : c->d_stage_buf + (size_t)(j & 1) * S * c->lay.stride;
+  };
+  // the event after which stage j's destination is free
+  auto stage_free = [&](int j) -> cudaEvent_t { return j < 2 ? c->ev_plan : c->ev_done[j - 2]; };
+
+  // fill of stage j's misses on the side stream: host copies (memcpy mode)
+  // after `after`, the repack into the stage's destination after `dst_free`;
+  // the main stream then waits for it.
+  auto fill_stage = [&](int j, int nmiss, cudaEvent_t after, cudaEvent_t dst_free, int mlo,
+                        bool from_mailbox) -> int {
     if (cudaStreamWaitEvent(c->side, after, 0) != cudaSuccess) return MOE_ERR_CUDA;
     ra.stage = j;
+    ra.slots = stage_base(j);
     if (g.fill_mode == MOE_FILL_MEMCPY) {
       {
         Launch l(c, K_MEMCPY, c->side);
@@ -549,6 +577,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       ra.src_slot_stride = 0;
       ra.by_expert = 1;
     }
+    if (dst_free != after && cudaStreamWaitEvent(c->side, dst_free, 0) != cudaSuccess) return MOE_ERR_CUDA;
     {
       Launch l(c, K_REPACK, c->side);
       if (launch_repack(ra, S, nmiss, c->side) != cudaSuccess) return MOE_ERR_CUDA;
@@ -558,12 +587,34 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       return MOE_ERR_CUDA;
     return MOE_OK;
   };
+  // After a staged call: the blocks the final state maps live in the stage
+  // buffers for stages >= 1; copy them into their slots (slots [0, mL) from
+  // the last stage, [mL, S) from the one before when that one is >= 1), once
+  // stage 0's compute no longer reads the slots.  The main stream waits.
+  auto finalize_stages = [&](int n_st, int n0, int nM) -> int {
+    if (n_st < 2) return MOE_OK;
+    const int jL = n_st - 1, mL = std::min(nM, n0 + jL * S) - (n0 + (jL - 1) * S);
+    if (cudaStreamWaitEvent(c->side, c->ev_done[0], 0) != cudaSuccess) return MOE_ERR_CUDA;
+    const size_t stride = c->lay.stride;
+    if (mL > 0 &&
+        cudaMemcpyAsync(layer_slots, stage_base(jL), (size_t)mL * stride, cudaMemcpyDeviceToDevice, c->side) !=
+            cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (jL - 1 >= 1 && mL < S &&
+        cudaMemcpyAsync(layer_slots + (size_t)mL * stride, stage_base(jL - 1) + (size_t)mL * stride,
+                        (size_t)(S - mL) * stride, cudaMemcpyDeviceToDevice, c->side) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (cudaEventRecord(c->ev_fin, c->side) != cudaSuccess || cudaStreamWaitEvent(st, c->ev_fin, 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  };
 
   const bool fused_ok = T <= kTokPerUnit && fused_miss_supported(g.hidden, g.ffn);
 
   // misses of a single-stage call through the fused kernel on the side stream
   // (after `after`), the main stream waiting for it before the combine
   auto fused_stage0 = [&](cudaEvent_t after, int nmiss_max, bool copies) -> int {
+    ra.slots = layer_slots;
     if (cudaStreamWaitEvent(c->side, after, 0) != cudaSuccess) return MOE_ERR_CUDA;
     if (g.fill_mode == MOE_FILL_MEMCPY) {
       if (copies) {
@@ -619,7 +670,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   } else if (!need_host) {
     // pull fill, single stage guaranteed: the fill overlaps the hit gate/up
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
-    int rc = fill_stage(0, maxU, c->ev_plan, 0, false);  // main waits for it from here on
+    int rc = fill_stage(0, maxU, c->ev_plan, c->ev_plan, 0, false);  // main waits for it from here on
     if (rc != MOE_OK) return poison(c, rc);
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, 0, maxUnits, st));
     if (dc_ok) {
@@ -645,15 +696,19 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
       const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
       if (mhi > mlo) {
-        rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+        rc = fill_stage(j, mhi - mlo, c->ev_plan, stage_free(j), mlo, true);
         if (rc != MOE_OK) return poison(c, rc);
       }
+      FfnArgs fj = fa;
+      fj.slots = stage_base(j);
       const int sg = std::min(maxG, S + (P + kGemmN - 1) / kGemmN + 1);  // units of one stage, bound
       MOE_LAUNCH(K_GEMM_GATEUP,
-                 launch_gemm_gateup(fa, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
-      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fa, c->h16_maps, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
-      if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+                 launch_gemm_gateup(fj, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
+      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fj, c->h16_maps, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
+      if (cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
     }
+    rc = finalize_stages(n_st, n0, nM);
+    if (rc != MOE_OK) return poison(c, rc);
     MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
   } else {
     MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 0, 0, maxUnits, st));
@@ -677,21 +732,24 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
         const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
         const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
         if (mhi > mlo) {
-          rc = fill_stage(j, mhi - mlo, j == 0 ? c->ev_plan : c->ev_done[j - 1], mlo, true);
+          rc = fill_stage(j, mhi - mlo, c->ev_plan, stage_free(j), mlo, true);
           if (rc != MOE_OK) return poison(c, rc);
         }
+        FfnArgs fj = fa;
+        fj.slots = stage_base(j);
         const int ulo = j == 0 ? hdr.hit_units : c->h_mail_ub[j];
         const int uhi = c->h_mail_ub[j + 1];
-        if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fa, 1, j, uhi - ulo, st));
+        if (uhi > ulo) MOE_LAUNCH(K_GATEUP, launch_gateup(fj, 1, j, uhi - ulo, st));
         if (n_st == 1 && dc_ok) {
-          MOE_LAUNCH(K_DOWN, launch_down_combine(fa, c->d_w, c->d_gpu_slot, T, d_out, st));
+          MOE_LAUNCH(K_DOWN, launch_down_combine(fj, c->d_w, c->d_gpu_slot, T, d_out, st));
         } else {
           const int dlo = c->h_mail_ub[j];
-          if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fa, 2, j, uhi - dlo, st));
-          if (j + 1 < n_st && cudaEventRecord(c->ev_done[j], st) != cudaSuccess)
-            return poison(c, MOE_ERR_CUDA);
+          if (uhi > dlo) MOE_LAUNCH(K_DOWN, launch_down(fj, 2, j, uhi - dlo, st));
+          if (cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
         }
       }
+      rc = finalize_stages(n_st, n0, nM);
+      if (rc != MOE_OK) return poison(c, rc);
       if (n_st > 1 || !dc_ok)
         MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
     }
