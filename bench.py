@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernel-pass", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="decode: time eager layer calls instead of the captured step graph")
     ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0,
                     help="decode: run only the first N layers of the model (profiling captures); 0 = all")
@@ -351,7 +353,8 @@ def main():
     W, K = args.warmup, args.steps
     assert W >= 3 and K >= 1
     t_setup = time.time()
-    nsteps = W + 3 * K
+    G0 = 2                        # graph warm-up steps (capture and first replays)
+    nsteps = W + G0 + 3 * K
     eb = sh.expert_bytes
     store = host_store(sh.L * sh.E * eb)
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
@@ -393,6 +396,40 @@ def main():
     cold_ms = e0.elapsed_time(e1)
     st1 = cache.stats(-1)
 
+    # ---- one step (all layer calls) captured as a CUDA graph: the timed region
+    # replays it, each step's inputs copied into the captured input buffers
+    # (device to device); the pull-fill single-token schedule has no host wait
+    graph = None
+    launches_per_step = None
+    if not args.no_graph and fill == moe.MOE_FILL_PULL:
+        lg_cur = torch.empty((sh.L, 1, sh.E), dtype=torch.float32, device="cuda")
+        x_cur = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
+        lc = [ctypes.c_void_p(lg_cur[l].data_ptr()) for l in range(sh.L)]
+        xc = [ctypes.c_void_p(x_cur[l].data_ptr()) for l in range(sh.L)]
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        n0 = cache.launch_count()
+        with torch.cuda.graph(graph, stream=cap):
+            cs = ctypes.c_void_p(cap.cuda_stream)
+            for l in range(sh.L):
+                rc = fwd(handle, l, lc[l], xc[l], 1, o_ptr[l], cs)
+                if rc != 0:
+                    raise moe.MoeError(rc, f"moe_layer_forward (capture) layer {l}")
+        launches_per_step = cache.launch_count() - n0
+
+        def run_graph(s0, s1):
+            for s in range(s0, s1):
+                lg_cur.copy_(logits_d[s], non_blocking=True)
+                x_cur.copy_(x_d[s], non_blocking=True)
+                graph.replay()
+        run_graph(W, W + G0)
+    else:
+        run_steps(W, W + G0)
+    torch.cuda.synchronize()
+    st1t = cache.stats(-1)    # baseline of the timed region
+    W1 = W + G0
+
     # ---- timed region: K steps, inputs resident in HBM
     clocks = ClockSampler(local)
     clocks.start()
@@ -400,11 +437,14 @@ def main():
     torch.cuda.synchronize()
     n_launch0 = cache.launch_count()
     e0.record()
-    run_steps(W, W + K)
+    if graph is not None:
+        run_graph(W1, W1 + K)
+    else:
+        run_steps(W1, W1 + K)
     e1.record()
     torch.cuda.synchronize()
     barrier()
-    n_launch = cache.launch_count() - n_launch0
+    n_launch = (launches_per_step * K if graph is not None else cache.launch_count() - n_launch0)
     dev_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     st2 = cache.stats(-1)
@@ -415,7 +455,7 @@ def main():
     if not args.no_kernel_pass:
         cache.set_timing(True)
         e0.record()
-        run_steps(W + K, W + 2 * K)
+        run_steps(W1 + K, W1 + 2 * K)
         e1.record()
         torch.cuda.synchronize()
         kpass_ms = e0.elapsed_time(e1)
@@ -436,7 +476,7 @@ def main():
         barrier()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for i, s in enumerate(range(W + 2 * K, W + 3 * K)):
+        for i, s in enumerate(range(W1 + 2 * K, W1 + 3 * K)):
             lg_step.copy_(lg_pin[s], non_blocking=True)
             x_step.copy_(x_pin[s], non_blocking=True)
             for l in range(sh.L):
@@ -465,7 +505,7 @@ def main():
 
     # ---- roofline of the dominant kernel and of the whole step
     hbm_peak, _, peak_kind = measured_peaks()
-    d = {key: st2[key] - st1[key] for key in st2 if key not in ("poisoned", "last_error")}
+    d = {key: st2[key] - st1t[key] for key in st2 if key not in ("poisoned", "last_error")}
     dk = {key: st3[key] - st2[key] for key in st3 if key not in ("poisoned", "last_error")}
     uniq = d["unique_hits"] + d["unique_misses"]
     uniq_k = dk["unique_hits"] + dk["unique_misses"]
@@ -555,6 +595,7 @@ def main():
                     if v["launches"]},
         "kernel_pass_ms_per_step": kpass_ms / K,
         "gpu_launches": int(n_launch),
+        "step_graph": graph is not None,
         "clocks": clk,
         "e2e": e2e,
         "setup_s": setup_s,

@@ -39,7 +39,9 @@ using namespace q4;
 
 constexpr uint64_t kDecodeWaitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr int kPubSlots = 4;
-constexpr int kDecodeThreads = kThreads + 64;     // 8 compute warps, producer, publisher
+// per CTA: GROUPS groups of 8 compute warps (each group works on its own
+// items), a producer warp and a publisher warp
+__host__ __device__ constexpr int decode_threads(int groups) { return groups * kThreads + 64; }
 constexpr int kHitQueue = 1 << 30;                 // claim code flag: item of the hit queue
 constexpr int kMissCtas = 48;                      // CTAs that serve the miss queue first
 
@@ -119,16 +121,29 @@ int decode_down_group(int H, int F) {
     if (g * dn <= gu) return g;
   return 1;
 }
-size_t decode_smem(int H, int F, int T, int NB) {
+// shared memory: NB ring slots, the call's inputs [T][H] and their block sums,
+// and per compute group one down item's inputs [T][F], their block sums and
+// the warp partials [8][T][32]
+// (rounded to 32 floats: each group's inputs are read with 16-byte loads)
+__host__ __device__ inline size_t decode_group_floats(int F, int T) {
+  const size_t n = (size_t)T * F + (size_t)T * (F / 32) + (size_t)kWarps * T * 32;
+  return (n + 31) / 32 * 32;
+}
+size_t decode_smem(int H, int F, int T, int NB, int groups) {
   return (size_t)NB * decode_slot_bytes(H, F, decode_down_group(H, F)) +
-         sizeof(float) * ((size_t)T * H + (size_t)T * (H / 32) + (size_t)T * F + (size_t)T * (F / 32) +
-                          (size_t)kWarps * T * 32);
+         sizeof(float) * ((size_t)T * H + (size_t)T * (H / 32) + (size_t)groups * decode_group_floats(F, T));
 }
 constexpr size_t kDecodeSmemCap = 226 * 1024;
 
 // Compute warps (0-7) synchronise among themselves with a named barrier; the
 // producer (warp 8) and publisher (warp 9) run beside them on mbarriers.
-__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory"); }
+__device__ __forceinline__ void group_sync(int group) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + group), "n"(kThreads) : "memory");
+}
+template <int GROUPS>
+__device__ __forceinline__ void all_compute_sync() {
+  asm volatile("bar.sync 3, %0;" ::"n"(GROUPS * kThreads) : "memory");
+}
 
 __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity) {
   uint64_t t0 = 0;
@@ -166,8 +181,8 @@ __device__ __forceinline__ void load_block(const unsigned char *buf, bool miss, 
 // the plan writes is read before it.
 __device__ __forceinline__ void wait_plan() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <int NB, int TMAX>
-__global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const DecodeJob j) {
+template <int NB, int TMAX, int GROUPS>
+__global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel(const DecodeJob j) {
   const PlanHdr *hd = j.hdr;
   QueueShape qs;
   qs.nH = 0;
@@ -184,12 +199,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
   unsigned char *ring = sm;
   float *xs = reinterpret_cast<float *>(sm + NB * slot_bytes);  // [T][H]: the call's inputs
   float *xsum = xs + (size_t)T * j.H;                           // [T][H/32]
-  float *hs = xsum + (size_t)T * nbH;                           // [T][F]: one down item's inputs
-  float *hsum = hs + (size_t)T * j.F;                           // [T][F/32]
-  float *red = hsum + (size_t)T * nbF;                          // [warps][T][32]
+float *gbase = xsum + (size_t)T * nbH;                        // per compute group, below
   __shared__ __align__(8) uint64_t full[NB], empty[NB], pub[kPubSlots], pubfree[kPubSlots], published;
   __shared__ int s_item[NB], s_pub[kPubSlots];
-  __shared__ int s_ok, s_ok_down;  // decisions of thread 0, each read after a barrier
+  __shared__ int s_ok[GROUPS], s_ok_down[GROUPS];  // decisions of a group's thread 0, read after a barrier
 
   auto mat_of = [&](int mat) -> const MatLayout & {
     return mat == 0 ? j.lay.gate : mat == 1 ? j.lay.up : j.lay.down;
@@ -205,12 +218,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
     }
     mbar_init(&published, 1);
     fence_mbar_init();
-    s_ok = 1;
-    s_ok_down = 1;
+    for (int g = 0; g < GROUPS; ++g) s_ok[g] = s_ok_down[g] = 1;
   }
   __syncthreads();
 
-  if (warp == kWarps) {
+  if (warp == GROUPS * kWarps) {
     // ---- producer: claim items in order, bulk-copy each one's tiles into the ring
     wait_plan();
     if (hd->error) return;
@@ -253,8 +265,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
           second = true;
         }
         if (code < 0) {
-          s_item[s] = -1;
-          mbar_arrive(&full[s]);
+          // the end of the list, once for each compute group
+          for (int c2 = c; c2 < c + GROUPS; ++c2) {
+            const int s2 = c2 % NB;
+            if (c2 > c && c2 >= NB && !ring_wait(&empty[s2], (uint32_t)((c2 / NB) - 1) & 1u)) break;
+            s_item[s2] = -1;
+            mbar_arrive(&full[s2]);
+          }
           break;
         }
         if (code & kHitQueue) sequential = false;  // HBM reads only from here on
@@ -283,7 +300,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
     return;
   }
 
-  if (warp == kWarps + 1) {
+  if (warp == GROUPS * kWarps + 1) {
     // ---- publisher: after an item's outputs are stored, make them visible and
     // count them; the last down tile of a (token, row tile) does its combine
     wait_plan();
@@ -346,35 +363,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
   for (int t = 0; t < T; ++t) {
     if (j.x_bf16) {
       const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(j.x) + (size_t)t * j.H;
-      for (int c = tid; c < j.H; c += kThreads) xs[t * j.H + c] = __bfloat162float(src[c]);
+      for (int c = tid; c < j.H; c += GROUPS * kThreads) xs[t * j.H + c] = __bfloat162float(src[c]);
     } else {
       const float4 *src = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(j.x) + (size_t)t * j.H);
       float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * j.H);
-      for (int c = tid; c < j.H / 4; c += kThreads) dst[c] = src[c];
+      for (int c = tid; c < j.H / 4; c += GROUPS * kThreads) dst[c] = src[c];
     }
   }
-  compute_sync();
-  for (int i = warp; i < T * nbH; i += kWarps) {
+  all_compute_sync<GROUPS>();
+  for (int i = warp; i < T * nbH; i += GROUPS * kWarps) {
     float v = xs[(size_t)i * 32 + lane];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0) xsum[i] = v;
   }
-  compute_sync();
+  all_compute_sync<GROUPS>();
+  // this warp's group, and its thread and warp index within the group
+  const int group = warp / kWarps;
+  const int gtid = tid - group * kThreads;
+  const int gwarp = warp - group * kWarps;
+  float *hs = gbase + (size_t)group * decode_group_floats(j.F, T);  // [T][F]: one down item's inputs
+  float *hsum = hs + (size_t)T * j.F;                                // [T][F/32]
+  float *red = hsum + (size_t)T * nbF;                               // [warps][T][32]
   wait_plan();
   if (hd->error) return;
   qs.nH = hd->n_hits;
   qs.nM = hd->n_stage0_miss;
 
-  int c = 0;
-  for (;; ++c) {
+  int c = group;
+  for (;; c += GROUPS) {
     const int s = c % NB;
     const uint32_t parity = (uint32_t)(c / NB) & 1u;
     // one thread waits (bounded) and shares the decision, so that every
     // compute thread leaves the loop together
-    if (tid == 0) s_ok = ring_wait(&full[s], parity) ? 1 : 0;
-    compute_sync();
-    if (!s_ok) {
+    if (gtid == 0) s_ok[group] = ring_wait(&full[s], parity) ? 1 : 0;
+    group_sync(group);
+    if (!s_ok[group]) {
       flag_error(j.err, 3);
       break;
     }
@@ -393,7 +417,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
 
     if (is_down) {
       // h of this expert needs all of its gate and up tiles
-      if (tid == 0) {
+      if (gtid == 0) {
         int ok = 0;
         uint64_t t0 = 0;
         for (uint32_t i = 0; i < kSpinLimit; ++i) {
@@ -405,29 +429,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
             else if (t - t0 > kDecodeWaitNs) break;
           }
         }
-        s_ok_down = ok;
+        s_ok_down[group] = ok;
       }
-      compute_sync();
-      if (!s_ok_down) {
+      group_sync(group);
+      if (!s_ok_down[group]) {
         flag_error(j.err, 3);
         break;
       }
       // h = silu(g) * u of the pairs (written by other CTAs: read through L2)
       for (int q = 0; q < n; ++q) {
         const size_t base = (size_t)j.perm[it.pair_begin + q] * j.F;
-        for (int c2 = tid; c2 < K; c2 += kThreads) {
+        for (int c2 = gtid; c2 < K; c2 += kThreads) {
           const float gv = __ldcg(j.g + base + c2), uv = __ldcg(j.u + base + c2);
           hs[q * K + c2] = gv / (1.f + expf(-gv)) * uv;
         }
       }
-      compute_sync();
-      for (int i = warp; i < n * nb; i += kWarps) {
+      group_sync(group);
+      for (int i = gwarp; i < n * nb; i += kWarps) {
         float v = hs[(size_t)i * 32 + lane];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         if (lane == 0) hsum[i] = v;
       }
-      compute_sync();
+      group_sync(group);
     }
     // input row of pick q: its token (gate/up) or its own staged h (down)
     int qrow[TMAX];
@@ -442,7 +466,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
 #pragma unroll
       for (int q = 0; q < TMAX; ++q) acc[q] = 0.f;
 #pragma unroll 1
-      for (int b = warp; b < nb; b += 2 * kWarps) {
+      for (int b = gwarp; b < nb; b += 2 * kWarps) {
         const int b2 = b + kWarps;
         const bool two = b2 < nb;
         uint4 q0, q1 = make_uint4(0, 0, 0, 0);
@@ -464,13 +488,13 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
           }
         }
       }
-      if (tt > 0) compute_sync();  // the previous tile's sums have been read
+      if (tt > 0) group_sync(group);  // the previous tile's sums have been read
 #pragma unroll
       for (int q = 0; q < TMAX; ++q)
-        if (q < n) red[(warp * T + q) * 32 + lane] = acc[q];
-      compute_sync();
-      if (tt == wk.nt - 1 && tid == 0) mbar_arrive(&empty[s]);  // the tiles are no longer read
-      for (int q = warp; q < n; q += kWarps) {
+        if (q < n) red[(gwarp * T + q) * 32 + lane] = acc[q];
+      group_sync(group);
+      if (tt == wk.nt - 1 && gtid == 0) mbar_arrive(&empty[s]);  // the tiles are no longer read
+      for (int q = gwarp; q < n; q += kWarps) {
         float v = 0.f;
         for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
         const int pair = j.perm[it.pair_begin + q];
@@ -480,7 +504,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
     }
     // hand the item to the publisher once every compute thread's stores are issued
     const int p = c % kPubSlots;
-    if (tid == 0) {
+    if (gtid == 0) {
       if (c >= kPubSlots && !ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u)) flag_error(j.err, 3);
       s_pub[p] = code;
     }
@@ -489,7 +513,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
   // end of the publisher's list
   {
     const int p = c % kPubSlots;
-    if (tid == 0) {
+    if (gtid == 0) {
       if (c >= kPubSlots) (void)ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u);
       s_pub[p] = -1;
     }
@@ -501,7 +525,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_layer_kernel(const D
 
 bool decode_layer_supported(int H, int F, int T) {
   if (T < 1 || T > kTokPerUnit || H % 32 || F % 32) return false;
-  return decode_smem(H, F, T, 2) <= kDecodeSmemCap;
+  return decode_smem(H, F, T, 2, 1) <= kDecodeSmemCap;
 }
 
 cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
@@ -532,15 +556,17 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   j.sync = sync;
   j.cbase = cbase;
   j.err = a.err;
-  // three items in flight per CTA when they fit, else two
-  const bool nb3 = decode_smem(a.H, a.F, T, 3) <= kDecodeSmemCap;
-  const size_t smem = decode_smem(a.H, a.F, T, nb3 ? 3 : 2);
+  // single-token calls: two compute groups and four items in flight per CTA;
+  // otherwise one group, three items in flight when they fit, else two
+  const bool two = T == 1 && decode_smem(a.H, a.F, T, 4, 2) <= kDecodeSmemCap;
+  const bool nb3 = decode_smem(a.H, a.F, T, 3, 1) <= kDecodeSmemCap;
+  const size_t smem = two ? decode_smem(a.H, a.F, T, 4, 2) : decode_smem(a.H, a.F, T, nb3 ? 3 : 2, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sms);
-  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.blockDim = dim3(decode_threads(two ? 2 : 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -550,9 +576,10 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, j);
   };
-  static size_t c31 = 0, c21 = 0, c38 = 0, c28 = 0;
-  if (T == 1) return nb3 ? go(decode_layer_kernel<3, 1>, c31) : go(decode_layer_kernel<2, 1>, c21);
-  return nb3 ? go(decode_layer_kernel<3, kTokPerUnit>, c38) : go(decode_layer_kernel<2, kTokPerUnit>, c28);
+  static size_t c412 = 0, c311 = 0, c211 = 0, c381 = 0, c281 = 0;
+  if (two) return go(decode_layer_kernel<4, 1, 2>, c412);
+  if (T == 1) return nb3 ? go(decode_layer_kernel<3, 1, 1>, c311) : go(decode_layer_kernel<2, 1, 1>, c211);
+  return nb3 ? go(decode_layer_kernel<3, kTokPerUnit, 1>, c381) : go(decode_layer_kernel<2, kTokPerUnit, 1>, c281);
 }
 
 }  // namespace moe
