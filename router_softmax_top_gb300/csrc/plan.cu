@@ -21,6 +21,8 @@
 namespace moe {
 namespace {
 
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
 constexpr int NT = kPlanThreads;
 constexpr int NW = NT / 32;
 
@@ -516,11 +518,18 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   float lg4[4], lg8[8];
   if (E <= 128) load_logits<4>(a.logits, E, lg4);
   else if (E <= 256) load_logits<8>(a.logits, E, lg8);
+  // the state goes to shared memory by asynchronous copies that land while
+  // the router runs (it needs only the logits)
   for (int i = lane; i < S; i += 32) {
-    s_se[i] = a.slot_expert[i];
-    s_st[i] = a.slot_stamp[i];
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_se[i])), "l"(a.slot_expert + i)
+                 : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(&s_st[i])), "l"(a.slot_stamp + i)
+                 : "memory");
   }
-  for (int i = lane; i < E; i += 32) s_es[i] = a.expert_slot[i];
+  for (int i = lane; i < E; i += 32)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_es[i])), "l"(a.expert_slot + i)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
   const unsigned long long now = *a.clock + 1ull;
   if (lane == 0) s_bad = 0;
   if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
@@ -538,6 +547,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
       route_token<32>(row, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
     }
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncwarp();
   if (s_bad) {
     write_error(a);

@@ -119,3 +119,65 @@ def test_repeated_calls_reuse_slots_written_on_the_way():
     st = p.gpu.stats(0)
     assert st["unique_misses"] == 8 and st["unique_hits"] == 8
     p.close()
+
+
+def test_step_graph_replay_matches_eager_calls():
+    # pull fill, single-token calls: a step of layer calls captured as a CUDA
+    # graph and replayed gives bitwise the outputs and statistics of the same
+    # calls issued one by one
+    import ctypes
+    import torch
+    import router_softmax_top_gb300 as moe
+    sh = synth.DECODE
+    layers = [0, 1]
+    L = len(layers)
+    store = pinned_store(L, sh.E, sh.H, sh.F, seed=4)
+    steps = 12
+    _, logits, x = synth.decode_inputs(sh, steps, batch=1, seed=4, layers=layers)
+    lg_d = torch.from_numpy(logits).cuda()
+    x_d = torch.from_numpy(x).cuda()
+
+    def make():
+        return moe.MoECache(n_layers=L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
+                            slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=moe.MOE_FILL_PULL)
+
+    fwd = moe.lib().moe_layer_forward
+    # eager
+    a = make()
+    out_a = torch.empty((steps, L, 1, sh.H), device="cuda")
+    sa = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for s in range(steps):
+        for l in range(L):
+            assert fwd(a.handle, l, ctypes.c_void_p(lg_d[s, l].data_ptr()), ctypes.c_void_p(x_d[s, l].data_ptr()),
+                       1, ctypes.c_void_p(out_a[s, l].data_ptr()), sa) == 0
+    torch.cuda.synchronize()
+    # graph: first step eager (warms the library up), then capture one step and replay
+    b = make()
+    out_b = torch.empty((steps, L, 1, sh.H), device="cuda")
+    lg_cur = torch.empty((L, 1, sh.E), device="cuda")
+    x_cur = torch.empty((L, 1, sh.H), device="cuda")
+    out_cur = torch.empty((L, 1, sh.H), device="cuda")
+    for l in range(L):
+        assert fwd(b.handle, l, ctypes.c_void_p(lg_d[0, l].data_ptr()), ctypes.c_void_p(x_d[0, l].data_ptr()),
+                   1, ctypes.c_void_p(out_b[0, l].data_ptr()), sa) == 0
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=cap):
+        cs = ctypes.c_void_p(cap.cuda_stream)
+        for l in range(L):
+            assert fwd(b.handle, l, ctypes.c_void_p(lg_cur[l].data_ptr()), ctypes.c_void_p(x_cur[l].data_ptr()),
+                       1, ctypes.c_void_p(out_cur[l].data_ptr()), cs) == 0
+    for s in range(1, steps):
+        lg_cur.copy_(lg_d[s])
+        x_cur.copy_(x_d[s])
+        g.replay()
+        out_b[s].copy_(out_cur)
+    torch.cuda.synchronize()
+    assert torch.equal(out_a, out_b)
+    sa_, sb_ = a.stats(-1), b.stats(-1)
+    for key in ("calls", "pick_hits", "pick_misses", "unique_hits", "unique_misses", "evictions"):
+        assert sa_[key] == sb_[key], key
+    assert sb_["unique_misses"] > 0 and sb_["poisoned"] == 0
+    a.close()
+    b.close()
