@@ -56,6 +56,18 @@ def host_store(nbytes: int):
     _HOST_MAPS.append(mm)
     return torch.from_numpy(arr)
 
+
+def huge_page_kb():
+    """AnonHugePages of this process (kB), from /proc/self/smaps_rollup."""
+    try:
+        with open("/proc/self/smaps_rollup") as f:
+            for line in f:
+                if line.startswith("AnonHugePages:"):
+                    return int(line.split()[1])
+    except OSError:
+        pass
+    return None
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -358,6 +370,7 @@ def main():
     eb = sh.expert_bytes
     store = host_store(sh.L * sh.E * eb)
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
+    store_huge_kb = huge_page_kb()
     picks, logits_h, x_h = synth.decode_inputs(sh, nsteps, batch=1, seed=rank)
     logits_d = torch.from_numpy(logits_h).cuda()     # [steps, L, 1, E]
     x_d = torch.from_numpy(x_h).cuda()               # [steps, L, 1, H]
@@ -596,6 +609,8 @@ def main():
         "kernel_pass_ms_per_step": kpass_ms / K,
         "gpu_launches": int(n_launch),
         "step_graph": graph is not None,
+        "host_store_huge_fraction": (None if store_huge_kb is None
+                                     else min(1.0, store_huge_kb * 1024 / sh.store_bytes)),
         "clocks": clk,
         "e2e": e2e,
         "setup_s": setup_s,
