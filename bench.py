@@ -84,7 +84,7 @@ def parse():
                     help="decode: time eager layer calls instead of the captured step graph")
     ap.add_argument("--threads", type=int, default=0)
     ap.add_argument("--layers", type=int, default=0,
-                    help="decode: run only the first N layers of the model (profiling captures); 0 = all")
+                    help="run only the first N layers of the model (profiling captures); 0 = all")
     return ap.parse_args()
 
 
@@ -256,6 +256,9 @@ def run_prefill(args):
 
     import router_softmax_top_gb300 as moe
     sh = synth.PREFILL
+    if args.layers:
+        import dataclasses
+        sh = dataclasses.replace(sh, L=min(sh.L, args.layers))
     T = 512
     W, K = max(3, args.warmup), args.steps
     torch.cuda.set_device(0)
