@@ -35,7 +35,8 @@ struct PlanHdr {
   int32_t pick_misses;
   int32_t hit_units;  // GEMV units of the stage-0 hits: [0, hit_units)
   int32_t hit_gunits; // GEMM units of the stage-0 hits: [0, hit_gunits)
-  int32_t pad[4];
+  uint32_t epoch;     // call number of the handle (1, 2, ...): tags the decode layer kernel's outputs
+  int32_t pad[3];
 };
 
 // A work item = one distinct expert of the call.  Items are ordered: stage-0
@@ -154,6 +155,7 @@ struct PlanArgs {
   Mailbox *mailbox;   // device alias of the mapped host mailbox, or null
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;
+  uint32_t *epoch;    // the handle's call counter (device), advanced by every accepted call
 };
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
@@ -233,12 +235,13 @@ cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const 
 
 // Whole expert FFN + combine of a single-stage call of at most 8 tokens with the
 // pull fill, in one persistent launch (misses read from the mapped host store
-// and written into their slots on the way).  g, u: [T*k, F] scratch.  sync:
-// [0], [1] queue heads, [2 + i] per work item, [cbase + t * H/32 + r] per token
-// and row tile (zeroed by the plan kernel).
+// and written into their slots on the way).
 bool decode_layer_supported(int H, int F, int T);
+// gu: tagged gate then up outputs (2 x T*k rows of F), yt: tagged down outputs
+// (T*k rows of H); sync: [0], [1] queue heads, [2] abort word, [cbase + t*H/32 + r]
+// picks done of token t, row tile r (zeroed by the plan)
 cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
-                                float *g, float *u, float *out, int32_t *sync, int cbase, int T, int n_sms,
+                                uint64_t *gu, uint64_t *yt, float *out, int32_t *sync, int cbase, int T, int n_sms,
                                 cudaStream_t st);
 
 enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,

@@ -12,21 +12,24 @@
 // (gate/up tiles, then down groups) and hits (likewise).  When the call has
 // misses, 24 CTAs serve the miss queue, so the host link is busy from the
 // start and no hit waits behind a tile in flight on it, then turn to the hit
-// queue; the other CTAs serve the hit queue only (a CTA's GPU-scope fence
-// also waits for its copies in flight, so a host read there would hold up
-// the publication of hit outputs).  A down group waits for the gate/up tiles
-// of its expert, which come earlier in the same queue; a CTA claims items only
+// queue; the other CTAs serve the hit queue only, so that no hit waits in a
+// ring behind a copy from the host.  A down group needs the gate/up tiles of
+// its expert, which come earlier in the same queue; a CTA claims items only
 // while it runs, processes them in claim order, and takes from its second
 // queue only once its first is exhausted, so every waited-for tile is held by
 // a running CTA that reaches it.  Each CTA keeps its next items loading (bulk
-// copies, a producer warp) while its compute warps work, and a publisher warp
-// makes finished outputs visible and counts them.
+// copies, a producer warp) while its compute warps work.
 //
-// gate and up are stored separately (g, u); a down tile forms h = silu(g) * u
-// while staging its input, with the same expression the other kernels use.
+// Outputs that other CTAs read (gate, up and down rows) are stored as 64-bit
+// words: the fp32 value and the number of the call that wrote it.  A reader
+// polls each word until it carries this call's number, so no producer fences
+// its stores (a GPU-scope fence would also wait for the CTA's copies in flight
+// on the host link) and a down group starts on block b of h as soon as the
+// gate and up values of that block exist: each warp forms h = silu(g) * u of
+// its own blocks, with the same expression the other kernels use.
 // The weighted sum over a token's picks is done by whichever down tile of
-// that token and row tile finishes last (a per-(token, tile) counter): it adds
-// the k stored y rows in ascending pick order ("The idea: cache the hot
+// that token and row tile is counted last (a per-(token, tile) counter): it
+// adds the k down rows in ascending pick order ("The idea: cache the hot
 // experts on the GPU", step 4).  Every value is reduced in the canonical order
 // of the Q4_0 GEMV kernels, so results are bitwise those of the
 // tile-GEMV + combine path.
@@ -44,6 +47,7 @@ constexpr int kPubSlots = 4;
 __host__ __device__ constexpr int decode_threads(int groups) { return groups * kThreads + 64; }
 constexpr int kHitQueue = 1 << 30;                 // claim code flag: item of the hit queue
 constexpr int kMissCtas = 48;                      // CTAs that serve the miss queue first
+constexpr int kMaxDG = 4;                          // 32-row down tiles per down item, at most
 
 struct DecodeJob {
   const uint8_t *host;     // device alias of this layer's experts in the mapped host store
@@ -59,11 +63,11 @@ struct DecodeJob {
   int x_bf16;
   int T, k, H, F;
   int DG;                  // 32-row down tiles per down item (1, 2 or 4)
-  float *g, *u;            // [T*k, F]
-  float *y;                // [T*k, H]
+  uint64_t *g, *u;         // [T*k, F] tagged gate and up outputs
+  uint64_t *y;             // [T*k, H] tagged down outputs
   float *out;              // [T, H]
-  int32_t *sync;           // [0] miss queue head, [1] hit queue head, [2 + i] gate/up tiles done of
-                           // work item i, [cbase + t * H/32 + r] picks done of token t, row tile r
+  int32_t *sync;           // [0] miss queue head, [1] hit queue head, [2] abort word (a wait gave
+                           // up), [cbase + t * H/32 + r] picks done of token t, row tile r
   int cbase;
   int32_t *err;
 };
@@ -72,6 +76,44 @@ __device__ __forceinline__ uint64_t now_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Tagged values: the fp32 bits in the low word, the call number in the high word.
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t ep) {
+  const uint64_t w = ((uint64_t)ep << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ int ld_relaxed(const int32_t *p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Value at p once it carries call number ep.  Bounded: gives up after
+// kDecodeWaitNs, or soon after any CTA has given up (the abort word), and
+// then returns false.
+__device__ __forceinline__ bool wait_tagged(const uint64_t *p, uint32_t ep, int32_t *abort_word, float &v) {
+  uint64_t w = ld_tagged(p);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0; (uint32_t)(w >> 32) != ep; ++i) {
+    if ((i & 31u) == 31u) {
+      const uint64_t t = now_ns();
+      if (t0 == 0) t0 = t;
+      if (ld_relaxed(abort_word) || t - t0 > kDecodeWaitNs || i >= kSpinLimit) {
+        atomicExch(abort_word, 1);
+        v = 0.f;
+        return false;
+      }
+    }
+    __nanosleep(128);  // a poll is an L2 round trip: keep the request rate low
+    w = ld_tagged(p);
+  }
+  v = __uint_as_float((uint32_t)w);
+  return true;
 }
 
 // A claimed item: work item, matrix (0 gate, 1 up, 2 down), first 32-row tile
@@ -122,11 +164,10 @@ int decode_down_group(int H, int F) {
   return 1;
 }
 // shared memory: NB ring slots, the call's inputs [T][H] and their block sums,
-// and per compute group one down item's inputs [T][F], their block sums and
-// the warp partials [8][T][32]
-// (rounded to 32 floats: each group's inputs are read with 16-byte loads)
+// and per compute group one down item's inputs [T][F] and the warp partials
+// [8][T][32] (rounded to 32 floats: each group's inputs are read with 16-byte loads)
 __host__ __device__ inline size_t decode_group_floats(int F, int T) {
-  const size_t n = (size_t)T * F + (size_t)T * (F / 32) + (size_t)kWarps * T * 32;
+  const size_t n = (size_t)T * F + (size_t)kWarps * T * 32;
   return (n + 31) / 32 * 32;
 }
 size_t decode_smem(int H, int F, int T, int NB, int groups) {
@@ -191,7 +232,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
   qs.tH = j.H / 32;
   qs.DG = j.DG;
   qs.dG = (qs.tH + j.DG - 1) / j.DG;
-  const int T = j.T, nbH = j.H / 32, nbF = j.F / 32, tH = qs.tH;
+  const int T = j.T, nbH = j.H / 32, tH = qs.tH;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t slot_bytes = decode_slot_bytes(j.H, j.F, j.DG);
 
@@ -199,10 +240,10 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
   unsigned char *ring = sm;
   float *xs = reinterpret_cast<float *>(sm + NB * slot_bytes);  // [T][H]: the call's inputs
   float *xsum = xs + (size_t)T * j.H;                           // [T][H/32]
-float *gbase = xsum + (size_t)T * nbH;                        // per compute group, below
-  __shared__ __align__(8) uint64_t full[NB], empty[NB], pub[kPubSlots], pubfree[kPubSlots], published;
+  float *gbase = xsum + (size_t)T * nbH;                        // per compute group, below
+  __shared__ __align__(8) uint64_t full[NB], empty[NB], pub[kPubSlots], pubfree[kPubSlots];
   __shared__ int s_item[NB], s_pub[kPubSlots];
-  __shared__ int s_ok[GROUPS], s_ok_down[GROUPS];  // decisions of a group's thread 0, read after a barrier
+  __shared__ int s_ok[GROUPS];  // decisions of a group's thread 0, read after a barrier
 
   auto mat_of = [&](int mat) -> const MatLayout & {
     return mat == 0 ? j.lay.gate : mat == 1 ? j.lay.up : j.lay.down;
@@ -216,9 +257,8 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
       mbar_init(&pub[p], kThreads);
       mbar_init(&pubfree[p], 1);
     }
-    mbar_init(&published, 1);
     fence_mbar_init();
-    for (int g = 0; g < GROUPS; ++g) s_ok[g] = s_ok_down[g] = 1;
+    for (int g = 0; g < GROUPS; ++g) s_ok[g] = 1;
   }
   __syncthreads();
 
@@ -230,8 +270,7 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
     qs.nM = hd->n_stage0_miss;
     if (lane == 0) {
       // miss CTAs serve the miss queue, then help with the hits; hit CTAs never
-      // take a miss item: a GPU-scope fence waits for the CTA's copies in
-      // flight, and one from the host link would hold up the hit outputs
+      // take a miss item, so that no hit waits in a ring behind a host copy
       const int n_miss_ctas = qs.nM ? min((int)gridDim.x / 3, kMissCtas) : 0;
       const bool hit_first = (int)blockIdx.x >= n_miss_ctas;
       bool second = false, sequential = !hit_first;
@@ -243,17 +282,18 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
           for (int c2 = c - NB; c2 < c; ++c2) (void)ring_wait(&full[c2 % NB], (uint32_t)(c2 / NB) & 1u);
           break;
         }
-        // a miss CTA claims its next item only once the previous one is
-        // published: no publication then waits for a read in flight on the host
-        // link, and a hit item it takes is never queued behind a miss
-        if (sequential && c >= 1 && !ring_wait(&published, (uint32_t)(c - 1) & 1u)) {
-          flag_error(j.err, 3);
-          s_item[s] = -1;
-          mbar_arrive(&full[s]);
-          break;
+        // a miss CTA claims its next item only once the compute warps have
+        // issued every store of the previous one: no copy from the host is then
+        // in flight while they compute (their stores would queue behind it), and
+        // a hit item it takes is never queued behind a miss
+        bool gate_ok = true;
+        if (sequential && c >= 1) {
+          const int c2 = c - 1;
+          gate_ok = ring_wait(&pub[c2 % kPubSlots], (uint32_t)(c2 / kPubSlots) & 1u);
+          if (!gate_ok) flag_error(j.err, 3);
         }
         int code = -1;
-        for (;;) {
+        for (; gate_ok;) {
           const bool hitq = hit_first != second;
           const int size = hitq ? qs.hits() : qs.misses();
           const int pos = size > 0 ? atomicAdd(&j.sync[hitq ? 1 : 0], 1) : size;
@@ -301,12 +341,13 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
   }
 
   if (warp == GROUPS * kWarps + 1) {
-    // ---- publisher: after an item's outputs are stored, make them visible and
-    // count them; the last down tile of a (token, row tile) does its combine
+    // ---- publisher: counts each down item's rows per (token, row tile); the
+    // last one counted does that tile's weighted sum
     wait_plan();
     if (hd->error) return;
     qs.nH = hd->n_hits;
     qs.nM = hd->n_stage0_miss;
+    const uint32_t ep = hd->epoch;
     for (int c = 0;; ++c) {
       const int p = c % kPubSlots;
       int ok = 1;
@@ -323,16 +364,10 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
       if (code < 0) break;
       const Work wk = decode_claim(code, qs);
       const WorkItem it = j.items[wk.iu];
-      if (wk.mat != 2) {
-        if (lane == 0) {
-          __threadfence();
-          atomicAdd(&j.sync[2 + wk.iu], 1);
-        }
-      } else {
+      if (wk.mat == 2) {
         // bit (tt * 8 + i): pick i of this item completed row tile tile + tt
         unsigned done_mask = 0;
         if (lane == 0) {
-          __threadfence();
           for (int tt = 0; tt < wk.nt; ++tt)
             for (int i = 0; i < it.pair_count; ++i) {
               const int t = j.perm[it.pair_begin + i] / j.k;
@@ -340,21 +375,33 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
             }
         }
         done_mask = __shfl_sync(0xffffffffu, done_mask, 0);
-        if (done_mask) {
-          __threadfence();
-          // weighted sum over the picks of each completed (token, row tile), ascending
-          for (int tt = 0; tt < wk.nt; ++tt)
-            for (int i = 0; i < it.pair_count; ++i) {
-              if (!(done_mask >> (tt * 8 + i) & 1u)) continue;
-              const int t = j.perm[it.pair_begin + i] / j.k, r = (wk.tile + tt) * 32 + lane;
-              float o = 0.f;
-              for (int q = 0; q < j.k; ++q) o = fmaf(j.w[t * j.k + q], __ldcg(j.y + ((size_t)t * j.k + q) * j.H + r), o);
-              j.out[(size_t)t * j.H + r] = o;
+        // weighted sum over the picks of each completed (token, row tile), ascending
+        for (int tt = 0; tt < wk.nt; ++tt)
+          for (int i = 0; i < it.pair_count; ++i) {
+            if (!(done_mask >> (tt * 8 + i) & 1u)) continue;
+            const int t = j.perm[it.pair_begin + i] / j.k, r = (wk.tile + tt) * 32 + lane;
+            float o = 0.f;
+            bool yok = true;
+            // the k rows' words are loaded 8 at a time, all in flight together;
+            // one that does not carry this call's number yet is polled
+            for (int q0 = 0; q0 < j.k; q0 += 8) {
+              uint64_t yw[8];
+#pragma unroll
+              for (int i2 = 0; i2 < 8; ++i2)
+                if (q0 + i2 < j.k) yw[i2] = ld_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r);
+#pragma unroll
+              for (int i2 = 0; i2 < 8; ++i2)
+                if (q0 + i2 < j.k) {
+                  float yv = __uint_as_float((uint32_t)yw[i2]);
+                  if ((uint32_t)(yw[i2] >> 32) != ep)
+                    yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv) && yok;
+                  o = fmaf(j.w[t * j.k + q0 + i2], yv, o);
+                }
             }
-        }
+            if (!yok) flag_error(j.err, 3);
+            j.out[(size_t)t * j.H + r] = o;
+          }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&published);
     }
     return;
   }
@@ -383,12 +430,13 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
   const int gtid = tid - group * kThreads;
   const int gwarp = warp - group * kWarps;
   float *hs = gbase + (size_t)group * decode_group_floats(j.F, T);  // [T][F]: one down item's inputs
-  float *hsum = hs + (size_t)T * j.F;                                // [T][F/32]
-  float *red = hsum + (size_t)T * nbF;                               // [warps][T][32]
+  float *red = hs + (size_t)T * j.F;                                 // [warps][T][32]
   wait_plan();
   if (hd->error) return;
   qs.nH = hd->n_hits;
   qs.nM = hd->n_stage0_miss;
+  const uint32_t ep = hd->epoch;
+  int32_t *const abort_word = j.sync + 2;
 
   int c = group;
   for (;; c += GROUPS) {
@@ -412,54 +460,13 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
     const int nb = L.nb, K = 32 * nb, n = it.pair_count;
     const unsigned char *buf = ring + (size_t)s * slot_bytes;
     uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
-    const float *in = is_down ? hs : xs;
-    const float *insum = is_down ? hsum : xsum;
 
-    if (is_down) {
-      // h of this expert needs all of its gate and up tiles
-      if (gtid == 0) {
-        int ok = 0;
-        uint64_t t0 = 0;
-        for (uint32_t i = 0; i < kSpinLimit; ++i) {
-          if (ld_acquire(&j.sync[2 + wk.iu]) >= 2 * qs.tF) { ok = 1; break; }
-          __nanosleep(32);
-          if ((i & 63u) == 63u) {
-            const uint64_t t = now_ns();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > kDecodeWaitNs) break;
-          }
-        }
-        s_ok_down[group] = ok;
-      }
-      group_sync(group);
-      if (!s_ok_down[group]) {
-        flag_error(j.err, 3);
-        break;
-      }
-      // h = silu(g) * u of the pairs (written by other CTAs: read through L2)
-      for (int q = 0; q < n; ++q) {
-        const size_t base = (size_t)j.perm[it.pair_begin + q] * j.F;
-        for (int c2 = gtid; c2 < K; c2 += kThreads) {
-          const float gv = __ldcg(j.g + base + c2), uv = __ldcg(j.u + base + c2);
-          hs[q * K + c2] = gv / (1.f + expf(-gv)) * uv;
-        }
-      }
-      group_sync(group);
-      for (int i = gwarp; i < n * nb; i += kWarps) {
-        float v = hs[(size_t)i * 32 + lane];
+    if (!is_down) {
+      // ---- one 32-row tile of gate or up: inputs are the call's staged rows
+      int qrow[TMAX];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) hsum[i] = v;
-      }
-      group_sync(group);
-    }
-    // input row of pick q: its token (gate/up) or its own staged h (down)
-    int qrow[TMAX];
-#pragma unroll
-    for (int q = 0; q < TMAX; ++q) qrow[q] = q < n ? (is_down ? q : j.perm[it.pair_begin + q] / j.k) : 0;
-
-    for (int tt = 0; tt < wk.nt; ++tt) {
-      const int row = tt * 32 + lane;
+      for (int q = 0; q < TMAX; ++q) qrow[q] = q < n ? j.perm[it.pair_begin + q] / j.k : 0;
+      const int row = lane;
       // blocks warp, warp + 8, ... in ascending order, two at a time; each is
       // added exactly as block_term adds it
       float acc[TMAX];
@@ -471,8 +478,8 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
         const bool two = b2 < nb;
         uint4 q0, q1 = make_uint4(0, 0, 0, 0);
         unsigned short d0b, d1b = 0;
-        load_block(buf, wk.miss, wk.nt, row, b, nb, slot, L, wk.tile, q0, d0b);
-        if (two) load_block(buf, wk.miss, wk.nt, row, b2, nb, slot, L, wk.tile, q1, d1b);
+        load_block(buf, wk.miss, 1, row, b, nb, slot, L, wk.tile, q0, d0b);
+        if (two) load_block(buf, wk.miss, 1, row, b2, nb, slot, L, wk.tile, q1, d1b);
         float f0[32], f1[32];
         decode_block(q0, f0);
         decode_block(q1, f1);
@@ -480,26 +487,118 @@ float *gbase = xsum + (size_t)T * nbH;                        // per compute gro
 #pragma unroll
         for (int q = 0; q < TMAX; ++q) {
           if (q < n) {
-            const float *xr = in + (size_t)qrow[q] * K;
+            const float *xr = xs + (size_t)qrow[q] * K;
             const float t0 = dot32(f0, xr + 32 * b);
             const float t1 = two ? dot32(f1, xr + 32 * b2) : 0.f;
-            acc[q] = fmaf(d0, fmaf(256.f, t0, -136.f * insum[qrow[q] * nb + b]), acc[q]);
-            if (two) acc[q] = fmaf(d1, fmaf(256.f, t1, -136.f * insum[qrow[q] * nb + b2]), acc[q]);
+            acc[q] = fmaf(d0, fmaf(256.f, t0, -136.f * xsum[qrow[q] * nb + b]), acc[q]);
+            if (two) acc[q] = fmaf(d1, fmaf(256.f, t1, -136.f * xsum[qrow[q] * nb + b2]), acc[q]);
           }
         }
       }
-      if (tt > 0) group_sync(group);  // the previous tile's sums have been read
 #pragma unroll
       for (int q = 0; q < TMAX; ++q)
         if (q < n) red[(gwarp * T + q) * 32 + lane] = acc[q];
       group_sync(group);
-      if (tt == wk.nt - 1 && gtid == 0) mbar_arrive(&empty[s]);  // the tiles are no longer read
+      if (gtid == 0) mbar_arrive(&empty[s]);  // the tile is no longer read
+      uint64_t *dst = wk.mat == 0 ? j.g : j.u;
       for (int q = gwarp; q < n; q += kWarps) {
         float v = 0.f;
         for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
-        const int pair = j.perm[it.pair_begin + q];
-        if (is_down) j.y[(size_t)pair * j.H + (wk.tile + tt) * 32 + lane] = v;
-        else (wk.mat == 0 ? j.g : j.u)[(size_t)pair * j.F + wk.tile * 32 + lane] = v;
+        st_tagged(dst + (size_t)j.perm[it.pair_begin + q] * j.F + wk.tile * 32 + lane, v, ep);
+      }
+    } else {
+      // ---- up to kMaxDG 32-row tiles of down.  Each warp takes its blocks b
+      // (warp, warp + 8, ... ascending) one at a time: it forms block b of h
+      // for every pair from the tagged gate and up values (waiting for them
+      // where needed), then adds that block's term to each row of each tile.
+      float acc[kMaxDG][TMAX];
+#pragma unroll
+      for (int tt = 0; tt < kMaxDG; ++tt)
+#pragma unroll
+        for (int q = 0; q < TMAX; ++q) acc[tt][q] = 0.f;
+      bool ok = true;
+      // the pairs' rows, and the tagged gate/up words of the warp's next block:
+      // loaded one block ahead, so that they are in flight while the current
+      // block is computed (a word whose store has not landed yet is polled)
+      int prow[TMAX];
+      uint64_t gw[TMAX], uw[TMAX];
+#pragma unroll
+      for (int q = 0; q < TMAX; ++q) prow[q] = q < n ? j.perm[it.pair_begin + q] : 0;
+      auto fetch = [&](int b) {
+#pragma unroll
+        for (int q = 0; q < TMAX; ++q)
+          if (q < n) {
+            const size_t e = (size_t)prow[q] * j.F + 32 * b + lane;
+            gw[q] = ld_tagged(j.g + e);
+            uw[q] = ld_tagged(j.u + e);
+          }
+      };
+      if (gwarp < nb) fetch(gwarp);
+#pragma unroll 1
+      for (int b = gwarp; b < nb; b += kWarps) {
+        float hq[TMAX];
+#pragma unroll
+        for (int q = 0; q < TMAX; ++q) {
+          hq[q] = 0.f;
+          if (q < n) {
+            const size_t e = (size_t)prow[q] * j.F + 32 * b + lane;
+            float gv = __uint_as_float((uint32_t)gw[q]), uv = __uint_as_float((uint32_t)uw[q]);
+            if ((uint32_t)(gw[q] >> 32) != ep) ok = wait_tagged(j.g + e, ep, abort_word, gv) && ok;
+            if ((uint32_t)(uw[q] >> 32) != ep) ok = wait_tagged(j.u + e, ep, abort_word, uv) && ok;
+            const float h = gv / (1.f + expf(-gv)) * uv;
+            hs[q * K + 32 * b + lane] = h;
+            // block sum X_b: lane j holds value j, fixed xor tree
+            float v = h;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            hq[q] = v;
+          }
+        }
+        if (b + kWarps < nb) fetch(b + kWarps);
+        __syncwarp();
+        // the item's tiles two at a time for one token (two independent
+        // decode/dot chains), one at a time for several (one chain per token)
+        constexpr int kStep = TMAX == 1 ? 2 : 1;
+#pragma unroll
+        for (int tt = 0; tt < kMaxDG; tt += kStep) {
+          if (tt < wk.nt) {
+            const bool two = kStep == 2 && tt + 1 < wk.nt;
+            uint4 q0, q1 = make_uint4(0, 0, 0, 0);
+            unsigned short d0b, d1b = 0;
+            load_block(buf, wk.miss, wk.nt, tt * 32 + lane, b, nb, slot, L, wk.tile, q0, d0b);
+            if (two) load_block(buf, wk.miss, wk.nt, (tt + 1) * 32 + lane, b, nb, slot, L, wk.tile, q1, d1b);
+            float f0[32], f1[32];
+            decode_block(q0, f0);
+            decode_block(q1, f1);
+            const float d0 = half_bits(d0b), d1 = half_bits(d1b);
+#pragma unroll
+            for (int q = 0; q < TMAX; ++q)
+              if (q < n) {
+                const float *hb = hs + (size_t)q * K + 32 * b;
+                const float t0 = dot32(f0, hb);
+                const float t1 = two ? dot32(f1, hb) : 0.f;
+                acc[tt][q] = fmaf(d0, fmaf(256.f, t0, -136.f * hq[q]), acc[tt][q]);
+                if (two) acc[tt + 1][q] = fmaf(d1, fmaf(256.f, t1, -136.f * hq[q]), acc[tt + 1][q]);
+              }
+          }
+        }
+      }
+      if (!ok) flag_error(j.err, 3);
+#pragma unroll
+      for (int tt = 0; tt < kMaxDG; ++tt) {
+        if (tt < wk.nt) {
+          if (tt > 0) group_sync(group);  // the previous tile's sums have been read
+#pragma unroll
+          for (int q = 0; q < TMAX; ++q)
+            if (q < n) red[(gwarp * T + q) * 32 + lane] = acc[tt][q];
+          group_sync(group);
+          if (tt == wk.nt - 1 && gtid == 0) mbar_arrive(&empty[s]);  // the tiles are no longer read
+          for (int q = gwarp; q < n; q += kWarps) {
+            float v = 0.f;
+            for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
+            st_tagged(j.y + (size_t)j.perm[it.pair_begin + q] * j.H + (wk.tile + tt) * 32 + lane, v, ep);
+          }
+        }
       }
     }
     // hand the item to the publisher once every compute thread's stores are issued
@@ -529,7 +628,7 @@ bool decode_layer_supported(int H, int F, int T) {
 }
 
 cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
-                                float *g, float *u, float *out, int32_t *sync, int cbase, int T, int n_sms,
+                                uint64_t *gu, uint64_t *yt, float *out, int32_t *sync, int cbase, int T, int n_sms,
                                 cudaStream_t st) {
   if (!decode_layer_supported(a.H, a.F, T)) return cudaErrorInvalidValue;
   DecodeJob j;
@@ -549,9 +648,9 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   j.H = a.H;
   j.F = a.F;
   j.DG = decode_down_group(a.H, a.F);
-  j.g = g;
-  j.u = u;
-  j.y = a.y;
+  j.g = gu;
+  j.u = gu + (size_t)T * a.k * a.F;
+  j.y = yt;
   j.out = out;
   j.sync = sync;
   j.cbase = cbase;

@@ -67,7 +67,10 @@ struct moe_cache {
   MissItem *d_miss = nullptr;
   PlanHdr *d_hdr = nullptr;
   int32_t *d_sync = nullptr;  // per-call counters: queue head, per item, per (token, row tile)
-  float *d_u = nullptr;         // up outputs of the decode layer kernel [maxP, F] (gate outputs use d_h)
+  // decode layer kernel: gate/up outputs [2][maxPd][F] and down outputs [maxPd][H], each value
+  // stored with the number of the call that wrote it (maxPd = pairs of 8 tokens)
+  uint64_t *d_gut = nullptr, *d_yt = nullptr;
+  uint32_t *d_epoch = nullptr;  // call counter, advanced by the plan
   int32_t *d_route_bad = nullptr;  // non-finite-logit flag of the grid router
   int n_sms = 0;
   WorkUnit *d_gunits = nullptr;
@@ -225,7 +228,9 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_miss);
   cudaFree(c->d_hdr);
   cudaFree(c->d_sync);
-  cudaFree(c->d_u);
+  cudaFree(c->d_gut);
+  cudaFree(c->d_yt);
+  cudaFree(c->d_epoch);
   cudaFree(c->d_route_bad);
   cudaFree(c->d_gunits);
   cudaFree(c->d_gunit_begin);
@@ -363,7 +368,10 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_miss, c->maxU) == cudaSuccess;
   ok = ok && dalloc(&c->d_hdr, 1) == cudaSuccess;
   ok = ok && dalloc(&c->d_sync, (size_t)c->maxU + 2 + (size_t)cfg->max_tokens * (cfg->hidden / 32)) == cudaSuccess;
-  ok = ok && dalloc(&c->d_u, (size_t)c->maxP * cfg->ffn) == cudaSuccess;
+  const size_t maxPd = (size_t)std::min(cfg->max_tokens, kTokPerUnit) * cfg->top_k;
+  ok = ok && dalloc(&c->d_gut, 2 * maxPd * cfg->ffn) == cudaSuccess;
+  ok = ok && dalloc(&c->d_yt, maxPd * cfg->hidden) == cudaSuccess;
+  ok = ok && dalloc(&c->d_epoch, 1) == cudaSuccess;
   ok = ok && dalloc(&c->d_route_bad, 1) == cudaSuccess &&
        cudaMemsetAsync(c->d_route_bad, 0, sizeof(int32_t), (cudaStream_t)cuda_stream) == cudaSuccess;
   c->maxGunits = c->maxU + (c->maxP + kGemmN - 1) / kGemmN + 1;
@@ -433,6 +441,9 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   okm = okm && cudaMemsetAsync(c->d_clock, 0, sizeof(uint64_t) * L, st) == cudaSuccess;
   okm = okm && cudaMemsetAsync(c->d_stats, 0, sizeof(uint64_t) * L * kNStat, st) == cudaSuccess;
   okm = okm && cudaMemsetAsync(c->d_hdr, 0, sizeof(PlanHdr), st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_epoch, 0, sizeof(uint32_t), st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_gut, 0, sizeof(uint64_t) * 2 * maxPd * cfg->ffn, st) == cudaSuccess;
+  okm = okm && cudaMemsetAsync(c->d_yt, 0, sizeof(uint64_t) * maxPd * cfg->hidden, st) == cudaSuccess;
   okm = okm && cudaStreamSynchronize(st) == cudaSuccess;
   if (!okm) return fail(MOE_ERR_CUDA);
   *out = c;
@@ -489,6 +500,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.sync = c->d_sync;
   pa.route_bad = c->d_route_bad;
   pa.routed = 0;
+  pa.epoch = c->d_epoch;
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
   pa.sync_n = 2 + maxU + (use_decode ? T * (g.hidden / 32) : 0);
   pa.mailbox = need_host ? c->d_mail : nullptr;
@@ -656,7 +668,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     // pull fill, single stage, few tokens: the whole layer in one launch after
     // the plan (misses from the mapped host store, hits from their slots)
     const uint8_t *host_layer = static_cast<const uint8_t *>(c->host_dev) + (size_t)layer * c->store.layer_stride;
-    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, c->d_w, c->d_h, c->d_u,
+    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, c->d_w, c->d_gut, c->d_yt,
                                              static_cast<float *>(d_out), c->d_sync, 2 + maxU, T, c->n_sms, st));
   } else if (!need_host && fused_ok) {
     // pull fill, single stage guaranteed, few tokens: misses read once from the

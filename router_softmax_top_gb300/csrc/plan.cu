@@ -230,6 +230,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   for (int i = tid; i < a.sync_n; i += NT) a.sync[i] = 0;
   if (tid < 8) scal[tid] = 0;
   const unsigned long long now = *a.clock + 1ull;
+  const uint32_t epoch = *a.epoch + 1u;
   __syncthreads();
   if (a.routed) {
     // ids and weights come from route_kernel (earlier on the stream)
@@ -459,6 +460,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     h.pick_misses = P - pick_hits;
     h.hit_units = hit_units;
     h.hit_gunits = hit_gunits;
+    h.epoch = epoch;
+    *a.epoch = epoch;
     *a.hdr = h;
     *a.clock = now;
     uint64_t *st = a.stats;
@@ -531,6 +534,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
                  : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");
   const unsigned long long now = *a.clock + 1ull;
+  const uint32_t epoch = *a.epoch + 1u;  // loaded early: the header is the last thing written
   if (lane == 0) s_bad = 0;
   if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
   for (int i = lane; i < a.sync_n; i += 32) a.sync[i] = 0;
@@ -699,6 +703,8 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     h.pick_misses = P - pick_hits;
     h.hit_units = tot_hit_units;
     h.hit_gunits = nH;
+    h.epoch = epoch;
+    *a.epoch = epoch;
     *a.hdr = h;
     *a.clock = now;
     unsigned long long *st = reinterpret_cast<unsigned long long *>(a.stats);
