@@ -57,6 +57,25 @@ def host_store(nbytes: int):
     return torch.from_numpy(arr)
 
 
+def host_store_numa(t):
+    """Pages of the host store per NUMA node ({"N0": pages, ...}), from
+    /proc/self/numa_maps (the mapping that holds the store's first byte)."""
+    try:
+        addr = t.data_ptr()
+        best = None
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                parts = line.split()
+                start = int(parts[0], 16)
+                if start <= addr and (best is None or start > best[0]):
+                    best = (start, parts)
+        if best is None:
+            return None
+        return {p.split("=")[0]: int(p.split("=")[1]) for p in best[1] if p[:1] == "N" and "=" in p}
+    except (OSError, ValueError):
+        return None
+
+
 def huge_page_kb():
     """AnonHugePages of this process (kB), from /proc/self/smaps_rollup."""
     try:
@@ -374,6 +393,7 @@ def main():
     store = host_store(sh.L * sh.E * eb)
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
     store_huge_kb = huge_page_kb()
+    store_numa = host_store_numa(store)
     picks, logits_h, x_h = synth.decode_inputs(sh, nsteps, batch=1, seed=rank)
     logits_d = torch.from_numpy(logits_h).cuda()     # [steps, L, 1, E]
     x_d = torch.from_numpy(x_h).cuda()               # [steps, L, 1, H]
@@ -614,6 +634,7 @@ def main():
         "step_graph": graph is not None,
         "host_store_huge_fraction": (None if store_huge_kb is None
                                      else min(1.0, store_huge_kb * 1024 / sh.store_bytes)),
+        "host_store_numa_pages": store_numa,
         "clocks": clk,
         "e2e": e2e,
         "setup_s": setup_s,
