@@ -48,6 +48,8 @@ __host__ __device__ constexpr int decode_threads(int groups) { return groups * k
 constexpr int kHitQueue = 1 << 30;                 // claim code flag: item of the hit queue
 constexpr int kMissCtas = 48;                      // CTAs that serve the miss queue first
 constexpr int kMaxDG = 4;                          // 32-row down tiles per down item, at most
+constexpr int kMissDG = 2;                         // ... of the miss queue, at most
+constexpr int kHitDG = 2;                          // ... of the hit queue, at most
 
 struct DecodeJob {
   const uint8_t *host;     // device alias of this layer's experts in the mapped host store
@@ -123,9 +125,10 @@ struct Work {
   bool miss;
 };
 struct QueueShape {
-  int nH, nM, tF, tH, DG, dG;  // dG = down items per expert
-  __device__ int misses() const { return nM * (2 * tF + dG); }
-  __device__ int hits() const { return nH * (2 * tF + dG); }
+  int nH, nM, tF, tH;
+  int DGh, dGh, DGm, dGm;  // per queue (hits, misses): 32-row tiles per down item, down items per expert
+  __device__ int misses() const { return nM * (2 * tF + dGm); }
+  __device__ int hits() const { return nH * (2 * tF + dGh); }
 };
 // Queue position -> item.  Each queue: all gate/up tiles, then all down groups.
 __device__ __forceinline__ Work decode_claim(int code, const QueueShape &q) {
@@ -143,10 +146,11 @@ __device__ __forceinline__ Work decode_claim(int code, const QueueShape &q) {
     w.nt = 1;
   } else {
     const int i = pos - A;
-    w.iu = base + i / q.dG;
+    const int DG = hitq ? q.DGh : q.DGm, dG = hitq ? q.dGh : q.dGm;
+    w.iu = base + i / dG;
     w.mat = 2;
-    w.tile = (i % q.dG) * q.DG;
-    w.nt = min(q.DG, q.tH - w.tile);
+    w.tile = (i % dG) * DG;
+    w.nt = min(DG, q.tH - w.tile);
   }
   return w;
 }
@@ -230,8 +234,10 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
   qs.nM = 0;
   qs.tF = j.F / 32;
   qs.tH = j.H / 32;
-  qs.DG = j.DG;
-  qs.dG = (qs.tH + j.DG - 1) / j.DG;
+  qs.DGh = min(j.DG, kHitDG);
+  qs.dGh = (qs.tH + qs.DGh - 1) / qs.DGh;
+  qs.DGm = min(j.DG, kMissDG);
+  qs.dGm = (qs.tH + qs.DGm - 1) / qs.DGm;
   const int T = j.T, nbH = j.H / 32, tH = qs.tH;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const size_t slot_bytes = decode_slot_bytes(j.H, j.F, j.DG);
