@@ -7,13 +7,13 @@
 // and RAM Offload", "RAM offload": weights stream from host RAM when they do
 // not fit); cached experts are read from their slots in HBM; both are computed
 // by the same CTAs.  Work items are 32-row tiles of gate or of up, and groups
-// of up to 4 consecutive 32-row tiles of down (one input staging for 128 output
-// rows), of one expert.  Two queues hold them in dependency order: misses
-// (gate/up tiles, then down groups) and hits (likewise).  When the call has
-// misses, 24 CTAs serve the miss queue, so the host link is busy from the
-// start and no hit waits behind a tile in flight on it, then turn to the hit
-// queue; the other CTAs serve the hit queue only, so that no hit waits in a
-// ring behind a copy from the host.  A down group needs the gate/up tiles of
+// of up to 2 consecutive 32-row tiles of down, of one expert.  Two queues hold
+// them in dependency order: misses (gate/up tiles, then down groups) and hits
+// (likewise).  When the call has misses, 48 CTAs serve the miss queue, each
+// with one item at a time, so the host link is busy from the start and no
+// compute of a miss CTA runs beside its own copy from the host; they then turn
+// to the hit queue.  The other CTAs serve the hit queue only, so that no hit
+// waits in a ring behind a copy from the host.  A down group needs the gate/up tiles of
 // its expert, which come earlier in the same queue; a CTA claims items only
 // while it runs, processes them in claim order, and takes from its second
 // queue only once its first is exhausted, so every waited-for tile is held by
@@ -275,11 +275,15 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     qs.nH = hd->n_hits;
     qs.nM = hd->n_stage0_miss;
     if (lane == 0) {
-      // miss CTAs serve the miss queue, then help with the hits; hit CTAs never
-      // take a miss item, so that no hit waits in a ring behind a host copy
+      // miss CTAs serve the miss queue, then help with the hits; hit CTAs serve
+      // the hit queue only.  A miss CTA claims one item at a time: the next
+      // claim waits until the compute warps have issued every store of the
+      // previous item, so no copy from the host is in flight while they compute
+      // (their stores would queue behind it), and a hit item taken after a
+      // miss is never queued behind it
       const int n_miss_ctas = qs.nM ? min((int)gridDim.x / 3, kMissCtas) : 0;
       const bool hit_first = (int)blockIdx.x >= n_miss_ctas;
-      bool second = false, sequential = !hit_first;
+      bool second = false, prev_miss = false;
       for (int c = 0;; ++c) {
         const int s = c % NB;
         if (c >= NB && !ring_wait(&empty[s], (uint32_t)((c / NB) - 1) & 1u)) {
@@ -288,23 +292,24 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           for (int c2 = c - NB; c2 < c; ++c2) (void)ring_wait(&full[c2 % NB], (uint32_t)(c2 / NB) & 1u);
           break;
         }
-        // a miss CTA claims its next item only once the compute warps have
-        // issued every store of the previous one: no copy from the host is then
-        // in flight while they compute (their stores would queue behind it), and
-        // a hit item it takes is never queued behind a miss
-        bool gate_ok = true;
-        if (sequential && c >= 1) {
-          const int c2 = c - 1;
-          gate_ok = ring_wait(&pub[c2 % kPubSlots], (uint32_t)(c2 / kPubSlots) & 1u);
-          if (!gate_ok) flag_error(j.err, 3);
-        }
+        bool gate_ok = true, waited = false;
         int code = -1;
-        for (; gate_ok;) {
+        for (;;) {
           const bool hitq = hit_first != second;
+          if (c >= 1 && (!hitq || prev_miss) && !waited) {
+            const int c2 = c - 1;
+            waited = true;
+            gate_ok = ring_wait(&pub[c2 % kPubSlots], (uint32_t)(c2 / kPubSlots) & 1u);
+            if (!gate_ok) {
+              flag_error(j.err, 3);
+              break;
+            }
+          }
           const int size = hitq ? qs.hits() : qs.misses();
           const int pos = size > 0 ? atomicAdd(&j.sync[hitq ? 1 : 0], 1) : size;
           if (pos < size) {
             code = pos | (hitq ? kHitQueue : 0);
+            prev_miss = !hitq;
             break;
           }
           if (second || hit_first) break;
@@ -320,7 +325,6 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           }
           break;
         }
-        if (code & kHitQueue) sequential = false;  // HBM reads only from here on
         s_item[s] = code;
         const Work wk = decode_claim(code, qs);
         const WorkItem it = j.items[wk.iu];
