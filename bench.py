@@ -599,11 +599,13 @@ def main():
         roofline_hbm = {"kernel": "decode_layer", "bound": "hbm", "achieved": hbm_alg / (dl["ms"] * 1e-3) / 1e9,
                         "peak": hbm_peak, "unit": "GB/s",
                         "frac": hbm_alg / (dl["ms"] * 1e-3) / 1e9 / hbm_peak,
-                        "traffic": hbm_alg * per * ratio if ratio else None, "peak_source": peak_kind,
+                        "traffic": hit_b * per * ratio if ratio else None, "peak_source": peak_kind,
                         "launches": dl["launches"], "avg_launch_us": 1e3 * dl["ms"] * per,
                         "alg_bytes_per_launch": hbm_alg * per,
                         "note": "HBM side of the same kernel: hit blocks read, missed blocks written to "
-                                "their slots, activations and results; it overlaps the host-link reads"}
+                                "their slots, activations and results; it overlaps the host-link reads. "
+                                "traffic: DRAM read + write per launch from the committed capture's DRAM "
+                                "bytes per hit-block byte (the slot writes stayed in L2 there)"}
     t_roof = (d["unique_hits"] * sh.expert_bytes / (hbm_peak * 1e9) +
               d["unique_misses"] * sh.expert_bytes / (h2d_gbps * 1e9))
     t_roof_strict = t_roof + d["unique_misses"] * sh.expert_bytes / (hbm_peak * 1e9)
