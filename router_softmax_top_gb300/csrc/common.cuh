@@ -224,14 +224,29 @@ struct GemmMaps {
   CUtensorMap box[4];
 };
 cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps *out);
+// RawMaps: the slot planes of an array of n_slots slots (tiled layout) as
+// 32-bit-word tensors, so that one TMA copy brings a GEMM chunk (2 blocks of 4
+// consecutive 32-row tiles) of gate and up, or of down:
+//   gu_nib [slot][mat 2][tile][block][128 words]  box {128, 2, 4, 2, 1}
+//   gu_sc  [slot][mat 2][tile][block][16 words]   box {16, 2, 4, 2, 1}
+//   dn_nib [slot][tile][block][128 words]         box {128, 2, 4, 1}
+//   dn_sc  [slot][tile][block][16 words]          box {16, 2, 4, 1}
+// (tiles past the matrix read as zeros).
+struct RawMaps {
+  CUtensorMap gu_nib, gu_sc, dn_nib, dn_sc;
+};
+cudaError_t make_raw_maps(const uint8_t *base, int n_slots, uint64_t slot_stride, const SlotLayout &lay,
+                          RawMaps *out);
 cudaError_t launch_gather_sorted(const __nv_bfloat16 *x, const int32_t *perm, int P, int k, int H,
                                  __nv_bfloat16 *xs, cudaStream_t st);
-cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const WorkUnit *gunits,
-                               const int32_t *gunit_begin, __nv_bfloat16 *h16s, int range_kind, int stage,
-                               int max_gunits, cudaStream_t st);
-cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const WorkUnit *gunits,
-                             const int32_t *gunit_begin, int range_kind, int stage, int max_gunits,
-                             cudaStream_t st);
+// raw, slot0: the maps of the slot array that holds a.slots, and the index of
+// a.slots' slot 0 in it
+cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const RawMaps &raw, int slot0,
+                               const WorkUnit *gunits, const int32_t *gunit_begin, __nv_bfloat16 *h16s,
+                               int range_kind, int stage, int max_gunits, cudaStream_t st);
+cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const RawMaps &raw, int slot0,
+                             const WorkUnit *gunits, const int32_t *gunit_begin, int range_kind, int stage,
+                             int max_gunits, cudaStream_t st);
 
 // Whole expert FFN + combine of a single-stage call of at most 8 tokens with the
 // pull fill, in one persistent launch (misses read from the mapped host store

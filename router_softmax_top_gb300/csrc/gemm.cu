@@ -10,8 +10,11 @@
 // pair-sorted order, so the tile's B operand is a contiguous row range that a
 // TMA tensor copy lands directly in the 128-byte-swizzled K-major layout.
 // Roles (11 warps):
-//   warp 9     brings each chunk's Q4_0 weights into a raw ring with bulk
-//              copies (per matrix, 4 contiguous runs of nibbles and of scales);
+//   warp 9     brings each chunk's Q4_0 weights into a raw ring with two TMA
+//              tensor copies (nibbles, scales) over the slot planes viewed as
+//              [slot][matrix][tile][block][words] (one instruction per plane
+//              instead of one bulk copy per 1 KB run: issuing 16 bulk copies
+//              took as long as a whole chunk's dequantisation and MMAs);
 //   warp 10    brings each chunk's activation rows into a 6-deep ring with
 //              TMA tensor copies;
 //   warps 0-7  dequantise the raw chunk to bf16, w = (q - 8) * bf16(d) rounded
@@ -134,19 +137,29 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(gsa(bar))
       : "memory");
 }
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   gsa(dst)),
-               "l"(src), "r"(bytes), "r"(gsa(bar))
-               : "memory");
+// TMA tensor copies of one 4-D / 5-D box (coordinates innermost first).
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x0, int x1, int x2, int x3,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5}], [%6];" ::"r"(gsa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(gsa(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *map, int x0, int x1, int x2, int x3,
+                                            int x4, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(gsa(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(x4), "r"(gsa(bar))
+      : "memory");
 }
 __device__ __forceinline__ void expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(gsa(bar)), "r"(bytes) : "memory");
 }
 
 struct GemmJob {
-  const uint8_t *slots;
-  uint64_t slot_stride;
+  int slot0;         // index of the layer's (or stage buffer's) slot 0 in the raw maps' slot array
   MatLayout m0, m1;  // gate, up (NMAT 2) or down (NMAT 1)
   int R, nb;         // output rows, input 32-blocks
   const int32_t *perm;
@@ -172,24 +185,27 @@ __device__ __forceinline__ bool gunit_range(const PlanHdr *h, const int32_t *gb,
 constexpr size_t kBTileBytes = (size_t)kGemmN * 128;  // one chunk of up to 128 activation rows
 template <int NMAT>
 constexpr size_t a_stage_bytes() { return (size_t)NMAT * kGemmM * 128; }
+// Q4_0 of one chunk (4 row tiles x 2 blocks per matrix), as the TMA boxes land:
+// nibbles [matrix][tile][block][512 B], then scales [matrix][tile][block][64 B]
 template <int NMAT>
-constexpr size_t raw_stage_bytes() {  // Q4_0 of one chunk: 4 row tiles x 2 blocks, per matrix
-  return (size_t)NMAT * (4 * 1024 + 4 * 128);
-}
+constexpr size_t raw_stage_bytes() { return (size_t)NMAT * (4 * 1024 + 4 * 128); }
 template <int NMAT>
 constexpr size_t gemm_smem_bytes() {
   return kAStages * a_stage_bytes<NMAT>() + kBStages * kBTileBytes + kRawStages * raw_stage_bytes<NMAT>() + 1024;
 }
 
 // Dequantise block bi (32 inputs) of row r of one matrix from the raw chunk
-// into the swizzled bf16 tile `a` (row r, 16-byte chunks 4 bi .. 4 bi + 3).
-__device__ __forceinline__ void dequant_block(const unsigned char *rm, unsigned char *a, int r, int bi, bool valid) {
+// (nib: the matrix's nibbles [tile][block][32 rows][16 B], sc: its scales
+// [tile][block][32 rows]) into the swizzled bf16 tile `a` (row r, 16-byte
+// chunks 4 bi .. 4 bi + 3).
+__device__ __forceinline__ void dequant_block(const unsigned char *nib, const unsigned char *sc, unsigned char *a,
+                                              int r, int bi, bool valid) {
   uint4 q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
   float d = 0.f;
   if (valid) {
-    q = *reinterpret_cast<const uint4 *>(rm + (r >> 5) * 1024 + bi * 512 + (r & 31) * 16);
+    q = *reinterpret_cast<const uint4 *>(nib + (r >> 5) * 1024 + bi * 512 + (r & 31) * 16);
     d = __half2float(__ushort_as_half(
-        *reinterpret_cast<const unsigned short *>(rm + 4 * 1024 + (r >> 5) * 128 + bi * 64 + (r & 31) * 2)));
+        *reinterpret_cast<const unsigned short *>(sc + (r >> 5) * 128 + bi * 64 + (r & 31) * 2)));
   }
   // two nibbles side by side under the bf16 exponent of 128: 0x4300|q is
   // 128 + q exactly; minus 136 gives q - 8 exactly; times d rounds once
@@ -227,7 +243,8 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int issue
 
 template <int NMAT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    umma_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmJob j) {
+    umma_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ RawMaps raw_maps,
+                     const GemmJob j) {
   int lo, hi;
   if (!gunit_range(j.hdr, j.gunit_begin, j.range_kind, j.stage, lo, hi)) return;
   const int gu = lo + (int)blockIdx.y;
@@ -283,12 +300,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_base;
-  const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
+  const int slot_ix = j.slot0 + it.slot;
 
   if (warp == kRawWarp) {
-    // ---- raw Q4_0 loader: per chunk and matrix, n_rt contiguous 1 KB nibble
-    // runs (32 rows x blocks 2c, 2c+1 of one row tile) and n_rt 128 B scale runs
+    // ---- raw Q4_0 loader: per chunk, blocks 2c, 2c+1 of row tiles rt0 .. rt0+3
+    // of each matrix: one tensor copy of the nibbles, one of the scales (the
+    // full boxes land, tiles past the matrix as zeros)
     if (lane == 0) {
+      const CUtensorMap *mn = NMAT == 2 ? &raw_maps.gu_nib : &raw_maps.dn_nib;
+      const CUtensorMap *ms = NMAT == 2 ? &raw_maps.gu_sc : &raw_maps.dn_sc;
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mn)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(ms)) : "memory");
       int c = 0;
       for (; c < n_chunks; ++c) {
         const int s = c % kRawStages;
@@ -297,16 +319,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           break;
         }
         unsigned char *rs = raw + (size_t)s * raw_stage_bytes<NMAT>();
-        expect_tx(&rfull[s], (uint32_t)(NMAT * n_rt * (1024 + 128)));
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const MatLayout &L = m == 0 ? j.m0 : j.m1;
-          for (int q = 0; q < n_rt; ++q) {
-            const uint64_t e = ((uint64_t)(rt0 + q) * nb + 2 * c) * 32;
-            unsigned char *dm = rs + m * (4 * 1024 + 4 * 128);
-            bulk_load(dm + q * 1024, slot + L.nib_off + e * 16, 1024, &rfull[s]);
-            bulk_load(dm + 4 * 1024 + q * 128, slot + L.sc_off + e * 2, 128, &rfull[s]);
-          }
+        expect_tx(&rfull[s], (uint32_t)raw_stage_bytes<NMAT>());
+        if (NMAT == 2) {
+          tma_load_5d(rs, mn, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
+          tma_load_5d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
+        } else {
+          tma_load_4d(rs, mn, 0, 2 * c, rt0, slot_ix, &rfull[s]);
+          tma_load_4d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, slot_ix, &rfull[s]);
         }
       }
       drain_ring(rfull, kRawStages, c);
@@ -374,12 +393,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const unsigned char *rs = raw + (size_t)rsi * raw_stage_bytes<NMAT>();
       unsigned char *st = sa_base + (size_t)sa * a_stage_bytes<NMAT>();
       if (NMAT == 2) {
-        const unsigned char *rm = rs + hi_half * (4 * 1024 + 4 * 128);
+        const unsigned char *nib = rs + hi_half * 4096, *sc = rs + NMAT * 4096 + hi_half * 512;
         unsigned char *a = st + (size_t)hi_half * kGemmM * 128;
-        dequant_block(rm, a, r, 0, valid);
-        dequant_block(rm, a, r, 1, valid);
+        dequant_block(nib, sc, a, r, 0, valid);
+        dequant_block(nib, sc, a, r, 1, valid);
       } else {
-        dequant_block(rs, st, r, hi_half, valid);
+        dequant_block(rs, rs + NMAT * 4096, st, r, hi_half, valid);
       }
       g_mbar_arrive(&rempty[rsi]);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -425,7 +444,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <int NMAT>
-cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmJob &j, int max_gunits, cudaStream_t st) {
+cudaError_t launch_gemm_t(const GemmMaps &maps, const RawMaps &raw, const GemmJob &j, int max_gunits,
+                          cudaStream_t st) {
   if (max_gunits <= 0) return cudaSuccess;
   if (j.nb % 2) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes<NMAT>();
@@ -433,7 +453,7 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const GemmJob &j, int max_gunits
   const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT>, smem, cur);
   if (e != cudaSuccess) return e;
   dim3 grid((j.R + kGemmM - 1) / kGemmM, max_gunits);
-  umma_gemm_kernel<NMAT><<<grid, kGemmThreads, smem, st>>>(maps, j);
+  umma_gemm_kernel<NMAT><<<grid, kGemmThreads, smem, st>>>(maps, raw, j);
   return cudaGetLastError();
 }
 
@@ -447,10 +467,10 @@ __global__ void gather_sorted_kernel(const uint4 *__restrict__ x, const int32_t 
   }
 }
 
-GemmJob base_job(const FfnArgs &a, const WorkUnit *gunits, const int32_t *gunit_begin, int range_kind, int stage) {
+GemmJob base_job(const FfnArgs &a, int slot0, const WorkUnit *gunits, const int32_t *gunit_begin, int range_kind,
+                 int stage) {
   GemmJob j;
-  j.slots = a.slots;
-  j.slot_stride = a.slot_stride;
+  j.slot0 = slot0;
   j.perm = a.perm;
   j.items = a.items;
   j.gunits = gunits;
@@ -466,18 +486,26 @@ GemmJob base_job(const FfnArgs &a, const WorkUnit *gunits, const int32_t *gunit_
 
 }  // namespace
 
-cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps *out) {
-  using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                              const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+// cuTensorMapEncodeTiled from the driver (the runtime links no driver library)
+EncodeFn tensor_map_encoder() {
   static EncodeFn encode = nullptr;
   if (!encode) {
     void *fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
-    encode = reinterpret_cast<EncodeFn>(fn);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn) encode = reinterpret_cast<EncodeFn>(fn);
   }
+  return encode;
+}
+}  // namespace
+
+cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps *out) {
+  const EncodeFn encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
   if ((reinterpret_cast<uintptr_t>(base) & 15u) || K % kGemmK || rows <= 0) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * sizeof(__nv_bfloat16)};
@@ -492,6 +520,53 @@ cudaError_t make_gemm_maps(const __nv_bfloat16 *base, int K, int rows, GemmMaps 
   return cudaSuccess;
 }
 
+cudaError_t make_raw_maps(const uint8_t *base, int n_slots, uint64_t slot_stride, const SlotLayout &lay,
+                          RawMaps *out) {
+  const EncodeFn encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  if (!base || n_slots <= 0 || (reinterpret_cast<uintptr_t>(base) & 15u) || (slot_stride & 15u))
+    return cudaErrorInvalidValue;
+  // planes of one matrix: nibbles [tiles][nb][32][16 B] = 128 words per (tile, block),
+  // scales [tiles][nb][32] fp16 = 16 words; gate and up are mat_stride apart
+  const uint64_t mat_stride = lay.up.nib_off - lay.gate.nib_off;
+  if (lay.up.sc_off - lay.gate.sc_off != mat_stride || (mat_stride & 15u)) return cudaErrorInvalidValue;
+  const cuuint32_t elem[5] = {1, 1, 1, 1, 1};
+  auto enc = [&](CUtensorMap *m, uint64_t off, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                 const cuuint32_t *box) -> bool {
+    if (off & 15u) return false;
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, (cuuint32_t)rank, const_cast<uint8_t *>(base) + off, dims,
+                  strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const int gnb = lay.gate.nb, gt = lay.gate.rows / 32, dnb = lay.down.nb, dt = lay.down.rows / 32;
+  bool ok = true;
+  {
+    const cuuint64_t dims[5] = {128, (cuuint64_t)gnb, (cuuint64_t)gt, 2, (cuuint64_t)n_slots};
+    const cuuint64_t strides[4] = {512, (cuuint64_t)gnb * 512, mat_stride, slot_stride};
+    const cuuint32_t box[5] = {128, 2, 4, 2, 1};
+    ok = ok && enc(&out->gu_nib, lay.gate.nib_off, 5, dims, strides, box);
+  }
+  {
+    const cuuint64_t dims[5] = {16, (cuuint64_t)gnb, (cuuint64_t)gt, 2, (cuuint64_t)n_slots};
+    const cuuint64_t strides[4] = {64, (cuuint64_t)gnb * 64, mat_stride, slot_stride};
+    const cuuint32_t box[5] = {16, 2, 4, 2, 1};
+    ok = ok && enc(&out->gu_sc, lay.gate.sc_off, 5, dims, strides, box);
+  }
+  {
+    const cuuint64_t dims[4] = {128, (cuuint64_t)dnb, (cuuint64_t)dt, (cuuint64_t)n_slots};
+    const cuuint64_t strides[3] = {512, (cuuint64_t)dnb * 512, slot_stride};
+    const cuuint32_t box[4] = {128, 2, 4, 1};
+    ok = ok && enc(&out->dn_nib, lay.down.nib_off, 4, dims, strides, box);
+  }
+  {
+    const cuuint64_t dims[4] = {16, (cuuint64_t)dnb, (cuuint64_t)dt, (cuuint64_t)n_slots};
+    const cuuint64_t strides[3] = {64, (cuuint64_t)dnb * 64, slot_stride};
+    const cuuint32_t box[4] = {16, 2, 4, 1};
+    ok = ok && enc(&out->dn_sc, lay.down.sc_off, 4, dims, strides, box);
+  }
+  return ok ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gather_sorted(const __nv_bfloat16 *x, const int32_t *perm, int P, int k, int H,
                                  __nv_bfloat16 *xs, cudaStream_t st) {
   if (P <= 0) return cudaSuccess;
@@ -503,28 +578,28 @@ cudaError_t launch_gather_sorted(const __nv_bfloat16 *x, const int32_t *perm, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const WorkUnit *gunits,
-                               const int32_t *gunit_begin, __nv_bfloat16 *h16s, int range_kind, int stage,
-                               int max_gunits, cudaStream_t st) {
-  GemmJob j = base_job(a, gunits, gunit_begin, range_kind, stage);
+cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const RawMaps &raw, int slot0,
+                               const WorkUnit *gunits, const int32_t *gunit_begin, __nv_bfloat16 *h16s,
+                               int range_kind, int stage, int max_gunits, cudaStream_t st) {
+  GemmJob j = base_job(a, slot0, gunits, gunit_begin, range_kind, stage);
   j.m0 = a.lay.gate;
   j.m1 = a.lay.up;
   j.R = a.F;
   j.nb = a.H / 32;
   j.h16s = h16s;
-  return launch_gemm_t<2>(xs_maps, j, max_gunits, st);
+  return launch_gemm_t<2>(xs_maps, raw, j, max_gunits, st);
 }
 
-cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const WorkUnit *gunits,
-                             const int32_t *gunit_begin, int range_kind, int stage, int max_gunits,
-                             cudaStream_t st) {
-  GemmJob j = base_job(a, gunits, gunit_begin, range_kind, stage);
+cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const RawMaps &raw, int slot0,
+                             const WorkUnit *gunits, const int32_t *gunit_begin, int range_kind, int stage,
+                             int max_gunits, cudaStream_t st) {
+  GemmJob j = base_job(a, slot0, gunits, gunit_begin, range_kind, stage);
   j.m0 = a.lay.down;
   j.m1 = a.lay.down;
   j.R = a.H;
   j.nb = a.F / 32;
   j.y = a.y;
-  return launch_gemm_t<1>(h16s_maps, j, max_gunits, st);
+  return launch_gemm_t<1>(h16s_maps, raw, j, max_gunits, st);
 }
 
 }  // namespace moe

@@ -78,6 +78,7 @@ struct moe_cache {
   __nv_bfloat16 *d_h16 = nullptr;  // gate/up output of the GEMM path, pair-sorted rows [maxP, F]
   __nv_bfloat16 *d_xs = nullptr;   // activations in pair-sorted order [maxP, H]
   GemmMaps xs_maps, h16_maps;
+  RawMaps slot_maps, stage_maps;  // the slot planes of all layers' slots, of the stage buffers
   int maxGunits = 0;
   uint8_t *d_staging = nullptr;
   int staging_blocks = 0;
@@ -381,7 +382,10 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
     ok = dalloc(&c->d_h16, (size_t)c->maxP * cfg->ffn) == cudaSuccess &&
          dalloc(&c->d_xs, (size_t)c->maxP * cfg->hidden) == cudaSuccess;
     if (ok && (make_gemm_maps(c->d_xs, cfg->hidden, c->maxP, &c->xs_maps) != cudaSuccess ||
-               make_gemm_maps(c->d_h16, cfg->ffn, c->maxP, &c->h16_maps) != cudaSuccess))
+               make_gemm_maps(c->d_h16, cfg->ffn, c->maxP, &c->h16_maps) != cudaSuccess ||
+               make_raw_maps(c->d_slots, L * S, c->lay.stride, c->lay, &c->slot_maps) != cudaSuccess ||
+               (c->d_stage_buf &&
+                make_raw_maps(c->d_stage_buf, 2 * S, c->lay.stride, c->lay, &c->stage_maps) != cudaSuccess)))
       return fail(MOE_ERR_CUDA);
   }
   if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
@@ -696,8 +700,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     const int maxG = std::min(c->maxGunits, maxU + (P + kGemmN - 1) / kGemmN + 1);
     const __nv_bfloat16 *xb = static_cast<const __nv_bfloat16 *>(d_x);
     MOE_LAUNCH(K_GATHER, launch_gather_sorted(xb, c->d_perm, P, k, g.hidden, c->d_xs, st));
-    MOE_LAUNCH(K_GEMM_GATEUP,
-               launch_gemm_gateup(fa, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 0, 0, maxG, st));
+    MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(fa, c->xs_maps, c->slot_maps, layer * S, c->d_gunits,
+                                                 c->d_gunit_begin, c->d_h16, 0, 0, maxG, st));
     int rc = wait_mailbox(c, c->seq, st);
     if (rc != MOE_OK) return poison(c, rc);
     const PlanHdr hdr = c->h_mail->hdr;
@@ -713,10 +717,15 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       }
       FfnArgs fj = fa;
       fj.slots = stage_base(j);
+      // the tensor maps of the slot array stage j reads, and its slot 0 there
+      const bool in_layer = j == 0 || !c->d_stage_buf;
+      const RawMaps &rm = in_layer ? c->slot_maps : c->stage_maps;
+      const int slot0 = in_layer ? layer * S : (j & 1) * S;
       const int sg = std::min(maxG, S + (P + kGemmN - 1) / kGemmN + 1);  // units of one stage, bound
-      MOE_LAUNCH(K_GEMM_GATEUP,
-                 launch_gemm_gateup(fj, c->xs_maps, c->d_gunits, c->d_gunit_begin, c->d_h16, 1, j, sg, st));
-      MOE_LAUNCH(K_GEMM_DOWN, launch_gemm_down(fj, c->h16_maps, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
+      MOE_LAUNCH(K_GEMM_GATEUP, launch_gemm_gateup(fj, c->xs_maps, rm, slot0, c->d_gunits, c->d_gunit_begin,
+                                                   c->d_h16, 1, j, sg, st));
+      MOE_LAUNCH(K_GEMM_DOWN,
+                 launch_gemm_down(fj, c->h16_maps, rm, slot0, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
       if (cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
     }
     rc = finalize_stages(n_st, n0, nM);
