@@ -58,7 +58,7 @@ extern "C" {
 #define MOE_ERR_INVALID_ARG 1   /* bad argument or config; non-finite logit      */
 #define MOE_ERR_CUDA 2          /* a CUDA runtime call failed                     */
 #define MOE_ERR_OOM 3           /* device or pinned allocation failed             */
-#define MOE_ERR_TIMEOUT 4       /* a bounded host wait gave up                    */
+#define MOE_ERR_TIMEOUT 4       /* a bounded host or device wait gave up          */
 #define MOE_ERR_HOST_STORE 5    /* host store invalid or could not be registered  */
 #define MOE_ERR_POISONED 6      /* an earlier call on this handle failed          */
 #define MOE_ERR_UNSUPPORTED 7   /* shape outside what the kernels implement       */
@@ -86,7 +86,9 @@ typedef struct {
     int32_t gemm_min_tokens; /* calls with n_tokens >= this use the tensor-core
                                 grouped GEMM (bf16 activations only); 0 = never    */
     int32_t reserved;        /* must be 0                                          */
-    int64_t timeout_us;      /* limit of every bounded host wait, > 0              */
+    int64_t timeout_us;      /* limit of every bounded host wait, > 0; the decode
+                                layer kernel's device waits use a quarter of it,
+                                clamped to [1 ms, 2 s] (other kernels: 2 s)        */
 } moe_cache_config;
 
 typedef struct {
@@ -163,6 +165,19 @@ int moe_layer_last_plan(const moe_cache *c, int32_t layer, int32_t *ids, float *
                         int32_t *gpu_slot, int32_t *stage, int32_t *miss_expert,
                         int32_t *miss_slot, int32_t *miss_evicted, int32_t *miss_stage,
                         int32_t *n_miss, int32_t *n_stages);
+
+/*
+ * Test hook: fault injection without a GPU fault.  what = MOE_INJECT_DECODE_WAIT
+ * makes the next call that runs the decode layer kernel (pull fill, one stage,
+ * <= 8 tokens) wait, in its down items, for a gate value carrying a call number
+ * that is never written: the wait can only end by its limit (timeout_us / 4,
+ * clamped as above), after which the kernel ends every other wait, finishes,
+ * and records the failure; the next forward or sync returns MOE_ERR_TIMEOUT and
+ * the handle is poisoned.  what = 0 clears a pending injection.  Returns
+ * MOE_ERR_INVALID_ARG for an unknown `what`.
+ */
+#define MOE_INJECT_DECODE_WAIT 1
+int moe_cache_inject(moe_cache *c, int32_t what);
 
 /*
  * Per-kernel timing with CUDA events on the streams the kernels run on.

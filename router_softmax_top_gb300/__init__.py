@@ -28,9 +28,11 @@ MOE_ERR_UNSUPPORTED = 7
 MOE_FILL_MEMCPY = 0
 MOE_FILL_PULL = 1
 
+MOE_INJECT_DECODE_WAIT = 1
+
 # every symbol include/moe_cache.h declares
 EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_stats",
-           "moe_layer_last_plan", "moe_cache_set_timing", "moe_cache_timing",
+           "moe_layer_last_plan", "moe_cache_inject", "moe_cache_set_timing", "moe_cache_timing",
            "moe_cache_probe_h2d", "moe_expert_bytes", "moe_cache_launch_count",
            "moe_cache_destroy", "moe_strerror", "moe_expert_ffn_static")
 
@@ -96,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_timing.restype = ctypes.c_int
         L.moe_cache_timing.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(u64),
                                        ctypes.POINTER(ctypes.c_double), i32, ctypes.POINTER(i32)]
+        L.moe_cache_inject.restype = ctypes.c_int
+        L.moe_cache_inject.argtypes = [vp, i32]
         L.moe_cache_probe_h2d.restype = ctypes.c_int
         L.moe_cache_probe_h2d.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double)]
         L.moe_expert_bytes.restype = u64
@@ -256,6 +260,10 @@ class MoECache:
                 "gpu_slot": gs.reshape(n_tokens, self.k), "stage": stg.reshape(n_tokens, self.k),
                 "miss_expert": me[:n].copy(), "miss_slot": ms[:n].copy(),
                 "miss_evicted": mv[:n].copy(), "miss_stage": mst[:n].copy(), "n_stages": ns.value}
+
+    def inject(self, what: int):
+        """Test hook: fault injection without a GPU fault (moe_cache_inject)."""
+        _check(lib().moe_cache_inject(self.handle, what), "moe_cache_inject")
 
     def set_timing(self, enable: bool):
         _check(lib().moe_cache_set_timing(self.handle, 1 if enable else 0), "moe_cache_set_timing")

@@ -40,7 +40,6 @@ namespace {
 
 using namespace q4;
 
-constexpr uint64_t kDecodeWaitNs = 2000000000ull;  // bounded waits: 2 s
 constexpr int kPubSlots = 4;
 // per CTA: GROUPS groups of 8 compute warps (each group works on its own
 // items), a producer warp and a publisher warp
@@ -71,6 +70,8 @@ struct DecodeJob {
   int32_t *sync;           // [0] miss queue head, [1] hit queue head, [2] abort word (a wait gave
                            // up), [cbase + t * H/32 + r] picks done of token t, row tile r
   int cbase;
+  uint64_t wait_ns;        // limit of every bounded wait
+  int inject;              // down items wait for a gate value that is never written
   int32_t *err;
 };
 
@@ -96,16 +97,17 @@ __device__ __forceinline__ int ld_relaxed(const int32_t *p) {
   return v;
 }
 // Value at p once it carries call number ep.  Bounded: gives up after
-// kDecodeWaitNs, or soon after any CTA has given up (the abort word), and
-// then returns false.
-__device__ __forceinline__ bool wait_tagged(const uint64_t *p, uint32_t ep, int32_t *abort_word, float &v) {
+// limit_ns, or soon after any CTA has given up (the abort word), and then
+// returns false.
+__device__ __forceinline__ bool wait_tagged(const uint64_t *p, uint32_t ep, int32_t *abort_word, float &v,
+                                            uint64_t limit_ns) {
   uint64_t w = ld_tagged(p);
   uint64_t t0 = 0;
   for (uint32_t i = 0; (uint32_t)(w >> 32) != ep; ++i) {
     if ((i & 31u) == 31u) {
       const uint64_t t = now_ns();
       if (t0 == 0) t0 = t;
-      if (ld_relaxed(abort_word) || t - t0 > kDecodeWaitNs || i >= kSpinLimit) {
+      if (ld_relaxed(abort_word) || t - t0 > limit_ns || i >= kSpinLimit) {
         atomicExch(abort_word, 1);
         v = 0.f;
         return false;
@@ -190,14 +192,14 @@ __device__ __forceinline__ void all_compute_sync() {
   asm volatile("bar.sync 3, %0;" ::"n"(GROUPS * kThreads) : "memory");
 }
 
-__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u) {
       const uint64_t t = now_ns();
       if (t0 == 0) t0 = t;
-      else if (t - t0 > kDecodeWaitNs) return false;
+      else if (t - t0 > limit_ns) return false;
     }
   }
   return false;
@@ -286,10 +288,10 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
       bool second = false, prev_miss = false;
       for (int c = 0;; ++c) {
         const int s = c % NB;
-        if (c >= NB && !ring_wait(&empty[s], (uint32_t)((c / NB) - 1) & 1u)) {
+        if (c >= NB && !ring_wait(&empty[s], (uint32_t)((c / NB) - 1) & 1u, j.wait_ns)) {
           // the compute warps stopped: no copy may still be landing when the CTA exits
           flag_error(j.err, 3);
-          for (int c2 = c - NB; c2 < c; ++c2) (void)ring_wait(&full[c2 % NB], (uint32_t)(c2 / NB) & 1u);
+          for (int c2 = c - NB; c2 < c; ++c2) (void)ring_wait(&full[c2 % NB], (uint32_t)(c2 / NB) & 1u, j.wait_ns);
           break;
         }
         bool gate_ok = true, waited = false;
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           if (c >= 1 && (!hitq || prev_miss) && !waited) {
             const int c2 = c - 1;
             waited = true;
-            gate_ok = ring_wait(&pub[c2 % kPubSlots], (uint32_t)(c2 / kPubSlots) & 1u);
+            gate_ok = ring_wait(&pub[c2 % kPubSlots], (uint32_t)(c2 / kPubSlots) & 1u, j.wait_ns);
             if (!gate_ok) {
               flag_error(j.err, 3);
               break;
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           // the end of the list, once for each compute group
           for (int c2 = c; c2 < c + GROUPS; ++c2) {
             const int s2 = c2 % NB;
-            if (c2 > c && c2 >= NB && !ring_wait(&empty[s2], (uint32_t)((c2 / NB) - 1) & 1u)) break;
+            if (c2 > c && c2 >= NB && !ring_wait(&empty[s2], (uint32_t)((c2 / NB) - 1) & 1u, j.wait_ns)) break;
             s_item[s2] = -1;
             mbar_arrive(&full[s2]);
           }
@@ -361,7 +363,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     for (int c = 0;; ++c) {
       const int p = c % kPubSlots;
       int ok = 1;
-      if (lane == 0) ok = ring_wait(&pub[p], (uint32_t)(c / kPubSlots) & 1u) ? 1 : 0;
+      if (lane == 0) ok = ring_wait(&pub[p], (uint32_t)(c / kPubSlots) & 1u, j.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) {
         if (lane == 0) flag_error(j.err, 3);
@@ -404,7 +406,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
                 if (q0 + i2 < j.k) {
                   float yv = __uint_as_float((uint32_t)yw[i2]);
                   if ((uint32_t)(yw[i2] >> 32) != ep)
-                    yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv) && yok;
+                    yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv, j.wait_ns) && yok;
                   o = fmaf(j.w[t * j.k + q0 + i2], yv, o);
                 }
             }
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     const uint32_t parity = (uint32_t)(c / NB) & 1u;
     // one thread waits (bounded) and shares the decision, so that every
     // compute thread leaves the loop together
-    if (gtid == 0) s_ok[group] = ring_wait(&full[s], parity) ? 1 : 0;
+    if (gtid == 0) s_ok[group] = ring_wait(&full[s], parity, j.wait_ns) ? 1 : 0;
     group_sync(group);
     if (!s_ok[group]) {
       flag_error(j.err, 3);
@@ -553,8 +555,10 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           if (q < n) {
             const size_t e = (size_t)prow[q] * j.F + 32 * b + lane;
             float gv = __uint_as_float((uint32_t)gw[q]), uv = __uint_as_float((uint32_t)uw[q]);
-            if ((uint32_t)(gw[q] >> 32) != ep) ok = wait_tagged(j.g + e, ep, abort_word, gv) && ok;
-            if ((uint32_t)(uw[q] >> 32) != ep) ok = wait_tagged(j.u + e, ep, abort_word, uv) && ok;
+            // injected fault: this call's number + 1 is never written
+            const uint32_t ep_g = (j.inject && gwarp == 0 && b == 0 && q == 0) ? ep + 1u : ep;
+            if ((uint32_t)(gw[q] >> 32) != ep_g) ok = wait_tagged(j.g + e, ep_g, abort_word, gv, j.wait_ns) && ok;
+            if ((uint32_t)(uw[q] >> 32) != ep) ok = wait_tagged(j.u + e, ep, abort_word, uv, j.wait_ns) && ok;
             const float h = gv / (1.f + expf(-gv)) * uv;
             hs[q * K + 32 * b + lane] = h;
             // block sum X_b: lane j holds value j, fixed xor tree
@@ -614,7 +618,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     // hand the item to the publisher once every compute thread's stores are issued
     const int p = c % kPubSlots;
     if (gtid == 0) {
-      if (c >= kPubSlots && !ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u)) flag_error(j.err, 3);
+      if (c >= kPubSlots && !ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u, j.wait_ns)) flag_error(j.err, 3);
       s_pub[p] = code;
     }
     mbar_arrive(&pub[p]);
@@ -623,7 +627,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
   {
     const int p = c % kPubSlots;
     if (gtid == 0) {
-      if (c >= kPubSlots) (void)ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u);
+      if (c >= kPubSlots) (void)ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u, j.wait_ns);
       s_pub[p] = -1;
     }
     mbar_arrive(&pub[p]);
@@ -639,7 +643,7 @@ bool decode_layer_supported(int H, int F, int T) {
 
 cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
                                 uint64_t *gu, uint64_t *yt, float *out, int32_t *sync, int cbase, int T, int n_sms,
-                                cudaStream_t st) {
+                                uint64_t wait_ns, int inject, cudaStream_t st) {
   if (!decode_layer_supported(a.H, a.F, T)) return cudaErrorInvalidValue;
   DecodeJob j;
   j.host = host_layer;
@@ -664,6 +668,8 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   j.out = out;
   j.sync = sync;
   j.cbase = cbase;
+  j.wait_ns = wait_ns;
+  j.inject = inject;
   j.err = a.err;
   // single-token calls: two compute groups and four items in flight per CTA;
   // otherwise one group, three items in flight when they fit, else two

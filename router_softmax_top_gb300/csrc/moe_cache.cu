@@ -97,6 +97,7 @@ struct moe_cache {
   std::vector<cudaEvent_t> ev_up, ev_done;
 
   int poisoned = 0, last_error = MOE_OK, cuda_error = 0;
+  int inject = 0;  // pending fault injection (moe_cache_inject)
   int last_layer = -1, last_T = 0;
   std::atomic<uint64_t> launches{0};
   TimingPool tp;
@@ -107,6 +108,13 @@ namespace {
 const char *const kKindNames[K_NKINDS] = {"plan",        "repack",    "q4_gateup_gemv", "q4_down_gemv",
                                           "combine",     "gemm_gateup", "gemm_down",    "gather",
                                           "h2d_memcpy",  "fused_miss",  "decode_layer"};
+
+// The handle's device error word: 1 = a non-finite router logit (the plan),
+// anything else = a bounded device wait gave up.
+int device_error_code(const moe_cache *c) {
+  const int32_t e = __atomic_load_n(c->h_err, __ATOMIC_ACQUIRE);
+  return e == 0 ? MOE_OK : e == 1 ? MOE_ERR_INVALID_ARG : MOE_ERR_TIMEOUT;
+}
 
 int poison(moe_cache *c, int code) {
   if (!c->poisoned) {
@@ -458,7 +466,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
                               int32_t n_tokens, float *d_out, void *cuda_stream) {
   if (!c) return MOE_ERR_INVALID_ARG;
   if (c->poisoned) return MOE_ERR_POISONED;
-  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) return poison(c, MOE_ERR_INVALID_ARG);
+  if (const int de = device_error_code(c)) return poison(c, de);
   const moe_cache_config &g = c->cfg;
   if (layer < 0 || layer >= g.n_layers || n_tokens < 0 || n_tokens > g.max_tokens)
     return MOE_ERR_INVALID_ARG;
@@ -672,8 +680,15 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     // pull fill, single stage, few tokens: the whole layer in one launch after
     // the plan (misses from the mapped host store, hits from their slots)
     const uint8_t *host_layer = static_cast<const uint8_t *>(c->host_dev) + (size_t)layer * c->store.layer_stride;
+    // the device waits of the kernel give up after a quarter of timeout_us (so
+    // that a host wait outlasts them), within [1 ms, 2 s]
+    const uint64_t wait_ns =
+        (uint64_t)std::min<int64_t>(std::max<int64_t>(g.timeout_us / 4, 1000), 2000000) * 1000u;
+    const int inject = c->inject == MOE_INJECT_DECODE_WAIT;
+    c->inject = 0;
     MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, c->d_w, c->d_gut, c->d_yt,
-                                             static_cast<float *>(d_out), c->d_sync, 2 + maxU, T, c->n_sms, st));
+                                             static_cast<float *>(d_out), c->d_sync, 2 + maxU, T, c->n_sms,
+                                             wait_ns, inject, st));
   } else if (!need_host && fused_ok) {
     // pull fill, single stage guaranteed, few tokens: misses read once from the
     // host store and computed on the way; hits computed beside them
@@ -786,7 +801,7 @@ MOE_API int moe_cache_sync(moe_cache *c, void *cuda_stream) {
   int rc = wait_stream((cudaStream_t)cuda_stream, c->cfg.timeout_us);
   if (rc == MOE_OK) rc = wait_stream(c->side, c->cfg.timeout_us);
   if (rc != MOE_OK) return poison(c, rc);
-  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) return poison(c, MOE_ERR_INVALID_ARG);
+  if (const int de = device_error_code(c)) return poison(c, de);
   return c->poisoned ? c->last_error : MOE_OK;
 }
 
@@ -817,7 +832,7 @@ MOE_API int moe_cache_stats(const moe_cache *cc, int32_t layer, moe_cache_stats_
   out->bytes_uploaded = acc[6];
   out->stages = acc[7];
   out->staged_calls = acc[8];
-  if (__atomic_load_n(c->h_err, __ATOMIC_ACQUIRE)) poison(c, MOE_ERR_INVALID_ARG);
+  if (const int de = device_error_code(c)) poison(c, de);
   out->poisoned = c->poisoned;
   out->last_error = c->last_error;
   out->cuda_error = c->cuda_error;
@@ -887,6 +902,12 @@ MOE_API int moe_cache_timing(moe_cache *c, const char **names, uint64_t *launche
     if (ms) ms[i] = c->tp.ms[i];
   }
   if (n) *n = K_NKINDS;
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_inject(moe_cache *c, int32_t what) {
+  if (!c || (what != 0 && what != MOE_INJECT_DECODE_WAIT)) return MOE_ERR_INVALID_ARG;
+  c->inject = what;
   return MOE_OK;
 }
 

@@ -1,7 +1,8 @@
 """Error paths of the C ABI on the GPU: edge sizes, rejected inputs, poisoning,
-host-side failure injection (a wait whose limit is too short).  Nothing here
-faults or hangs the device: every failure is made on the host or is a value
-check the kernels perform."""
+failure injection (a host wait whose limit is too short; a device wait for a
+value that is never written, ended by its limit).  Nothing here faults or
+hangs the device: every failure is made on the host, is a value check the
+kernels perform, or is a bounded device wait that runs out."""
 import numpy as np
 import pytest
 
@@ -122,6 +123,42 @@ def test_timeout_on_host_wait_poisons(store):
         assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
     c.close()                                      # waits for the work in flight, frees all
     torch.cuda.synchronize()
+
+
+def test_device_wait_limit_poisons(store):
+    # injected fault, no GPU fault: the decode layer kernel waits for a gate
+    # value carrying a call number that is never written.  Its bounded wait
+    # (timeout_us / 4 = 50 ms) gives up, ends the other CTAs' waits, the kernel
+    # finishes, and the handle reports MOE_ERR_TIMEOUT at the next sync; the
+    # device stays usable.
+    import torch
+    c = _cache(store, fill_mode=moe.MOE_FILL_PULL, timeout_us=200_000)
+    lg, x = _inputs(1)
+    out = torch.empty((1, TINY.H), device="cuda")
+    c.forward(0, lg, x, out)                       # a normal call first
+    assert c.sync() == moe.MOE_OK
+    c.inject(moe.MOE_INJECT_DECODE_WAIT)
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_OK   # launched: the failure shows at the sync
+    assert c.sync() == moe.MOE_ERR_TIMEOUT
+    st = c.stats(-1)
+    assert st["poisoned"] == 1 and st["last_error"] == moe.MOE_ERR_TIMEOUT
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
+    c.close()
+    torch.cuda.synchronize()
+    # a fresh handle on the same device computes normally
+    c2 = _cache(store, fill_mode=moe.MOE_FILL_PULL)
+    c2.forward(0, lg, x, out)
+    assert c2.sync() == moe.MOE_OK and c2.stats(-1)["poisoned"] == 0
+    assert torch.isfinite(out).all()
+    c2.close()
+
+
+def test_inject_rejects_unknown_code(store):
+    c = _cache(store)
+    with pytest.raises(moe.MoeError):
+        c.inject(7)
+    c.inject(0)
+    c.close()
 
 
 def test_unaligned_store_rejected(store):
