@@ -377,42 +377,54 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
       const Work wk = decode_claim(code, qs);
       const WorkItem it = j.items[wk.iu];
       if (wk.mat == 2) {
-        // bit (tt * 8 + i): pick i of this item completed row tile tile + tt
-        unsigned done_mask = 0;
-        if (lane == 0) {
-          for (int tt = 0; tt < wk.nt; ++tt)
-            for (int i = 0; i < it.pair_count; ++i) {
-              const int t = j.perm[it.pair_begin + i] / j.k;
-              if (atomicAdd(&j.sync[j.cbase + t * tH + wk.tile + tt], 1) == j.k - 1) done_mask |= 1u << (tt * 8 + i);
-            }
+        // bit (tt * 8 + i): pick i of this item completed row tile tile + tt.
+        // One counter per lane, all in flight together; meanwhile the first
+        // two combinations' first 8 down rows are loaded on speculation (the
+        // common single-token case: the tail of the call is then one round trip)
+        const int pc = it.pair_count, ncomb = wk.nt * pc;
+        int old = -1;
+        if (lane < ncomb) {
+          const int t = j.perm[it.pair_begin + lane % pc] / j.k;
+          old = atomicAdd(&j.sync[j.cbase + t * tH + wk.tile + lane / pc], 1);
         }
-        done_mask = __shfl_sync(0xffffffffu, done_mask, 0);
-        // weighted sum over the picks of each completed (token, row tile), ascending
-        for (int tt = 0; tt < wk.nt; ++tt)
-          for (int i = 0; i < it.pair_count; ++i) {
-            if (!(done_mask >> (tt * 8 + i) & 1u)) continue;
-            const int t = j.perm[it.pair_begin + i] / j.k, r = (wk.tile + tt) * 32 + lane;
-            float o = 0.f;
-            bool yok = true;
-            // the k rows' words are loaded 8 at a time, all in flight together;
-            // one that does not carry this call's number yet is polled
-            for (int q0 = 0; q0 < j.k; q0 += 8) {
-              uint64_t yw[8];
+        uint64_t spec[2][8];
 #pragma unroll
-              for (int i2 = 0; i2 < 8; ++i2)
-                if (q0 + i2 < j.k) yw[i2] = ld_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r);
+        for (int c2 = 0; c2 < 2; ++c2)
+          if (c2 < ncomb) {
+            const int t = j.perm[it.pair_begin + c2 % pc] / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
 #pragma unroll
-              for (int i2 = 0; i2 < 8; ++i2)
-                if (q0 + i2 < j.k) {
-                  float yv = __uint_as_float((uint32_t)yw[i2]);
-                  if ((uint32_t)(yw[i2] >> 32) != ep)
-                    yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv, j.wait_ns) && yok;
-                  o = fmaf(j.w[t * j.k + q0 + i2], yv, o);
-                }
-            }
-            if (!yok) flag_error(j.err, 3);
-            j.out[(size_t)t * j.H + r] = o;
+            for (int i2 = 0; i2 < 8; ++i2)
+              if (i2 < j.k) spec[c2][i2] = ld_tagged(j.y + ((size_t)t * j.k + i2) * j.H + r);
           }
+        const unsigned last = __ballot_sync(0xffffffffu, old == j.k - 1);
+        // weighted sum over the picks of each completed (token, row tile), ascending
+        for (int c2 = 0; c2 < ncomb; ++c2) {
+          if (!(last >> c2 & 1u)) continue;
+          const int t = j.perm[it.pair_begin + c2 % pc] / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
+          float o = 0.f;
+          bool yok = true;
+          // the k rows' words 8 at a time, all in flight together; one that does
+          // not carry this call's number yet is polled
+          for (int q0 = 0; q0 < j.k; q0 += 8) {
+            uint64_t yw[8];
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2)
+              if (q0 + i2 < j.k) {
+                if (q0 == 0 && c2 < 2) yw[i2] = c2 == 0 ? spec[0][i2] : spec[1][i2];
+                else yw[i2] = ld_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r);
+              }
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2)
+              if (q0 + i2 < j.k) {
+                float yv = __uint_as_float((uint32_t)yw[i2]);
+                if ((uint32_t)(yw[i2] >> 32) != ep)
+                  yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv, j.wait_ns) && yok;
+                o = fmaf(j.w[t * j.k + q0 + i2], yv, o);
+              }
+          }
+          if (!yok) flag_error(j.err, 3);
+          j.out[(size_t)t * j.H + r] = o;
+        }
       }
     }
     return;
