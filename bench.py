@@ -484,6 +484,10 @@ def main():
     dev_ms = e0.elapsed_time(e1)
     clk = clocks.stop()
     st2 = cache.stats(-1)
+    # the host link again right after the timed region: a drop against the probe
+    # before it means the link (or the host memory behind it) slowed down during
+    # the run, which the step's time then carries
+    h2d_gbps_after = cache.probe_h2d(24)
 
     # ---- per-kernel pass: the next K steps again with CUDA events around every
     # launch (on the stream each kernel runs on); kept out of the headline
@@ -611,7 +615,7 @@ def main():
     t_roof_strict = t_roof + d["unique_misses"] * sh.expert_bytes / (hbm_peak * 1e9)
     step_roof = {"bound": "hbm+h2d", "t_roof_ms": 1e3 * t_roof, "t_meas_ms": dev_ms,
                  "frac": t_roof / (dev_ms * 1e-3), "frac_strict": t_roof_strict / (dev_ms * 1e-3),
-                 "hbm_gbs": hbm_peak, "h2d_gbs_measured": h2d_gbps,
+                 "hbm_gbs": hbm_peak, "h2d_gbs_measured": h2d_gbps, "h2d_gbs_after": h2d_gbps_after,
                  "hit_bytes": d["unique_hits"] * sh.expert_bytes,
                  "miss_bytes": d["unique_misses"] * sh.expert_bytes}
     picks_t = d["pick_hits"] + d["pick_misses"]

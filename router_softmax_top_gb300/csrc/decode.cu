@@ -225,8 +225,13 @@ __device__ __forceinline__ void load_block(const unsigned char *buf, bool miss, 
 
 // Launched as a programmatic dependent of the plan kernel: everything before
 // griddepcontrol.wait (barriers, the staged inputs) overlaps the plan; nothing
-// the plan writes is read before it.
-__device__ __forceinline__ void wait_plan() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// the plan writes is read before it.  Only after it (the plan complete) may
+// the next call's plan kernel, a programmatic dependent of this grid, start
+// its prologue (which reads the counters this call's plan wrote).
+__device__ __forceinline__ void wait_plan() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+}
 
 template <int NB, int TMAX, int GROUPS>
 __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel(const DecodeJob j) {

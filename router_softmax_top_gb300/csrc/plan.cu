@@ -193,7 +193,9 @@ __device__ __forceinline__ MissItem miss_record(int i, int n0, int S, const int 
 }
 
 __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
-  asm volatile("griddepcontrol.launch_dependents;");  // see plan_small_kernel
+  // launched in stream order (the caller's inputs are complete): a dependent
+  // launched programmatically may start its plan-independent prologue now
+  asm volatile("griddepcontrol.launch_dependents;");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int E = a.E, S = a.S, k = a.k, T = a.T;
   const int P = T * k;
@@ -504,9 +506,6 @@ constexpr int kSmallMaxSlots = 256;
 constexpr int kRouteGridMin = 64;  // calls with more tokens route in their own grid
 
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
-  // a dependent launched programmatically may start its plan-independent
-  // prologue now; it reads the plan only after this grid has completed
-  asm volatile("griddepcontrol.launch_dependents;");
   const unsigned F = 0xffffffffu;
   const int E = a.E, S = a.S, k = a.k, T = a.T, P = T * k;
   const int lane = threadIdx.x;
@@ -517,12 +516,11 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ int s_es[kMaxExperts];
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
-  // the first token's logits and the whole per-layer state in one round of loads
-  float lg4[4], lg8[8];
-  if (E <= 128) load_logits<4>(a.logits, E, lg4);
-  else if (E <= 256) load_logits<8>(a.logits, E, lg8);
-  // the state goes to shared memory by asynchronous copies that land while
-  // the router runs (it needs only the logits)
+  // Launched as a programmatic dependent of the kernel before it: until
+  // griddepcontrol.wait it reads only the layer's state and the handle's
+  // counters, which only earlier plan kernels write (complete before that
+  // kernel passed its own wait), and writes nothing.  The state goes to shared
+  // memory by asynchronous copies that land while the router runs.
   for (int i = lane; i < S; i += 32) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_se[i])), "l"(a.slot_expert + i)
                  : "memory");
@@ -535,6 +533,14 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   asm volatile("cp.async.commit_group;" ::: "memory");
   const unsigned long long now = *a.clock + 1ull;
   const uint32_t epoch = *a.epoch + 1u;  // loaded early: the header is the last thing written
+  // the caller's logits, and scratch the kernel before may still read, only
+  // after it has completed; this grid's dependent (the decode layer kernel)
+  // may then start its plan-independent prologue
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
+  float lg4[4], lg8[8];
+  if (E <= 128) load_logits<4>(a.logits, E, lg4);
+  else if (E <= 256) load_logits<8>(a.logits, E, lg8);
   if (lane == 0) s_bad = 0;
   if (lane < kSmallMaxSlots / 32) s_pinned[lane] = 0;
   for (int i = lane; i < a.sync_n; i += 32) a.sync[i] = 0;
@@ -756,8 +762,18 @@ bool plan_small_ok(int T, int E, int k, int S) {
 
 cudaError_t launch_plan(const PlanArgs &a_in, cudaStream_t st) {
   if (plan_small_ok(a_in.T, a_in.E, a_in.k, a_in.S)) {
-    plan_small_kernel<<<1, 32, 0, st>>>(a_in);
-    return cudaGetLastError();
+    // a programmatic dependent of the kernel before it (see plan_small_kernel)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_small_kernel, a_in);
   }
   PlanArgs a = a_in;
   a.routed = 0;
