@@ -100,8 +100,7 @@ __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, 
     const uint32_t b = __float_as_uint(v[i] == 0.f ? 0.f : v[i]);
     key[i] = (i * 32 + lane < E) ? ((b & 0x80000000u) ? ~b : (b | 0x80000000u)) : 0u;
   }
-  uint32_t taken = 0;
-  float my_p = 0.f;
+  uint32_t taken = 0, my_key = 0;
   int my_id = -1;
   for (int q = 0; q < k; ++q) {
     uint32_t bk = 0;
@@ -116,12 +115,14 @@ __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, 
         bi = (uint32_t)(i * 32 + lane);
     const int id = (int)__reduce_min_sync(0xffffffffu, bi);
     if ((id & 31) == lane) taken |= 1u << (id >> 5);
-    // the chosen value, from its owner lane
-    float ov = 0.f;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) ov = (i == (id >> 5)) ? v[i] : ov;
-    const float bvv = __shfl_sync(0xffffffffu, ov, id & 31);
-    if (lane == q) { my_p = expf(bvv - m) / z; my_id = id; }
+    if (lane == q) { my_key = mk; my_id = id; }
+  }
+  // pick q's probability on lane q, all k at once: its value is its key
+  // mapped back (-0 came out as +0, which has the same exponential)
+  float my_p = 0.f;
+  if (lane < k) {
+    const uint32_t kb = (my_key & 0x80000000u) ? (my_key & 0x7fffffffu) : ~my_key;
+    my_p = expf(__uint_as_float(kb) - m) / z;
   }
   float sum = lane < k ? my_p : 0.f;
 #pragma unroll
