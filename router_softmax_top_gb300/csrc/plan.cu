@@ -64,10 +64,11 @@ __device__ __forceinline__ void load_logits(const float *row, int E, float v[VPL
   for (int i = 0; i < VPL; ++i) v[i] = (i * 32 + lane < E) ? row[i * 32 + lane] : -INFINITY;
 }
 
-// Router for one token from its loaded logits.
+// Router for one token from its loaded logits (s_ids: an optional copy of the
+// ids in shared memory).
 template <int VPL>
 __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, int32_t *ids, float *w,
-                             int *bad_flag) {
+                             int *bad_flag, int32_t *s_ids = nullptr) {
   const int lane = threadIdx.x & 31;
   bool bad = false;
   float m = -INFINITY;
@@ -129,6 +130,7 @@ __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, 
   for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
     ids[lane] = my_id;
+    if (s_ids) s_ids[lane] = my_id;
     w[lane] = weight_mode == 1 ? my_p / sum : my_p;
   }
 }
@@ -136,10 +138,10 @@ __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, 
 // Router for one token, VPL logits per lane.
 template <int VPL>
 __device__ void route_token(const float *row, int E, int k, int weight_mode, int32_t *ids,
-                            float *w, int *bad_flag) {
+                            float *w, int *bad_flag, int32_t *s_ids = nullptr) {
   float v[VPL];
   load_logits<VPL>(row, E, v);
-  route_values<VPL>(v, E, k, weight_mode, ids, w, bad_flag);
+  route_values<VPL>(v, E, k, weight_mode, ids, w, bad_flag, s_ids);
 }
 
 // Routing of a large call as its own grid: one warp per token; a non-finite
@@ -517,6 +519,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ int s_es[kMaxExperts];
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
+  __shared__ int32_t s_ids[32];  // the routed ids, pair order (P <= 32)
   // Launched as a programmatic dependent of the kernel before it: until
   // griddepcontrol.wait it reads only the layer's state and the handle's
   // counters, which only earlier plan kernels write (complete before that
@@ -550,12 +553,12 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     const float *row = a.logits + (size_t)t * E;
     if (E <= 128) {
       if (t > 0) load_logits<4>(row, E, lg4);
-      route_values<4>(lg4, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+      route_values<4>(lg4, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad, s_ids + t * k);
     } else if (E <= 256) {
       if (t > 0) load_logits<8>(row, E, lg8);
-      route_values<8>(lg8, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+      route_values<8>(lg8, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad, s_ids + t * k);
     } else {
-      route_token<32>(row, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad);
+      route_token<32>(row, E, k, a.weight_mode, a.ids + t * k, a.w + t * k, &s_bad, s_ids + t * k);
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
@@ -567,7 +570,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
 
   // distinct experts: one leader lane per expert
   const bool act = lane < P;
-  const int e = act ? a.ids[lane] : -1 - lane;
+  const int e = act ? s_ids[lane] : -1 - lane;
   const unsigned same = __match_any_sync(F, e);
   const int leader = __ffs(same) - 1;
   const bool lead = act && leader == lane;
