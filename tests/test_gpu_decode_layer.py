@@ -181,3 +181,70 @@ def test_step_graph_replay_matches_eager_calls():
     assert sb_["unique_misses"] > 0 and sb_["poisoned"] == 0
     a.close()
     b.close()
+
+
+def test_full_decode_config_graph_sampled():
+    # the decode workload at full size (30 layers, 12.8 GB host store) in the
+    # launch configuration the bench times: one step of 30 layer calls
+    # captured as a CUDA graph and replayed.  The oracle follows every call
+    # (its cache state) and computes the outputs of sampled steps, one eager
+    # and two replayed; statistics must agree exactly at the end.
+    import ctypes
+    import torch
+    import oracle
+    import router_softmax_top_gb300 as moe
+    sh = synth.DECODE
+    L = sh.L
+    store = pinned_store(L, sh.E, sh.H, sh.F, seed=0)
+    W, K = 6, 18
+    steps = W + K
+    _, logits, x = synth.decode_inputs(sh, steps, batch=1, seed=0)
+    lg_d = torch.from_numpy(logits).cuda()
+    x_d = torch.from_numpy(x).cuda()
+    c = moe.MoECache(n_layers=L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
+                     slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=moe.MOE_FILL_PULL)
+    orc = oracle.Cache(L, sh.E, sh.k, sh.H, sh.F, sh.S, store.numpy())
+    fwd = moe.lib().moe_layer_forward
+    out = torch.empty((L, 1, sh.H), device="cuda")
+    check = {W - 1, W + K // 2, steps - 1}
+    worst = 0.0
+
+    def follow(s):
+        # the oracle's calls of step s; the outputs of sampled steps compared
+        nonlocal worst
+        res = [orc.forward(l, logits[s, l], x[s, l] if s in check else None, compute=s in check)
+               for l in range(L)]
+        if s in check:
+            torch.cuda.synchronize()
+            got = out.cpu().numpy()
+            for l in range(L):
+                worst = max(worst, row_rel_err(got[l], res[l]["out"]).max())
+
+    sa = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for s in range(W):
+        for l in range(L):
+            assert fwd(c.handle, l, ctypes.c_void_p(lg_d[s, l].data_ptr()), ctypes.c_void_p(x_d[s, l].data_ptr()),
+                       1, ctypes.c_void_p(out[l].data_ptr()), sa) == 0
+        follow(s)
+    lg_cur = torch.empty((L, 1, sh.E), device="cuda")
+    x_cur = torch.empty((L, 1, sh.H), device="cuda")
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=cap):
+        cs = ctypes.c_void_p(cap.cuda_stream)
+        for l in range(L):
+            assert fwd(c.handle, l, ctypes.c_void_p(lg_cur[l].data_ptr()), ctypes.c_void_p(x_cur[l].data_ptr()),
+                       1, ctypes.c_void_p(out[l].data_ptr()), cs) == 0
+    for s in range(W, steps):
+        lg_cur.copy_(lg_d[s])
+        x_cur.copy_(x_d[s])
+        g.replay()
+        follow(s)
+    torch.cuda.synchronize()
+    assert worst <= DECODE_TOL, worst
+    per_layer = [orc.stats(l) for l in range(L)]
+    assert_stats_equal(c.stats(-1), {key: sum(d[key] for d in per_layer) for key in per_layer[0]})
+    st = c.stats(-1)
+    assert st["poisoned"] == 0 and st["calls"] == L * steps and st["unique_misses"] > 0
+    c.close()
