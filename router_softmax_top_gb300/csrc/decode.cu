@@ -120,6 +120,37 @@ __device__ __forceinline__ bool wait_tagged(const uint64_t *p, uint32_t ep, int3
   return true;
 }
 
+// Inputs are staged with each 32-value block interleaved: value j at position
+// 2j for j < 16, 2(j - 16) + 1 otherwise, so that values j and 16 + j sit side
+// by side for the paired FMA below.
+__device__ __forceinline__ int ilv(int j) { return ((j & 15) << 1) | (j >> 4); }
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b,
+                                                    unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// dot32 over an interleaved block: the two partial sums (values 0..15 and
+// 16..31, each in ascending order) advance together in one paired FMA per
+// step, then are added: bitwise the canonical dot32.
+__device__ __forceinline__ float dot32_ilv(const float f[32], const float *xi) {
+  unsigned long long s = 0ull;
+#pragma unroll
+  for (int i = 0; i < 16; i += 2) {
+    const float4 a = *reinterpret_cast<const float4 *>(xi + 2 * i);  // x[i], x[16+i], x[i+1], x[17+i]
+    s = ffma2(pack2(f[i], f[16 + i]), pack2(a.x, a.y), s);
+    s = ffma2(pack2(f[i + 1], f[17 + i]), pack2(a.z, a.w), s);
+  }
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(s));
+  return lo + hi;
+}
+
 // A claimed item: work item, matrix (0 gate, 1 up, 2 down), first 32-row tile
 // and number of tiles, source.
 struct Work {
@@ -435,20 +466,28 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     return;
   }
 
-  // ---- compute warps: the call's inputs once (the staging of stage_rows)
+  // ---- compute warps: the call's inputs once (the staging of stage_rows),
+  // blocks interleaved
   for (int t = 0; t < T; ++t) {
+    float *dst = xs + (size_t)t * j.H;
     if (j.x_bf16) {
       const __nv_bfloat16 *src = reinterpret_cast<const __nv_bfloat16 *>(j.x) + (size_t)t * j.H;
-      for (int c = tid; c < j.H; c += GROUPS * kThreads) xs[t * j.H + c] = __bfloat162float(src[c]);
+      for (int c = tid; c < j.H; c += GROUPS * kThreads) dst[(c & ~31) + ilv(c & 31)] = __bfloat162float(src[c]);
     } else {
       const float4 *src = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(j.x) + (size_t)t * j.H);
-      float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)t * j.H);
-      for (int c = tid; c < j.H / 4; c += GROUPS * kThreads) dst[c] = src[c];
+      for (int c = tid; c < j.H / 4; c += GROUPS * kThreads) {
+        const float4 v = src[c];
+        const int e = 4 * c, base = e & ~31, jj = e & 31;
+        dst[base + ilv(jj)] = v.x;
+        dst[base + ilv(jj + 1)] = v.y;
+        dst[base + ilv(jj + 2)] = v.z;
+        dst[base + ilv(jj + 3)] = v.w;
+      }
     }
   }
   all_compute_sync<GROUPS>();
   for (int i = warp; i < T * nbH; i += GROUPS * kWarps) {
-    float v = xs[(size_t)i * 32 + lane];
+    float v = xs[(size_t)i * 32 + ilv(lane)];  // lane j holds value j
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     if (lane == 0) xsum[i] = v;
@@ -517,8 +556,8 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
         for (int q = 0; q < TMAX; ++q) {
           if (q < n) {
             const float *xr = xs + (size_t)qrow[q] * K;
-            const float t0 = dot32(f0, xr + 32 * b);
-            const float t1 = two ? dot32(f1, xr + 32 * b2) : 0.f;
+            const float t0 = dot32_ilv(f0, xr + 32 * b);
+            const float t1 = two ? dot32_ilv(f1, xr + 32 * b2) : 0.f;
             acc[q] = fmaf(d0, fmaf(256.f, t0, -136.f * xsum[qrow[q] * nb + b]), acc[q]);
             if (two) acc[q] = fmaf(d1, fmaf(256.f, t1, -136.f * xsum[qrow[q] * nb + b2]), acc[q]);
           }
@@ -577,7 +616,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
             if ((uint32_t)(gw[q] >> 32) != ep_g) ok = wait_tagged(j.g + e, ep_g, abort_word, gv, j.wait_ns) && ok;
             if ((uint32_t)(uw[q] >> 32) != ep) ok = wait_tagged(j.u + e, ep, abort_word, uv, j.wait_ns) && ok;
             const float h = gv / (1.f + expf(-gv)) * uv;
-            hs[q * K + 32 * b + lane] = h;
+            hs[q * K + 32 * b + ilv(lane)] = h;
             // block sum X_b: lane j holds value j, fixed xor tree
             float v = h;
 #pragma unroll
@@ -606,8 +645,8 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
             for (int q = 0; q < TMAX; ++q)
               if (q < n) {
                 const float *hb = hs + (size_t)q * K + 32 * b;
-                const float t0 = dot32(f0, hb);
-                const float t1 = two ? dot32(f1, hb) : 0.f;
+                const float t0 = dot32_ilv(f0, hb);
+                const float t1 = two ? dot32_ilv(f1, hb) : 0.f;
                 acc[tt][q] = fmaf(d0, fmaf(256.f, t0, -136.f * hq[q]), acc[tt][q]);
                 if (two) acc[tt + 1][q] = fmaf(d1, fmaf(256.f, t1, -136.f * hq[q]), acc[tt + 1][q]);
               }
