@@ -95,7 +95,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--fill", default="pull", choices=["memcpy", "pull"])
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
-    ap.add_argument("--cpu-sample-steps", type=int, default=4)
+    ap.add_argument("--cpu-sample-steps", type=int, default=96)  # ~14 s of oracle work on 16 cores
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-kernel-pass", action="store_true")
