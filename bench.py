@@ -647,7 +647,7 @@ def main():
     }
     # ---- CPU baseline: the oracle as it stands on a bounded sample (rank 0, N = 1)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = max(1, args.cpu_sample_steps)
+        n = max(1, min(args.cpu_sample_steps, logits_h.shape[0]))
         v, dt, cores = run_oracle_sample(sh, store.numpy(), logits_h, x_h, n, args.threads)
         result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                   "sample": f"first {n} decode steps (one token through all {sh.L} "
