@@ -388,7 +388,7 @@ def main():
     assert W >= 3 and K >= 1
     t_setup = time.time()
     G0 = 2                        # graph warm-up steps (capture and first replays)
-    nsteps = W + G0 + 3 * K
+    nsteps = max(W + G0 + 3 * K, args.cpu_sample_steps)  # (the CPU baseline's sample too)
     eb = sh.expert_bytes
     store = host_store(sh.L * sh.E * eb)
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
