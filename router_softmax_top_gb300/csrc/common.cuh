@@ -255,11 +255,15 @@ bool decode_layer_supported(int H, int F, int T);
 // gu: tagged gate then up outputs (2 x T*k rows of F), yt: tagged down outputs
 // (T*k rows of H); sync: [0], [1] queue heads, [2] abort word, [cbase + t*H/32 + r]
 // picks done of token t, row tile r (zeroed by the plan)
+// host_layer, expert_stride: where missed blocks are read (the layer's experts in
+// the mapped host store, or the staging buffer with miss_ready set: block r of
+// staging holds miss r once miss_ready[r] carries the call number).
 // wait_ns: limit of every bounded device wait; inject: down items wait for a
 // gate value that is never written (fault injection: the limit ends the wait)
-cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
-                                uint64_t *gu, uint64_t *yt, float *out, int32_t *sync, int cbase, int T, int n_sms,
-                                uint64_t wait_ns, int inject, cudaStream_t st);
+cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride,
+                                const uint32_t *miss_ready, const float *w, uint64_t *gu, uint64_t *yt, float *out,
+                                int32_t *sync, int cbase, int T, int n_sms, uint64_t wait_ns, int inject,
+                                cudaStream_t st);
 
 enum KernelKind { K_PLAN = 0, K_REPACK, K_GATEUP, K_DOWN, K_COMBINE, K_GEMM_GATEUP, K_GEMM_DOWN,
                   K_GATHER, K_MEMCPY, K_FUSED, K_DECODE, K_NKINDS };

@@ -51,8 +51,12 @@ constexpr int kMissDG = 2;                         // ... of the miss queue, at 
 constexpr int kHitDG = 2;                          // ... of the hit queue, at most
 
 struct DecodeJob {
-  const uint8_t *host;     // device alias of this layer's experts in the mapped host store
-  uint64_t expert_stride;  // bytes between experts in the store
+  const uint8_t *host;     // device alias of this layer's experts in the mapped host store, or
+                           // the staging buffer (miss_ready set)
+  uint64_t expert_stride;  // bytes between experts in the store (between blocks in staging)
+  const uint32_t *miss_ready;  // staging mode: [r] carries the call number once miss r's block
+                               // has landed in staging block r (copied from the host by the
+                               // copy engine); null: misses read from the mapped store
   uint8_t *slots;          // layer's slot 0
   uint64_t slot_stride;
   SlotLayout lay;
@@ -312,6 +316,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     if (hd->error) return;
     qs.nH = hd->n_hits;
     qs.nM = hd->n_stage0_miss;
+    const uint32_t ep = hd->epoch;
     if (lane == 0) {
       // miss CTAs serve the miss queue, then help with the hits; hit CTAs serve
       // the hit queue only.  A miss CTA claims one item at a time: the next
@@ -370,11 +375,30 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
         const int nb = L.nb;
         unsigned char *dst = ring + (size_t)s * slot_bytes;
         if (wk.miss) {
-          // canonical rows [32 tile, 32 (tile + nt)) of the matrix: one contiguous run
+          // canonical rows [32 tile, 32 (tile + nt)) of the matrix: one contiguous run,
+          // from the mapped store, or from staging block r once it has landed
+          uint64_t src = (uint64_t)it.expert;
+          if (j.miss_ready) {
+            const int r = wk.iu - qs.nH;
+            src = (uint64_t)r;
+            uint64_t t0 = 0;
+            for (uint32_t i = 0; (uint32_t)ld_acquire(reinterpret_cast<const int32_t *>(j.miss_ready + r)) != ep; ++i) {
+              __nanosleep(256);
+              if ((i & 15u) == 15u) {
+                const uint64_t t = now_ns();
+                if (t0 == 0) t0 = t;
+                if (ld_relaxed(j.sync + 2) || t - t0 > j.wait_ns || i >= kSpinLimit) {
+                  atomicExch(j.sync + 2, 1);
+                  flag_error(j.err, 3);
+                  break;
+                }
+              }
+            }
+          }
           const uint32_t bytes = (uint32_t)(32 * nb * 18);
           mbar_expect_tx(&full[s], bytes * wk.nt);
-          bulk_g2s(dst, j.host + (uint64_t)it.expert * j.expert_stride + L.nib_off + (uint64_t)wk.tile * bytes,
-                   bytes * wk.nt, &full[s]);
+          bulk_g2s(dst, j.host + src * j.expert_stride + L.nib_off + (uint64_t)wk.tile * bytes, bytes * wk.nt,
+                   &full[s]);
         } else {
           // tiled slot planes: nibbles [tiles][nb][32][16 B], then scales [tiles][nb][32]
           const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
@@ -697,13 +721,15 @@ bool decode_layer_supported(int H, int F, int T) {
   return decode_smem(H, F, T, 2, 1) <= kDecodeSmemCap;
 }
 
-cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride, const float *w,
-                                uint64_t *gu, uint64_t *yt, float *out, int32_t *sync, int cbase, int T, int n_sms,
-                                uint64_t wait_ns, int inject, cudaStream_t st) {
+cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uint64_t expert_stride,
+                                const uint32_t *miss_ready, const float *w, uint64_t *gu, uint64_t *yt, float *out,
+                                int32_t *sync, int cbase, int T, int n_sms, uint64_t wait_ns, int inject,
+                                cudaStream_t st) {
   if (!decode_layer_supported(a.H, a.F, T)) return cudaErrorInvalidValue;
   DecodeJob j;
   j.host = host_layer;
   j.expert_stride = expert_stride;
+  j.miss_ready = miss_ready;
   j.slots = const_cast<uint8_t *>(a.slots);
   j.slot_stride = a.slot_stride;
   j.lay = a.lay;

@@ -82,6 +82,11 @@ struct moe_cache {
   int maxGunits = 0;
   uint8_t *d_staging = nullptr;
   int staging_blocks = 0;
+  // memcpy fill through the decode layer kernel: [r] = call number once staging
+  // block r has landed, written by a stream memory operation after the copy
+  uint32_t *d_miss_ready = nullptr;
+  using WriteValueFn = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+  WriteValueFn write_value32 = nullptr;
 
   // mapped host words
   unsigned char *h_mail_raw = nullptr;
@@ -146,6 +151,13 @@ void tp_flush(moe_cache *c) {
     }
   }
   t.used = 0;
+}
+
+// Room for n more timed launches now (flushing waits for the device), so that
+// no flush falls where the host must not block.
+void tp_reserve(moe_cache *c, int n) {
+  TimingPool &t = c->tp;
+  if (t.on && t.used + n > (int)t.kind.size()) tp_flush(c);
 }
 
 int tp_begin(moe_cache *c, int kind, cudaStream_t st) {
@@ -246,6 +258,7 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_h16);
   cudaFree(c->d_xs);
   cudaFree(c->d_staging);
+  cudaFree(c->d_miss_ready);
   if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->side) cudaStreamDestroy(c->side);
@@ -398,7 +411,19 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   }
   if (ok && cfg->fill_mode == MOE_FILL_MEMCPY) {
     c->staging_blocks = std::min(S, c->maxU);
-    ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess;
+    ok = cudaMalloc(&c->d_staging, (size_t)c->staging_blocks * eb) == cudaSuccess &&
+         dalloc(&c->d_miss_ready, c->staging_blocks) == cudaSuccess &&
+         cudaMemset(c->d_miss_ready, 0, sizeof(uint32_t) * c->staging_blocks) == cudaSuccess;
+    // cuStreamWriteValue32 from the driver; without it the memcpy fill keeps
+    // its event-ordered schedule
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn)
+      c->write_value32 = reinterpret_cast<moe_cache::WriteValueFn>(fn);
+    else
+      cudaGetLastError();
   } else if (ok) {
     c->staging_blocks = 1;  // used by the bandwidth probe only
     ok = cudaMalloc(&c->d_staging, eb) == cudaSuccess;
@@ -514,7 +539,11 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.routed = 0;
   pa.epoch = c->d_epoch;
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
-  pa.sync_n = 2 + maxU + (use_decode ? T * (g.hidden / 32) : 0);
+  // memcpy fill, one stage guaranteed (distinct experts <= slots), few tokens:
+  // the decode layer kernel too, its misses read from staging as they land
+  const bool use_decode_mc = g.fill_mode == MOE_FILL_MEMCPY && c->write_value32 && !use_gemm && maxU <= S &&
+                             maxU <= c->staging_blocks && decode_layer_supported(g.hidden, g.ffn, T);
+  pa.sync_n = 2 + maxU + ((use_decode || use_decode_mc) ? T * (g.hidden / 32) : 0);
   pa.mailbox = need_host ? c->d_mail : nullptr;
   pa.mailbox_stage_cap = c->mail_stage_cap;
   pa.seq = c->seq;
@@ -634,6 +663,10 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   };
 
   const bool fused_ok = T <= kTokPerUnit && fused_miss_supported(g.hidden, g.ffn);
+  // the decode layer kernel's device waits give up after a quarter of
+  // timeout_us (so that a host wait outlasts them), within [1 ms, 2 s]
+  const uint64_t decode_wait_ns =
+      (uint64_t)std::min<int64_t>(std::max<int64_t>(g.timeout_us / 4, 1000), 2000000) * 1000u;
 
   // misses of a single-stage call through the fused kernel on the side stream
   // (after `after`), the main stream waiting for it before the combine
@@ -680,15 +713,45 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     // pull fill, single stage, few tokens: the whole layer in one launch after
     // the plan (misses from the mapped host store, hits from their slots)
     const uint8_t *host_layer = static_cast<const uint8_t *>(c->host_dev) + (size_t)layer * c->store.layer_stride;
-    // the device waits of the kernel give up after a quarter of timeout_us (so
-    // that a host wait outlasts them), within [1 ms, 2 s]
-    const uint64_t wait_ns =
-        (uint64_t)std::min<int64_t>(std::max<int64_t>(g.timeout_us / 4, 1000), 2000000) * 1000u;
     const int inject = c->inject == MOE_INJECT_DECODE_WAIT;
     c->inject = 0;
-    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, c->d_w, c->d_gut, c->d_yt,
-                                             static_cast<float *>(d_out), c->d_sync, 2 + maxU, T, c->n_sms,
-                                             wait_ns, inject, st));
+    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, host_layer, c->store.expert_stride, nullptr, c->d_w, c->d_gut,
+                                             c->d_yt, static_cast<float *>(d_out), c->d_sync, 2 + maxU, T,
+                                             c->n_sms, decode_wait_ns, inject, st));
+  } else if (use_decode_mc) {
+    // memcpy fill, one stage: the decode layer kernel starts on the hits at
+    // once; its misses wait, each for its staging block.  The host reads the
+    // miss list from the mailbox and, on the side stream, copies each missed
+    // block into staging (cudaMemcpyAsync) and then writes the call number
+    // into that block's ready word (a stream memory write, fenced after the copy).
+    // Nothing between the kernel's launch and the last copy may wait for the
+    // device (the kernel waits for the copies): the timing pool is made roomy first.
+    tp_reserve(c, 2);
+    const int inject = c->inject == MOE_INJECT_DECODE_WAIT;
+    c->inject = 0;
+    MOE_LAUNCH(K_DECODE, launch_decode_layer(fa, c->d_staging, c->expert_bytes, c->d_miss_ready, c->d_w,
+                                             c->d_gut, c->d_yt, static_cast<float *>(d_out), c->d_sync, 2 + maxU,
+                                             T, c->n_sms, decode_wait_ns, inject, st));
+    int rc = wait_mailbox(c, c->seq, st);
+    if (rc != MOE_OK) return poison(c, rc);
+    const PlanHdr hdr = c->h_mail->hdr;
+    if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
+    if (hdr.n_stages != 1 || hdr.n_miss > c->staging_blocks) return poison(c, MOE_ERR_CUDA);
+    if (hdr.n_miss > 0) {
+      if (cudaStreamWaitEvent(c->side, c->ev_plan, 0) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+      Launch l(c, K_MEMCPY, c->side);
+      const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) + (size_t)layer * c->store.layer_stride;
+      for (int i = 0; i < hdr.n_miss; ++i) {
+        const MissItem m = c->h_mail_miss[i];
+        if (m.expert < 0 || m.expert >= E) return poison(c, MOE_ERR_CUDA);
+        if (cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
+                            lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
+                            cudaMemcpyHostToDevice, c->side) != cudaSuccess ||
+            c->write_value32(reinterpret_cast<CUstream>(c->side),
+                             reinterpret_cast<CUdeviceptr>(c->d_miss_ready + i), hdr.epoch, 0) != CUDA_SUCCESS)
+          return poison(c, MOE_ERR_CUDA);
+      }
+    }
   } else if (!need_host && fused_ok) {
     // pull fill, single stage guaranteed, few tokens: misses read once from the
     // host store and computed on the way; hits computed beside them
