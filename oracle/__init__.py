@@ -20,16 +20,19 @@ _SO = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-NSTAT = 9
+NSTAT = 10
 STAT_NAMES = ("calls", "pick_hits", "pick_misses", "unique_hits", "unique_misses",
-              "evictions", "bytes_uploaded", "stages", "staged_calls")
+              "evictions", "bytes_uploaded", "stages", "staged_calls", "bypassed")
+
+POLICY_LRU = 0
+POLICY_SCORE = 1
 
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [("n_unique", ctypes.c_int32), ("n_hits", ctypes.c_int32),
                 ("n_miss", ctypes.c_int32), ("n_stages", ctypes.c_int32),
                 ("n_evict", ctypes.c_int32), ("pick_hits", ctypes.c_int32),
-                ("pick_misses", ctypes.c_int32)]
+                ("pick_misses", ctypes.c_int32), ("n_bypass", ctypes.c_int32)]
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
@@ -63,12 +66,14 @@ def lib() -> ctypes.CDLL:
             L.orc_lru_new.argtypes = [i32, i32]
             L.orc_lru_free.argtypes = [vp]
             L.orc_lru_get.argtypes = [vp, vp, vp, vp, vp]
+            L.orc_lru_set_policy.argtypes = [vp, i32, i32]
+            L.orc_lru_scores.argtypes = [vp, vp]
             L.orc_slot_map.restype = i32
             L.orc_slot_map.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanInfo)]
             L.orc_expert_ffn_parts.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
             L.orc_expert_ffn.argtypes = [vp, i32, i32, vp, vp]
             L.orc_cache_new.restype = vp
-            L.orc_cache_new.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, u64, u64, i32]
+            L.orc_cache_new.argtypes = [i32, i32, i32, i32, i32, i32, i32, vp, u64, u64, i32, i32, i32]
             L.orc_cache_free.argtypes = [vp]
             L.orc_cache_lru.restype = vp
             L.orc_cache_lru.argtypes = [vp, i32]
@@ -122,10 +127,12 @@ def router(logits: np.ndarray, k: int, weight_mode: int = 0):
 class LRU:
     """One layer's slot-map state (S slots, E experts)."""
 
-    def __init__(self, S: int, E: int):
+    def __init__(self, S: int, E: int, policy: int = POLICY_LRU, budget: int = 0):
         self.S, self.E = S, E
         self._h = lib().orc_lru_new(S, E)
         self._own = True
+        if policy != POLICY_LRU:
+            lib().orc_lru_set_policy(self._h, policy, budget)
 
     @classmethod
     def _borrow(cls, handle, S, E):
@@ -147,8 +154,9 @@ class LRU:
         me = np.empty(m, np.int32); ms = np.empty(m, np.int32)
         mv = np.empty(m, np.int32); mst = np.empty(m, np.int32)
         info = PlanInfo()
-        lib().orc_slot_map(self._h, _p(ids), T, k, _p(gs), _p(stg), _p(me), _p(ms), _p(mv),
-                           _p(mst), ctypes.byref(info))
+        if lib().orc_slot_map(self._h, _p(ids), T, k, _p(gs), _p(stg), _p(me), _p(ms), _p(mv),
+                              _p(mst), ctypes.byref(info)) != 0:
+            raise ValueError("the score policy plans single-stage calls only")
         n = info.n_miss
         return {"gpu_slot": gs.reshape(T, k), "stage": stg.reshape(T, k),
                 "miss_expert": me[:n].copy(), "miss_slot": ms[:n].copy(),
@@ -160,6 +168,12 @@ class LRU:
         ss = np.empty(self.S, np.uint64); clk = ctypes.c_uint64(0)
         lib().orc_lru_get(self._h, _p(se), _p(es), _p(ss), ctypes.byref(clk))
         return {"slot_expert": se, "expert_slot": es, "slot_stamp": ss, "clock": int(clk.value)}
+
+    def scores(self) -> np.ndarray:
+        """The decayed usage scores [E] (policy 1)."""
+        out = np.empty(self.E, np.float64)
+        lib().orc_lru_scores(self._h, _p(out))
+        return out
 
 
 # ---------------------------------------------------------------------- FFN
@@ -184,7 +198,7 @@ class Cache:
     canonical Q4_0 expert blocks, [layer][expert] with the given strides."""
 
     def __init__(self, L, E, k, H, F, S, store, weight_mode=0, layer_stride=None,
-                 expert_stride=None, threads=0):
+                 expert_stride=None, threads=0, policy=POLICY_LRU, admit_budget=0):
         self.L, self.E, self.k, self.H, self.F, self.S = L, E, k, H, F, S
         eb = 3 * F * H // 32 * 18
         self.expert_stride = eb if expert_stride is None else expert_stride
@@ -196,7 +210,8 @@ class Cache:
             self._store_ref = None
             addr = int(store)
         self._h = lib().orc_cache_new(L, E, k, H, F, S, weight_mode, ctypes.c_void_p(addr),
-                                      self.layer_stride, self.expert_stride, threads)
+                                      self.layer_stride, self.expert_stride, threads, policy,
+                                      admit_budget)
 
     def __del__(self):
         if getattr(self, "_h", None):
@@ -229,6 +244,8 @@ class Cache:
         rc = lib().orc_layer_forward(self._h, layer, _p(lg), _p(xa), is_bf16, T, int(bool(compute)),
                                      _p(out), _p(ids), _p(w), _p(gs), _p(stg), _p(me), _p(ms),
                                      _p(mv), _p(mst), _p(visits), ctypes.byref(info))
+        if rc == -2:
+            raise ValueError("the score policy plans single-stage calls only")
         if rc != 0:
             raise ValueError("non-finite router logit")
         n = info.n_miss

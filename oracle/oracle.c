@@ -148,6 +148,9 @@ typedef struct {
     int32_t *expert_slot;  /* [E]  slot of each expert, -1 = not cached        */
     uint64_t *slot_stamp;  /* [S]  call counter of the slot's last use         */
     uint64_t clock;        /* number of calls planned so far                   */
+    int policy;            /* 0: LRU; 1: decayed usage score with admission    */
+    int budget;            /* policy 1: admissions per call, 0 = unlimited     */
+    double *score;         /* [E]  policy 1: decayed usage per expert          */
 } orc_lru;
 
 orc_lru *orc_lru_new(int S, int E) {
@@ -160,14 +163,27 @@ orc_lru *orc_lru_new(int S, int E) {
     for (int s = 0; s < S; ++s) st->slot_expert[s] = -1;
     for (int e = 0; e < E; ++e) st->expert_slot[e] = -1;
     st->clock = 0;
+    st->policy = 0;
+    st->budget = 0;
+    st->score = (double *)calloc((size_t)E, sizeof(double));
     return st;
 }
+
+/* Replacement policy of the state: 0 = LRU (default), 1 = decayed score. */
+void orc_lru_set_policy(orc_lru *st, int policy, int budget) {
+    st->policy = policy;
+    st->budget = budget;
+}
+
+/* Copy of the decayed scores [E] (policy 1). */
+void orc_lru_scores(const orc_lru *st, double *out) { memcpy(out, st->score, sizeof(double) * st->E); }
 
 void orc_lru_free(orc_lru *st) {
     if (!st) return;
     free(st->slot_expert);
     free(st->expert_slot);
     free(st->slot_stamp);
+    free(st->score);
     free(st);
 }
 
@@ -184,6 +200,7 @@ void orc_lru_get(const orc_lru *st, int32_t *slot_expert, int32_t *expert_slot,
 typedef struct {
     int32_t n_unique, n_hits, n_miss, n_stages, n_evict;
     int32_t pick_hits, pick_misses;
+    int32_t n_bypass;      /* policy 1: misses computed without taking a slot */
 } orc_plan_info;
 
 /* Order two candidate slots for eviction: empty slots first (by slot index),
@@ -202,6 +219,127 @@ static void sort_victims(const orc_lru *st, int *v, int n) {
         while (j >= 0 && victim_before(st, x, v[j])) { v[j + 1] = v[j]; --j; }
         v[j + 1] = x;
     }
+}
+
+/*
+ * Policy 1: decayed usage score with admission ("Keeping the cache fresh": a
+ * usage score per expert decayed by 0.9 per token; a missed expert that scores
+ * higher than the weakest slot is promoted, up to a budget of copies).  Every
+ * miss is still computed (from the host store); only admitted ones take a slot.
+ *   clock += 1.  Token by token: every score *= 0.9, then each picked expert's
+ *   score += 1.  U, hits and misses as for LRU; the call must fit one stage
+ *   (|U| <= S), else -2.  Hits keep their slots (stamped).  Misses in order of
+ *   (score descending, id ascending); each, while the budget lasts (0 =
+ *   unlimited), takes the next empty slot (ascending index) if any, else the
+ *   weakest slot whose expert the call does not pick, by (score ascending,
+ *   index ascending), if its own score is strictly higher; otherwise it is
+ *   bypassed (slot -1, nothing evicted).  Every admission counts against the
+ *   budget.  Miss list in ascending expert order, all in stage 0.
+ */
+static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t *gpu_slot, int32_t *stage,
+                          int32_t *miss_expert, int32_t *miss_slot, int32_t *miss_evicted, int32_t *miss_stage,
+                          orc_plan_info *info) {
+    const int S = st->S, E = st->E;
+    memset(info, 0, sizeof(*info));
+    unsigned char *used = (unsigned char *)calloc((size_t)E, 1);
+    for (long p = 0; p < (long)T * k; ++p) used[ids[p]] = 1;
+    int nU = 0;
+    for (int e = 0; e < E; ++e) nU += used[e];
+    if (nU > S) { free(used); return -2; }
+    st->clock += 1;
+    const uint64_t now = st->clock;
+    for (int t = 0; t < T; ++t) {
+        for (int e = 0; e < E; ++e) st->score[e] = st->score[e] * 0.9;
+        for (int q = 0; q < k; ++q) st->score[ids[(long)t * k + q]] = st->score[ids[(long)t * k + q]] + 1.0;
+    }
+    int32_t *M = (int32_t *)malloc(sizeof(int32_t) * E), nM = 0;
+    int32_t *e_slot = (int32_t *)malloc(sizeof(int32_t) * E);
+    int32_t *d_old = (int32_t *)malloc(sizeof(int32_t) * E);
+    unsigned char *was_hit = (unsigned char *)calloc((size_t)E, 1);
+    int nH = 0;
+    for (int e = 0; e < E; ++e) {
+        e_slot[e] = -1;
+        d_old[e] = -1;
+        if (!used[e]) continue;
+        if (st->expert_slot[e] >= 0) {
+            was_hit[e] = 1;
+            ++nH;
+            e_slot[e] = st->expert_slot[e];
+            st->slot_stamp[e_slot[e]] = now;
+        } else {
+            M[nM++] = e;
+        }
+    }
+    info->n_unique = nU;
+    info->n_hits = nH;
+    info->n_miss = nM;
+    info->n_stages = 1;
+    for (long p = 0; p < (long)T * k; ++p) {
+        if (was_hit[ids[p]]) info->pick_hits++;
+        else info->pick_misses++;
+    }
+    /* empty slots ascending; slots of experts not picked, by (score, index) */
+    int *fr = (int *)malloc(sizeof(int) * S), nf = 0;
+    int *ev = (int *)malloc(sizeof(int) * S), nv = 0;
+    for (int s = 0; s < S; ++s) {
+        const int e = st->slot_expert[s];
+        if (e < 0) fr[nf++] = s;
+        else if (!used[e]) ev[nv++] = s;
+    }
+    for (int i = 1; i < nv; ++i) {         /* insertion sort by (score asc, index asc) */
+        int x = ev[i], j = i - 1;
+        while (j >= 0 && (st->score[st->slot_expert[x]] < st->score[st->slot_expert[ev[j]]] ||
+                          (st->score[st->slot_expert[x]] == st->score[st->slot_expert[ev[j]]] && x < ev[j]))) {
+            ev[j + 1] = ev[j];
+            --j;
+        }
+        ev[j + 1] = x;
+    }
+    /* misses by (score desc, id asc) */
+    int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (nM > 0 ? nM : 1));
+    for (int i = 0; i < nM; ++i) order[i] = M[i];
+    for (int i = 1; i < nM; ++i) {
+        int32_t x = order[i];
+        int j = i - 1;
+        while (j >= 0 && (st->score[x] > st->score[order[j]] || (st->score[x] == st->score[order[j]] && x < order[j]))) {
+            order[j + 1] = order[j];
+            --j;
+        }
+        order[j + 1] = x;
+    }
+    int remaining = st->budget > 0 ? st->budget : S + 1;
+    int fi = 0, vi = 0;
+    for (int i = 0; i < nM; ++i) {
+        const int m = order[i];
+        int s = -1, old = -1;
+        if (remaining > 0) {
+            if (fi < nf) s = fr[fi++];
+            else if (vi < nv && st->score[m] > st->score[st->slot_expert[ev[vi]]]) { s = ev[vi++]; old = st->slot_expert[s]; }
+        }
+        if (s >= 0) {
+            remaining -= 1;
+            if (old >= 0) { st->expert_slot[old] = -1; info->n_evict++; }
+            st->slot_expert[s] = m;
+            st->expert_slot[m] = s;
+            st->slot_stamp[s] = now;
+            e_slot[m] = s;
+            d_old[m] = old;
+        } else {
+            info->n_bypass++;
+        }
+    }
+    for (int i = 0; i < nM; ++i) {
+        miss_expert[i] = M[i];
+        miss_slot[i] = e_slot[M[i]];
+        miss_evicted[i] = d_old[M[i]];
+        miss_stage[i] = 0;
+    }
+    for (long p = 0; p < (long)T * k; ++p) {
+        gpu_slot[p] = e_slot[ids[p]];
+        stage[p] = 0;
+    }
+    free(used); free(M); free(e_slot); free(d_old); free(was_hit); free(fr); free(ev); free(order);
+    return 0;
 }
 
 /*
@@ -226,6 +364,8 @@ int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
                  int32_t *gpu_slot, int32_t *stage,
                  int32_t *miss_expert, int32_t *miss_slot, int32_t *miss_evicted,
                  int32_t *miss_stage, orc_plan_info *info) {
+    if (st->policy == 1)
+        return slot_map_score(st, ids, T, k, gpu_slot, stage, miss_expert, miss_slot, miss_evicted, miss_stage, info);
     const int S = st->S, E = st->E;
     memset(info, 0, sizeof(*info));
     st->clock += 1;
@@ -364,6 +504,7 @@ enum {
     ORC_STAT_BYTES_UPLOADED,
     ORC_STAT_STAGES,
     ORC_STAT_STAGED_CALLS,
+    ORC_STAT_BYPASSED,
     ORC_NSTAT
 };
 
@@ -379,7 +520,7 @@ typedef struct {
 
 orc_cache *orc_cache_new(int L, int E, int k, int H, int F, int S, int weight_mode,
                          const uint8_t *store, uint64_t layer_stride, uint64_t expert_stride,
-                         int n_threads) {
+                         int n_threads, int policy, int budget) {
     orc_cache *c = (orc_cache *)calloc(1, sizeof(orc_cache));
     c->L = L; c->E = E; c->k = k; c->H = H; c->F = F; c->S = S; c->weight_mode = weight_mode;
     c->store = store;
@@ -387,7 +528,10 @@ orc_cache *orc_cache_new(int L, int E, int k, int H, int F, int S, int weight_mo
     c->expert_stride = expert_stride;
     c->expert_bytes = 3ull * F * (H / 32) * 18;
     c->lru = (orc_lru **)malloc(sizeof(orc_lru *) * L);
-    for (int l = 0; l < L; ++l) c->lru[l] = orc_lru_new(S, E);
+    for (int l = 0; l < L; ++l) {
+        c->lru[l] = orc_lru_new(S, E);
+        orc_lru_set_policy(c->lru[l], policy, budget);
+    }
     c->slot_src = (const uint8_t **)calloc((size_t)L * S, sizeof(uint8_t *));
     c->stats = (uint64_t *)calloc((size_t)L * ORC_NSTAT, sizeof(uint64_t));
     c->n_threads = n_threads;
@@ -416,7 +560,8 @@ void orc_cache_stats(const orc_cache *c, int layer, uint64_t *out) {
  * Optional outputs: ids, w (double), gpu_slot, stage [T*k]; miss list arrays
  * [<= min(E, T*k)]; pair_visits [T*k] (how many times each (token, pick) pair
  * was computed); info.
- * Returns 0, or -1 when a logit is not finite (state untouched).
+ * Returns 0, -1 when a logit is not finite, -2 when the layer uses policy 1
+ * and the call needs more than one stage (state untouched in both cases).
  */
 int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *x, int x_bf16,
                       int T, int compute, float *out,
@@ -440,7 +585,10 @@ int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *
     int32_t *mv = (int32_t *)malloc(sizeof(int32_t) * maxm);
     int32_t *mst = (int32_t *)malloc(sizeof(int32_t) * maxm);
     orc_plan_info info;
-    orc_slot_map(c->lru[layer], ids, T, k, gpu_slot, stage, me, ms, mv, mst, &info);
+    if (orc_slot_map(c->lru[layer], ids, T, k, gpu_slot, stage, me, ms, mv, mst, &info) != 0) {
+        free(ids); free(w); free(gpu_slot); free(stage); free(me); free(ms); free(mv); free(mst);
+        return -2;  /* policy 1: the call needs more than one stage */
+    }
 
     uint64_t *st = c->stats + (size_t)layer * ORC_NSTAT;
     st[ORC_STAT_CALLS] += 1;
@@ -452,6 +600,7 @@ int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *
     st[ORC_STAT_BYTES_UPLOADED] += (uint64_t)info.n_miss * c->expert_bytes;
     st[ORC_STAT_STAGES] += (uint64_t)info.n_stages;
     st[ORC_STAT_STAGED_CALLS] += info.n_stages > 1 ? 1u : 0u;
+    st[ORC_STAT_BYPASSED] += (uint64_t)info.n_bypass;
 
     int32_t *visits = (int32_t *)calloc((size_t)P, sizeof(int32_t));
     const uint8_t **slot_src = c->slot_src + (size_t)layer * S;
@@ -468,7 +617,7 @@ int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *
      * every pair of the stage from its slot */
     for (int j = 0; j < info.n_stages; ++j) {
         for (int i = 0; i < info.n_miss; ++i)
-            if (mst[i] == j) slot_src[ms[i]] = layer_base + (size_t)me[i] * c->expert_stride;
+            if (mst[i] == j && ms[i] >= 0) slot_src[ms[i]] = layer_base + (size_t)me[i] * c->expert_stride;
         if (!compute) {
             for (long p = 0; p < P; ++p) if (stage[p] == j) visits[p] += 1;
             continue;
@@ -479,7 +628,9 @@ int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *
 #endif
         for (long p = 0; p < P; ++p) {
             if (stage[p] != j) continue;
-            const uint8_t *blk = slot_src[gpu_slot[p]];
+            /* a bypassed miss (policy 1) is computed from its store block */
+            const uint8_t *blk = gpu_slot[p] >= 0 ? slot_src[gpu_slot[p]]
+                                                  : layer_base + (size_t)ids[p] * c->expert_stride;
             orc_expert_ffn(blk, H, c->F, xd + (size_t)(p / k) * H, y + (size_t)p * H);
             visits[p] += 1;
         }

@@ -1,0 +1,128 @@
+"""The oracle's decayed-score admission policy against an independent
+brute-force simulator (CPU only), exhaustive on tiny traces and on long random
+traces, plus closed forms, invariants and the policy's independence of outputs."""
+import itertools
+import random
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.score_bruteforce import BruteScore
+
+
+def _compare(S, E, trace, budget=0):
+    o = oracle.LRU(S, E, policy=oracle.POLICY_SCORE, budget=budget)
+    b = BruteScore(S, E, budget)
+    for call in trace:
+        po = o.plan(np.array(call, dtype=np.int32))
+        pb = b.call([list(t) for t in call])
+        assert po["gpu_slot"].tolist() == pb["gpu_slot"], (S, budget, trace)
+        assert (po["stage"] == 0).all()
+        recs = list(zip(po["miss_expert"].tolist(), po["miss_slot"].tolist(),
+                        po["miss_evicted"].tolist(), po["miss_stage"].tolist()))
+        assert recs == pb["misses"], (S, budget, trace)
+        for key in ("n_unique", "n_hits", "n_miss", "n_stages", "n_evict", "n_bypass", "pick_hits",
+                    "pick_misses"):
+            assert po["info"][key] == pb[key], (key, S, budget, trace)
+        so, sb = o.state(), b.state()
+        assert so["slot_expert"].tolist() == sb["slot_expert"]
+        assert so["expert_slot"].tolist() == sb["expert_slot"]
+        assert so["slot_stamp"].tolist() == sb["slot_stamp"]
+        assert so["clock"] == sb["clock"]
+        assert o.scores().tolist() == b.score          # bit for bit: same operations in doubles
+        # a bypass happens only with no empty slot left or the budget used up
+        assert po["info"]["n_hits"] + po["info"]["n_miss"] == po["info"]["n_unique"]
+
+
+def _token_choices(E, k):
+    return [list(p) for p in itertools.permutations(range(E), k)]
+
+
+@pytest.mark.parametrize("budget", [0, 1])
+@pytest.mark.parametrize("S,k,T,length", [(1, 1, 1, 6), (2, 1, 1, 6), (3, 1, 1, 5), (2, 2, 1, 4),
+                                          (3, 1, 2, 3), (2, 1, 2, 3), (3, 3, 1, 3)])
+def test_exhaustive_small(S, k, T, length, budget):
+    E = 4
+    calls = [c for c in itertools.product(_token_choices(E, k), repeat=T)
+             if len({e for tok in c for e in tok}) <= S]
+    for trace in itertools.product(calls, repeat=length):
+        _compare(S, E, [list(c) for c in trace], budget)
+
+
+@pytest.mark.parametrize("S,E,k,T,budget", [(4, 8, 2, 2, 0), (8, 16, 4, 2, 0), (8, 16, 4, 2, 2),
+                                            (32, 128, 8, 1, 0), (32, 128, 8, 4, 0), (32, 128, 8, 1, 3)])
+def test_random_long(S, E, k, T, budget):
+    rng = random.Random(S * 7 + E * 3 + k + T + budget)
+    zipf = np.array([1.0 / (r + 1) ** 1.1 for r in range(E)])
+    zipf /= zipf.sum()
+    trace = []
+    for _ in range(60):
+        call = []
+        for _t in range(T):
+            tok = []
+            while len(tok) < k:
+                e = int(np.searchsorted(np.cumsum(zipf), rng.random()))
+                if e < E and e not in tok:
+                    tok.append(e)
+            call.append(tok)
+        if len({e for tok in call for e in tok}) <= S:
+            trace.append(call)
+    _compare(S, E, trace, budget)
+
+
+def test_score_closed_form():
+    # one expert picked n times in a row: 1 + 0.9 + ... + 0.9^(n-1) = 10 (1 - 0.9^n)
+    o = oracle.LRU(4, 8, policy=oracle.POLICY_SCORE)
+    for n in range(1, 60):
+        o.plan(np.array([[3]], dtype=np.int32))
+        assert abs(o.scores()[3] - 10.0 * (1.0 - 0.9 ** n)) < 1e-12
+        assert o.scores()[0] == 0.0
+    # then unused for m tokens: decays by 0.9^m
+    s0 = o.scores()[3]
+    for m in range(1, 20):
+        o.plan(np.array([[5]], dtype=np.int32))
+        assert abs(o.scores()[3] - s0 * 0.9 ** m) < 1e-12
+
+
+def test_hot_expert_survives_one_off_misses():
+    # LRU evicts the hot expert for a stream of one-off experts; the score
+    # policy keeps it (the one-offs are bypassed once the slot is full)
+    S, E = 1, 16
+    lru = oracle.LRU(S, E)
+    sc = oracle.LRU(S, E, policy=oracle.POLICY_SCORE)
+    for _ in range(5):
+        lru.plan(np.array([[0]], dtype=np.int32))
+        sc.plan(np.array([[0]], dtype=np.int32))
+    for e in range(1, 6):
+        lru.plan(np.array([[e]], dtype=np.int32))
+        p = sc.plan(np.array([[e]], dtype=np.int32))
+        assert p["miss_slot"].tolist() == [-1] and p["info"]["n_bypass"] == 1
+    assert sc.state()["slot_expert"].tolist() == [0]
+    assert lru.state()["slot_expert"].tolist() == [5]
+
+
+def test_multi_stage_call_rejected():
+    o = oracle.LRU(2, 8, policy=oracle.POLICY_SCORE)
+    with pytest.raises(ValueError):
+        o.plan(np.array([[0, 1, 2]], dtype=np.int32))
+    assert o.state()["clock"] == 0                   # state untouched
+
+
+def test_outputs_do_not_depend_on_the_policy():
+    # every pair is computed from its expert's store bytes either way
+    sh = synth.TINY
+    store = synth.store(1, sh.E, sh.H, sh.F, seed=3)
+    a = oracle.Cache(1, sh.E, sh.k, sh.H, sh.F, sh.S, store)
+    b = oracle.Cache(1, sh.E, sh.k, sh.H, sh.F, sh.S, store, policy=oracle.POLICY_SCORE)
+    rng = np.random.default_rng(3)
+    bypassed = 0
+    for _ in range(12):
+        lg = rng.standard_normal((1, sh.E)).astype(np.float32)
+        x = rng.standard_normal((1, sh.H)).astype(np.float32)
+        ra, rb = a.forward(0, lg, x), b.forward(0, lg, x)
+        assert np.array_equal(ra["out"], rb["out"])
+        bypassed += rb["info"]["n_bypass"]
+    assert b.stats(0)["bypassed"] == bypassed > 0
+    assert a.stats(0)["bypassed"] == 0
