@@ -63,6 +63,25 @@ extern "C" {
 #define MOE_ERR_POISONED 6      /* an earlier call on this handle failed          */
 #define MOE_ERR_UNSUPPORTED 7   /* shape outside what the kernels implement       */
 
+/* Slot replacement policy.
+ * MOE_POLICY_LRU: every miss takes a slot; victims are empty slots, then the
+ *   least recently used slots whose expert the call does not pick.
+ * MOE_POLICY_SCORE ("Keeping the cache fresh": a decayed usage score per
+ *   expert, x0.9 per token; a miss that scores higher than the weakest slot is
+ *   promoted, up to a budget of copies): per layer, token by token every
+ *   expert's score is multiplied by 0.9 and each picked expert gains 1 (fp64).
+ *   Misses, strongest first (score descending, then lower id), take an empty
+ *   slot if any, else the weakest slot whose expert the call does not pick
+ *   (score ascending, then lower index) if their score is strictly higher,
+ *   while admit_budget lasts; other misses are bypassed: computed from the host
+ *   store like any miss but not cached (miss_slot -1, counted in `bypassed`).
+ *   Needs every call to fit one stage and the decode layer kernel: max_tokens x
+ *   top_k <= min(slots_per_layer, 32), max_tokens <= 8, no tensor-core GEMM
+ *   (gemm_min_tokens 0 or > max_tokens), and the pull fill or the memcpy fill
+ *   with stream memory writes; otherwise init returns MOE_ERR_UNSUPPORTED. */
+#define MOE_POLICY_LRU 0
+#define MOE_POLICY_SCORE 1
+
 /* How misses reach their slots. */
 #define MOE_FILL_MEMCPY 0  /* cudaMemcpyAsync per missed block on a side stream into a
                               staging area, overlapped with hit compute; then a device
@@ -85,6 +104,9 @@ typedef struct {
     int32_t fill_mode;       /* MOE_FILL_MEMCPY or MOE_FILL_PULL                   */
     int32_t gemm_min_tokens; /* calls with n_tokens >= this use the tensor-core
                                 grouped GEMM (bf16 activations only); 0 = never    */
+    int32_t policy;          /* slot replacement: MOE_POLICY_LRU (0) or
+                                MOE_POLICY_SCORE (1, see below)                   */
+    int32_t admit_budget;    /* MOE_POLICY_SCORE: admissions per call, 0 = no limit */
     int32_t reserved;        /* must be 0                                          */
     int64_t timeout_us;      /* limit of every bounded host wait, > 0; the decode
                                 layer kernel's device waits use a quarter of it,
@@ -108,6 +130,7 @@ typedef struct {
     uint64_t bytes_uploaded; /* unique_misses x expert block bytes                 */
     uint64_t stages;         /* sum over calls of the number of stages             */
     uint64_t staged_calls;   /* calls that needed more than one stage              */
+    uint64_t bypassed;       /* misses computed without taking a slot (policy 1)   */
     int32_t poisoned;        /* 1 once a call on the handle has failed             */
     int32_t last_error;      /* the code that poisoned it (or MOE_OK)              */
     int32_t cuda_error;      /* the cudaError_t behind MOE_ERR_CUDA (0 if none)     */

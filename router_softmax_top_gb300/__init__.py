@@ -30,6 +30,9 @@ MOE_FILL_PULL = 1
 
 MOE_INJECT_DECODE_WAIT = 1
 
+MOE_POLICY_LRU = 0
+MOE_POLICY_SCORE = 1
+
 # every symbol include/moe_cache.h declares
 EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_stats",
            "moe_layer_last_plan", "moe_cache_inject", "moe_cache_set_timing", "moe_cache_timing",
@@ -43,6 +46,7 @@ class MoeCacheConfig(ctypes.Structure):
                 ("slots_per_layer", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("weight_mode", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
                 ("fill_mode", ctypes.c_int32), ("gemm_min_tokens", ctypes.c_int32),
+                ("policy", ctypes.c_int32), ("admit_budget", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("timeout_us", ctypes.c_int64)]
 
 
@@ -56,7 +60,8 @@ class MoeCacheStats(ctypes.Structure):
                 ("pick_misses", ctypes.c_uint64), ("unique_hits", ctypes.c_uint64),
                 ("unique_misses", ctypes.c_uint64), ("evictions", ctypes.c_uint64),
                 ("bytes_uploaded", ctypes.c_uint64), ("stages", ctypes.c_uint64),
-                ("staged_calls", ctypes.c_uint64), ("poisoned", ctypes.c_int32),
+                ("staged_calls", ctypes.c_uint64), ("bypassed", ctypes.c_uint64),
+                ("poisoned", ctypes.c_int32),
                 ("last_error", ctypes.c_int32), ("cuda_error", ctypes.c_int32),
                 ("reserved", ctypes.c_int32)]
 
@@ -189,10 +194,12 @@ class MoECache:
     def __init__(self, *, n_layers, n_experts, top_k, hidden, ffn, slots_per_layer, max_tokens,
                  store, weight_mode=0, act_dtype="f32", fill_mode=MOE_FILL_MEMCPY,
                  gemm_min_tokens=0, timeout_us=10_000_000, layer_stride=None,
-                 expert_stride=None, stream=None):
-        self.cfg = MoeCacheConfig(n_layers, n_experts, top_k, hidden, ffn, slots_per_layer,
-                                  max_tokens, weight_mode, 1 if act_dtype == "bf16" else 0,
-                                  fill_mode, gemm_min_tokens, 0, timeout_us)
+                 expert_stride=None, stream=None, policy=MOE_POLICY_LRU, admit_budget=0):
+        self.cfg = MoeCacheConfig(n_layers=n_layers, n_experts=n_experts, top_k=top_k, hidden=hidden,
+                                  ffn=ffn, slots_per_layer=slots_per_layer, max_tokens=max_tokens,
+                                  weight_mode=weight_mode, act_dtype=1 if act_dtype == "bf16" else 0,
+                                  fill_mode=fill_mode, gemm_min_tokens=gemm_min_tokens, policy=policy,
+                                  admit_budget=admit_budget, reserved=0, timeout_us=timeout_us)
         eb = moe_expert_bytes(hidden, ffn)
         self.expert_bytes = eb
         if isinstance(store, tuple):

@@ -14,8 +14,8 @@ namespace moe {
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 constexpr int kPlanThreads = 256;
-constexpr int kNStat = 9;  // calls, pick_hits, pick_misses, unique_hits, unique_misses,
-                           // evictions, bytes_uploaded, stages, staged_calls
+constexpr int kNStat = 10;  // calls, pick_hits, pick_misses, unique_hits, unique_misses,
+                            // evictions, bytes_uploaded, stages, staged_calls, bypassed
 constexpr int kTokPerUnit = 8;  // tokens of one expert handled by one GEMV work unit
 constexpr int kGemmN = 128;     // routed pairs of one expert per tensor-core GEMM tile
 
@@ -156,7 +156,11 @@ struct PlanArgs {
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;
   uint32_t *epoch;    // the handle's call counter (device), advanced by every accepted call
+  int policy;         // 0 LRU, 1 decayed score with admission (plan_small_kernel only)
+  int admit_budget;   // policy 1: admissions per call, 0 = no limit
+  double *score;      // policy 1: the layer's decayed usage scores [E]
 };
+bool plan_small_ok(int T, int E, int k, int S);
 
 cudaError_t launch_plan(const PlanArgs &a, cudaStream_t st);
 size_t plan_smem_bytes(int E, int S);

@@ -242,15 +242,17 @@ __device__ __forceinline__ bool ring_wait(uint64_t *bar, uint32_t parity, uint64
 
 // Block b of row `row` of the item's tiles (row = 32 * tile-in-item + lane):
 // nibbles and scale bits; a miss also writes the block's tiled form into its
-// slot (fill on the way).
+// slot (fill on the way), unless it has none (a bypassed miss).
 __device__ __forceinline__ void load_block(const unsigned char *buf, bool miss, int nt, int row, int b, int nb,
                                            uint8_t *slot, const MatLayout &L, int tile0, uint4 &qv,
                                            unsigned short &db) {
   if (miss) {
     qv = canon_block(buf, row, b, nb, db);
-    const uint64_t e = tile_elem(tile0 * 32 + row, b, nb);
-    reinterpret_cast<uint4 *>(slot + L.nib_off)[e] = qv;
-    reinterpret_cast<unsigned short *>(slot + L.sc_off)[e] = db;
+    if (slot) {
+      const uint64_t e = tile_elem(tile0 * 32 + row, b, nb);
+      reinterpret_cast<uint4 *>(slot + L.nib_off)[e] = qv;
+      reinterpret_cast<unsigned short *>(slot + L.sc_off)[e] = db;
+    }
   } else {
     const int i = ((row >> 5) * nb + b) * 32 + (row & 31);
     qv = reinterpret_cast<const uint4 *>(buf)[i];
@@ -551,7 +553,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     const bool is_down = wk.mat == 2;
     const int nb = L.nb, K = 32 * nb, n = it.pair_count;
     const unsigned char *buf = ring + (size_t)s * slot_bytes;
-    uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
+    uint8_t *slot = it.slot >= 0 ? j.slots + (uint64_t)it.slot * j.slot_stride : nullptr;
 
     if (!is_down) {
       // ---- one 32-row tile of gate or up: inputs are the call's staged rows

@@ -57,6 +57,7 @@ struct moe_cache {
   cudaEvent_t ev_fin = nullptr;
   int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
   uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
+  double *d_score = nullptr;  // MOE_POLICY_SCORE: decayed usage per (layer, expert)
 
   // per-call scratch
   int32_t *d_ids = nullptr, *d_gpu_slot = nullptr, *d_stage = nullptr, *d_perm = nullptr;
@@ -236,6 +237,7 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_slot_stamp);
   cudaFree(c->d_clock);
   cudaFree(c->d_stats);
+  cudaFree(c->d_score);
   cudaFree(c->d_ids);
   cudaFree(c->d_gpu_slot);
   cudaFree(c->d_stage);
@@ -278,6 +280,8 @@ int check_config(const moe_cache_config *g) {
   if (g->act_dtype != 0 && g->act_dtype != 1) return MOE_ERR_INVALID_ARG;
   if (g->fill_mode != MOE_FILL_MEMCPY && g->fill_mode != MOE_FILL_PULL) return MOE_ERR_INVALID_ARG;
   if (g->gemm_min_tokens < 0 || g->reserved != 0 || g->timeout_us <= 0) return MOE_ERR_INVALID_ARG;
+  if ((g->policy != MOE_POLICY_LRU && g->policy != MOE_POLICY_SCORE) || g->admit_budget < 0)
+    return MOE_ERR_INVALID_ARG;
   if (g->hidden < 64 || g->hidden % 64 || g->ffn < 64 || g->ffn % 64) return MOE_ERR_UNSUPPORTED;
   if (g->hidden > 16384 || g->ffn > 16384) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -377,6 +381,8 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_slot_stamp, (size_t)L * S) == cudaSuccess;
   ok = ok && dalloc(&c->d_clock, (size_t)L) == cudaSuccess;
   ok = ok && dalloc(&c->d_stats, (size_t)L * kNStat) == cudaSuccess;
+  ok = ok && dalloc(&c->d_score, (size_t)L * E) == cudaSuccess &&
+       cudaMemset(c->d_score, 0, sizeof(double) * L * E) == cudaSuccess;
   ok = ok && dalloc(&c->d_ids, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_gpu_slot, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_stage, c->maxP) == cudaSuccess;
@@ -429,6 +435,17 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
     ok = cudaMalloc(&c->d_staging, eb) == cudaSuccess;
   }
   if (!ok) return fail(MOE_ERR_OOM);
+  // the score policy plans every call as one stage in the small plan kernel and
+  // runs it on the decode layer kernel (a bypassed miss is computed there from
+  // the host store, or from staging, without taking a slot)
+  if (cfg->policy == MOE_POLICY_SCORE) {
+    const int T = cfg->max_tokens, k = cfg->top_k;
+    const bool fill_ok = cfg->fill_mode == MOE_FILL_PULL || c->write_value32 != nullptr;
+    const bool gemm_off = cfg->gemm_min_tokens == 0 || cfg->gemm_min_tokens > T;
+    if (T > kTokPerUnit || T * k > std::min(S, 32) || !plan_small_ok(T, E, k, S) || !gemm_off || !fill_ok ||
+        !decode_layer_supported(cfg->hidden, cfg->ffn, T))
+      return fail(MOE_ERR_UNSUPPORTED);
+  }
 
   // mapped mailbox and error word
   c->mail_stage_cap = c->maxStages + 1;
@@ -538,12 +555,16 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.route_bad = c->d_route_bad;
   pa.routed = 0;
   pa.epoch = c->d_epoch;
+  pa.policy = g.policy;
+  pa.admit_budget = g.admit_budget;
+  pa.score = c->d_score + (size_t)layer * E;
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
   // memcpy fill, one stage guaranteed (distinct experts <= slots), few tokens:
   // the decode layer kernel too, its misses read from staging as they land
   const bool use_decode_mc = g.fill_mode == MOE_FILL_MEMCPY && c->write_value32 && !use_gemm && maxU <= S &&
                              maxU <= c->staging_blocks && decode_layer_supported(g.hidden, g.ffn, T);
   pa.sync_n = 2 + maxU + ((use_decode || use_decode_mc) ? T * (g.hidden / 32) : 0);
+  if (g.policy == MOE_POLICY_SCORE && !use_decode && !use_decode_mc) return MOE_ERR_UNSUPPORTED;
   pa.mailbox = need_host ? c->d_mail : nullptr;
   pa.mailbox_stage_cap = c->mail_stage_cap;
   pa.seq = c->seq;
@@ -895,6 +916,7 @@ MOE_API int moe_cache_stats(const moe_cache *cc, int32_t layer, moe_cache_stats_
   out->bytes_uploaded = acc[6];
   out->stages = acc[7];
   out->staged_calls = acc[8];
+  out->bypassed = acc[9];
   if (const int de = device_error_code(c)) poison(c, de);
   out->poisoned = c->poisoned;
   out->last_error = c->last_error;

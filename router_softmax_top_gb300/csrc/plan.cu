@@ -520,6 +520,8 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
   __shared__ int32_t s_ids[32];  // the routed ids, pair order (P <= 32)
+  __shared__ double s_score[kMaxExperts];  // policy 1: the layer's decayed usage scores
+  __shared__ int s_fr[kSmallMaxSlots];     // policy 1: empty slots, ascending
   // Launched as a programmatic dependent of the kernel before it: until
   // griddepcontrol.wait it reads only the layer's state and the handle's
   // counters, which only earlier plan kernels write (complete before that
@@ -534,6 +536,10 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   for (int i = lane; i < E; i += 32)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_es[i])), "l"(a.expert_slot + i)
                  : "memory");
+  if (a.policy == 1)
+    for (int i = lane; i < E; i += 32)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(&s_score[i])), "l"(a.score + i)
+                   : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");
   const unsigned long long now = *a.clock + 1ull;
   const uint32_t epoch = *a.epoch + 1u;  // loaded early: the header is the last thing written
@@ -566,6 +572,18 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   if (s_bad) {
     write_error(a);
     return;
+  }
+
+  // policy 1: token by token every score x0.9, then each pick +1 (fp64, no
+  // fused operations: the same bits as any plain evaluation of the rule)
+  if (a.policy == 1) {
+    for (int t = 0; t < T; ++t) {
+      for (int i = lane; i < E; i += 32) s_score[i] = __dmul_rn(s_score[i], 0.9);
+      __syncwarp();
+      if (lane < k) s_score[s_ids[t * k + lane]] = __dadd_rn(s_score[s_ids[t * k + lane]], 1.0);
+      __syncwarp();
+    }
+    for (int i = lane; i < E; i += 32) a.score[i] = s_score[i];
   }
 
   // distinct experts: one leader lane per expert
@@ -612,68 +630,141 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const int tot_hit_pairs = field(total, 2), tot_hit_units = field(total, 4);
   const int hr = field(before, 0), mr = field(before, 1);
 
-  // stage-0 victims: empty slots (by index), then unpinned slots by (stamp, index);
-  // miss rank r takes the r-th smallest key
-  __syncwarp();
-  unsigned long long key = ~0ull;
-  for (int c = 0; c * 32 < S; ++c) {
-    const int sl = c * 32 + lane;
-    if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
-      const int se = s_se[sl];
-      const unsigned long long kk =
-          se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
-      key = kk < key ? kk : key;
-    }
-  }
-  // lanes hold their smallest remaining key; keys beyond one per lane stay in s_key
-  const int kpl = (S + 31) / 32;
-  if (kpl > 1) {
+  int vslot = -1, evicted = -1;  // a miss leader's slot (-1: bypassed) and the expert it replaces
+  if (a.policy == 1) {
+    // decayed score with admission: rounds over the misses, strongest first
+    // (score descending, lower id); each takes the next empty slot, else the
+    // weakest slot whose expert the call does not pick (score ascending, lower
+    // index) if strictly stronger, while the budget lasts; the first miss that
+    // cannot be admitted ends the rounds (every later one is weaker: bypassed)
+    const int kpl = (S + 31) / 32;
+    int nf = 0;
     for (int c = 0; c < kpl; ++c) {
       const int sl = c * 32 + lane;
-      unsigned long long kk = ~0ull;
-      if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
-        const int se = s_se[sl];
-        kk = se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
-      }
-      s_key[sl] = kk;
+      const bool em = sl < S && s_se[sl] < 0;
+      const unsigned m = __ballot_sync(F, em);
+      if (em) s_fr[nf + __popc(m & ((1u << lane) - 1u))] = sl;
+      nf += __popc(m);
+    }
+    uint32_t evbits = 0;  // this lane's evictable slots, bit c = slot c * 32 + lane
+    for (int c = 0; c < kpl; ++c) {
+      const int sl = c * 32 + lane;
+      if (sl < S && s_se[sl] >= 0 && !((s_pinned[c] >> lane) & 1u)) evbits |= 1u << c;
     }
     __syncwarp();
-  }
-  int my_victim = -1;  // lane r holds the victim of miss rank r
-  for (int r = 0; r < nM; ++r) {
-    const unsigned hi = __reduce_min_sync(F, (unsigned)(key >> 32));
-    const unsigned lo = __reduce_min_sync(F, (unsigned)(key >> 32) == hi ? (unsigned)key : 0xffffffffu);
-    const unsigned long long best = ((unsigned long long)hi << 32) | lo;
-    const int sl = (int)(best & 2047ull);
-    if (lane == r) my_victim = sl;
-    if (lane == (sl & 31)) {
-      // the owner drops the taken key and exposes its next smallest
-      if (kpl == 1) {
-        key = ~0ull;
-      } else {
-        s_key[sl] = ~0ull;
-        key = ~0ull;
-        for (int c = 0; c < kpl; ++c) {
-          const unsigned long long kk = s_key[c * 32 + lane];
-          key = kk < key ? kk : key;
+    bool pend = miss;
+    int remaining = a.admit_budget > 0 ? a.admit_budget : S + 1, used_free = 0;
+    for (int r = 0; r < nM; ++r) {
+      double bs = pend ? s_score[e] : -1.0;
+      int bi = pend ? e : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const double os = __shfl_xor_sync(F, bs, o);
+        const int oi = __shfl_xor_sync(F, bi, o);
+        if (os > bs || (os == bs && oi < bi)) { bs = os; bi = oi; }
+      }
+      int slot = -1, old = -1;
+      if (remaining > 0) {
+        if (used_free < nf) {
+          slot = s_fr[used_free++];
+        } else {
+          double ws = __longlong_as_double(0x7ff0000000000000ll);  // +inf
+          int wsl = 0x7fffffff;
+          for (int c = 0; c < kpl; ++c)
+            if ((evbits >> c) & 1u) {
+              const int sl = c * 32 + lane;
+              const double sc = s_score[s_se[sl]];
+              if (sc < ws || (sc == ws && sl < wsl)) { ws = sc; wsl = sl; }
+            }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const double os = __shfl_xor_sync(F, ws, o);
+            const int osl = __shfl_xor_sync(F, wsl, o);
+            if (os < ws || (os == ws && osl < wsl)) { ws = os; wsl = osl; }
+          }
+          if (wsl != 0x7fffffff && bs > ws) {
+            slot = wsl;
+            old = s_se[wsl];
+            if ((wsl & 31) == lane) evbits &= ~(1u << (wsl >> 5));
+          }
+        }
+      }
+      if (slot >= 0) --remaining;
+      if (pend && e == bi) {
+        vslot = slot;
+        evicted = old;
+        pend = false;
+      }
+      if (slot < 0) break;
+    }
+  } else {
+    // stage-0 victims: empty slots (by index), then unpinned slots by (stamp, index);
+    // miss rank r takes the r-th smallest key
+    __syncwarp();
+    unsigned long long key = ~0ull;
+    for (int c = 0; c * 32 < S; ++c) {
+      const int sl = c * 32 + lane;
+      if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
+        const int se = s_se[sl];
+        const unsigned long long kk =
+            se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
+        key = kk < key ? kk : key;
+      }
+    }
+    // lanes hold their smallest remaining key; keys beyond one per lane stay in s_key
+    const int kpl = (S + 31) / 32;
+    if (kpl > 1) {
+      for (int c = 0; c < kpl; ++c) {
+        const int sl = c * 32 + lane;
+        unsigned long long kk = ~0ull;
+        if (sl < S && !((s_pinned[c] >> lane) & 1u)) {
+          const int se = s_se[sl];
+          kk = se < 0 ? (unsigned long long)sl : (1ull << 62) | ((unsigned long long)s_st[sl] << 11) | (unsigned)sl;
+        }
+        s_key[sl] = kk;
+      }
+      __syncwarp();
+    }
+    int my_victim = -1;  // lane r holds the victim of miss rank r
+    for (int r = 0; r < nM; ++r) {
+      const unsigned hi = __reduce_min_sync(F, (unsigned)(key >> 32));
+      const unsigned lo = __reduce_min_sync(F, (unsigned)(key >> 32) == hi ? (unsigned)key : 0xffffffffu);
+      const unsigned long long best = ((unsigned long long)hi << 32) | lo;
+      const int sl = (int)(best & 2047ull);
+      if (lane == r) my_victim = sl;
+      if (lane == (sl & 31)) {
+        // the owner drops the taken key and exposes its next smallest
+        if (kpl == 1) {
+          key = ~0ull;
+        } else {
+          s_key[sl] = ~0ull;
+          key = ~0ull;
+          for (int c = 0; c < kpl; ++c) {
+            const unsigned long long kk = s_key[c * 32 + lane];
+            key = kk < key ? kk : key;
+          }
         }
       }
     }
+    const int v = __shfl_sync(F, my_victim, miss ? mr : 0);
+    if (miss) {
+      vslot = v;
+      evicted = s_se[v];
+    }
   }
-  const int vslot = __shfl_sync(F, my_victim, miss ? mr : 0);
   const int my_slot = hit ? es0 : (miss ? vslot : -1);
-  const int evicted = miss ? s_se[vslot] : -1;
+  const int n_bypass = __popc(__ballot_sync(F, miss && vslot < 0));
   const int n_evict = __popc(__ballot_sync(F, miss && evicted >= 0));
   __syncwarp();
 
-  // new state
-  if (miss) {
+  // new state (a bypassed miss changes nothing)
+  if (miss && vslot >= 0) {
     a.slot_expert[vslot] = e;
     a.expert_slot[e] = vslot;
     a.slot_stamp[vslot] = now;
     if (evicted >= 0) a.expert_slot[evicted] = -1;
-    a.miss[mr] = MissItem{e, vslot, evicted, 0};
   }
+  if (miss) a.miss[mr] = MissItem{e, vslot, evicted, 0};
   if (hit) a.slot_stamp[es0] = now;
 
   // per-pair slot and stage
@@ -726,6 +817,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     atomicAdd(st + 5, (unsigned long long)n_evict);
     atomicAdd(st + 6, (unsigned long long)nM * a.expert_bytes);
     atomicAdd(st + 7, 1ull);
+    if (n_bypass) atomicAdd(st + 9, (unsigned long long)n_bypass);
     if (a.mailbox) {
       a.mailbox->hdr = h;
       int32_t *mub = reinterpret_cast<int32_t *>(a.mailbox + 1);

@@ -34,7 +34,7 @@ class Pair:
     """A CUDA cache and an oracle cache over the same pinned host store."""
 
     def __init__(self, L, E, k, H, F, S, store, max_tokens, fill_mode=0, act="f32",
-                 weight_mode=0, gemm_min_tokens=0, timeout_us=20_000_000):
+                 weight_mode=0, gemm_min_tokens=0, timeout_us=20_000_000, policy=0, admit_budget=0):
         import router_softmax_top_gb300 as moe
         self.moe = moe
         self.L, self.E, self.k, self.H, self.F, self.S = L, E, k, H, F, S
@@ -43,8 +43,10 @@ class Pair:
         self.gpu = moe.MoECache(n_layers=L, n_experts=E, top_k=k, hidden=H, ffn=F,
                                 slots_per_layer=S, max_tokens=max_tokens, store=store,
                                 weight_mode=weight_mode, act_dtype=act, fill_mode=fill_mode,
-                                gemm_min_tokens=gemm_min_tokens, timeout_us=timeout_us)
-        self.orc = oracle.Cache(L, E, k, H, F, S, store.numpy(), weight_mode=weight_mode)
+                                gemm_min_tokens=gemm_min_tokens, timeout_us=timeout_us,
+                                policy=policy, admit_budget=admit_budget)
+        self.orc = oracle.Cache(L, E, k, H, F, S, store.numpy(), weight_mode=weight_mode, policy=policy,
+                                admit_budget=admit_budget)
 
     def close(self):
         self.gpu.close()
@@ -78,5 +80,5 @@ def assert_plan_equal(plan, res, where=""):
 
 def assert_stats_equal(gpu_stats, orc_stats):
     for key in ("calls", "pick_hits", "pick_misses", "unique_hits", "unique_misses", "evictions",
-                "bytes_uploaded", "stages", "staged_calls"):
+                "bytes_uploaded", "stages", "staged_calls", "bypassed"):
         assert gpu_stats[key] == orc_stats[key], key

@@ -163,7 +163,7 @@ def test_inject_rejects_unknown_code(store):
 
 def test_unaligned_store_rejected(store):
     import ctypes
-    cfg = moe.MoeCacheConfig(1, TINY.E, TINY.k, TINY.H, TINY.F, TINY.S, 4, 0, 0, 0, 0, 0, 10**6)
+    cfg = moe.MoeCacheConfig(1, TINY.E, TINY.k, TINY.H, TINY.F, TINY.S, 4, 0, 0, 0, 0, 0, 0, 0, 10**6)
     hs = moe.MoeHostStore(store.data_ptr() + 2, store.numel() - 2, TINY.E * TINY.expert_bytes,
                           TINY.expert_bytes)
     h = ctypes.c_void_p()

@@ -58,13 +58,13 @@ def test_host_only_calls(lib):
 def test_init_rejects_bad_config_before_any_cuda_call(lib):
     store = moe.MoeHostStore(None, 0, 0, 0)
     h = ctypes.c_void_p()
-    bad = moe.MoeCacheConfig(1, 8, 9, 256, 512, 4, 4, 0, 0, 0, 0, 0, 1000)  # k > E
+    bad = moe.MoeCacheConfig(1, 8, 9, 256, 512, 4, 4, 0, 0, 0, 0, 0, 0, 0, 1000)  # k > E
     assert lib.moe_cache_init(ctypes.byref(bad), ctypes.byref(store), None, ctypes.byref(h)) \
         == moe.MOE_ERR_INVALID_ARG
-    bad = moe.MoeCacheConfig(1, 8, 2, 250, 512, 4, 4, 0, 0, 0, 0, 0, 1000)  # H not a multiple of 64
+    bad = moe.MoeCacheConfig(1, 8, 2, 250, 512, 4, 4, 0, 0, 0, 0, 0, 0, 0, 1000)  # H not a multiple of 64
     assert lib.moe_cache_init(ctypes.byref(bad), ctypes.byref(store), None, ctypes.byref(h)) \
         == moe.MOE_ERR_UNSUPPORTED
-    good = moe.MoeCacheConfig(1, 8, 2, 256, 512, 4, 4, 0, 0, 0, 0, 0, 1000)
+    good = moe.MoeCacheConfig(1, 8, 2, 256, 512, 4, 4, 0, 0, 0, 0, 0, 0, 0, 1000)
     assert lib.moe_cache_init(ctypes.byref(good), ctypes.byref(store), None, ctypes.byref(h)) \
         == moe.MOE_ERR_HOST_STORE   # null store
     assert not h.value
