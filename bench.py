@@ -94,6 +94,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--fill", default="pull", choices=["memcpy", "pull"])
+    ap.add_argument("--policy", default="lru", choices=["lru", "score"],
+                    help="slot replacement: LRU, or the decayed-score admission policy (decode workload)")
+    ap.add_argument("--admit-budget", type=int, default=0,
+                    help="score policy: admissions per call (0 = no limit)")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--cpu-sample-steps", type=int, default=96)  # ~14 s of oracle work on 16 cores
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -399,9 +403,10 @@ def main():
     x_d = torch.from_numpy(x_h).cuda()               # [steps, L, 1, H]
     out_d = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
     fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
+    policy = moe.MOE_POLICY_SCORE if args.policy == "score" else moe.MOE_POLICY_LRU
     cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
                          slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=fill,
-                         timeout_us=30_000_000)
+                         timeout_us=30_000_000, policy=policy, admit_budget=args.admit_budget)
     setup_s = time.time() - t_setup
     h2d_gbps = cache.probe_h2d(24)
     L = moe.lib()
@@ -624,9 +629,12 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": dev_ms_max / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": workload_config(sh, args.fill),
+        "config": dict(workload_config(sh, args.fill), policy=args.policy,
+                       **({"admit_budget": args.admit_budget} if args.policy == "score" else {})),
         "hit_rate": {"pick": d["pick_hits"] / max(1, picks_t),
-                     "unique": d["unique_hits"] / max(1, uniq)},
+                     "unique": d["unique_hits"] / max(1, uniq),
+                     "evictions_per_call": d["evictions"] / max(1, d["calls"]),
+                     "bypassed_per_call": d["bypassed"] / max(1, d["calls"])},
         "cold_start": {"steps": W, "tokens_per_s": W / (cold_ms * 1e-3),
                        "pick_hit_rate": cold["pick_hits"] / max(1, cold["pick_hits"] + cold["pick_misses"])},
         "achieved_hbm_gbs_step": (d["unique_hits"] + d["unique_misses"]) * sh.expert_bytes / (dev_ms * 1e-3) / 1e9,
