@@ -69,7 +69,7 @@ extern "C" {
  * MOE_POLICY_SCORE ("Keeping the cache fresh": a decayed usage score per
  *   expert, x0.9 per token; a miss that scores higher than the weakest slot is
  *   promoted, up to a budget of copies): per layer, token by token every
- *   expert's score is multiplied by 0.9 and each picked expert gains 1 (fp64).
+ *   expert's score is multiplied by 0.9 and each picked expert gains 1 (fp32).
  *   Misses, strongest first (score descending, then lower id), take an empty
  *   slot if any, else the weakest slot whose expert the call does not pick
  *   (score ascending, then lower index) if their score is strictly higher,

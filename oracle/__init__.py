@@ -170,8 +170,8 @@ class LRU:
         return {"slot_expert": se, "expert_slot": es, "slot_stamp": ss, "clock": int(clk.value)}
 
     def scores(self) -> np.ndarray:
-        """The decayed usage scores [E] (policy 1)."""
-        out = np.empty(self.E, np.float64)
+        """The decayed usage scores [E] (policy 1, fp32)."""
+        out = np.empty(self.E, np.float32)
         lib().orc_lru_scores(self._h, _p(out))
         return out
 

@@ -150,7 +150,7 @@ typedef struct {
     uint64_t clock;        /* number of calls planned so far                   */
     int policy;            /* 0: LRU; 1: decayed usage score with admission    */
     int budget;            /* policy 1: admissions per call, 0 = unlimited     */
-    double *score;         /* [E]  policy 1: decayed usage per expert          */
+    float *score;          /* [E]  policy 1: decayed usage per expert (fp32)   */
 } orc_lru;
 
 orc_lru *orc_lru_new(int S, int E) {
@@ -165,7 +165,7 @@ orc_lru *orc_lru_new(int S, int E) {
     st->clock = 0;
     st->policy = 0;
     st->budget = 0;
-    st->score = (double *)calloc((size_t)E, sizeof(double));
+    st->score = (float *)calloc((size_t)E, sizeof(float));
     return st;
 }
 
@@ -175,8 +175,8 @@ void orc_lru_set_policy(orc_lru *st, int policy, int budget) {
     st->budget = budget;
 }
 
-/* Copy of the decayed scores [E] (policy 1). */
-void orc_lru_scores(const orc_lru *st, double *out) { memcpy(out, st->score, sizeof(double) * st->E); }
+/* Copy of the decayed scores [E] (policy 1, fp32). */
+void orc_lru_scores(const orc_lru *st, float *out) { memcpy(out, st->score, sizeof(float) * st->E); }
 
 void orc_lru_free(orc_lru *st) {
     if (!st) return;
@@ -227,7 +227,7 @@ static void sort_victims(const orc_lru *st, int *v, int n) {
  * higher than the weakest slot is promoted, up to a budget of copies).  Every
  * miss is still computed (from the host store); only admitted ones take a slot.
  *   clock += 1.  Token by token: every score *= 0.9, then each picked expert's
- *   score += 1.  U, hits and misses as for LRU; the call must fit one stage
+ *   score += 1, in fp32 (each operation rounded).  U, hits and misses as for LRU; the call must fit one stage
  *   (|U| <= S), else -2.  Hits keep their slots (stamped).  Misses in order of
  *   (score descending, id ascending); each, while the budget lasts (0 =
  *   unlimited), takes the next empty slot (ascending index) if any, else the
@@ -249,8 +249,8 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
     st->clock += 1;
     const uint64_t now = st->clock;
     for (int t = 0; t < T; ++t) {
-        for (int e = 0; e < E; ++e) st->score[e] = st->score[e] * 0.9;
-        for (int q = 0; q < k; ++q) st->score[ids[(long)t * k + q]] = st->score[ids[(long)t * k + q]] + 1.0;
+        for (int e = 0; e < E; ++e) st->score[e] = st->score[e] * 0.9f;
+        for (int q = 0; q < k; ++q) st->score[ids[(long)t * k + q]] = st->score[ids[(long)t * k + q]] + 1.0f;
     }
     int32_t *M = (int32_t *)malloc(sizeof(int32_t) * E), nM = 0;
     int32_t *e_slot = (int32_t *)malloc(sizeof(int32_t) * E);

@@ -158,7 +158,7 @@ struct PlanArgs {
   uint32_t *epoch;    // the handle's call counter (device), advanced by every accepted call
   int policy;         // 0 LRU, 1 decayed score with admission (plan_small_kernel only)
   int admit_budget;   // policy 1: admissions per call, 0 = no limit
-  double *score;      // policy 1: the layer's decayed usage scores [E]
+  float *score;       // policy 1: the layer's decayed usage scores [E] (fp32)
 };
 bool plan_small_ok(int T, int E, int k, int S);
 

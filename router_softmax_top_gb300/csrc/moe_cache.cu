@@ -57,7 +57,7 @@ struct moe_cache {
   cudaEvent_t ev_fin = nullptr;
   int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
   uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
-  double *d_score = nullptr;  // MOE_POLICY_SCORE: decayed usage per (layer, expert)
+  float *d_score = nullptr;  // MOE_POLICY_SCORE: decayed usage per (layer, expert), fp32
 
   // per-call scratch
   int32_t *d_ids = nullptr, *d_gpu_slot = nullptr, *d_stage = nullptr, *d_perm = nullptr;
@@ -382,7 +382,7 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_clock, (size_t)L) == cudaSuccess;
   ok = ok && dalloc(&c->d_stats, (size_t)L * kNStat) == cudaSuccess;
   ok = ok && dalloc(&c->d_score, (size_t)L * E) == cudaSuccess &&
-       cudaMemset(c->d_score, 0, sizeof(double) * L * E) == cudaSuccess;
+       cudaMemset(c->d_score, 0, sizeof(float) * L * E) == cudaSuccess;
   ok = ok && dalloc(&c->d_ids, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_gpu_slot, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_stage, c->maxP) == cudaSuccess;

@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
   __shared__ int32_t s_ids[32];  // the routed ids, pair order (P <= 32)
-  __shared__ double s_score[kMaxExperts];  // policy 1: the layer's decayed usage scores
+  __shared__ float s_score[kMaxExperts];   // policy 1: the layer's decayed usage scores
   __shared__ int s_fr[kSmallMaxSlots];     // policy 1: empty slots, ascending
   // Launched as a programmatic dependent of the kernel before it: until
   // griddepcontrol.wait it reads only the layer's state and the handle's
@@ -538,7 +538,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
                  : "memory");
   if (a.policy == 1)
     for (int i = lane; i < E; i += 32)
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(&s_score[i])), "l"(a.score + i)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_score[i])), "l"(a.score + i)
                    : "memory");
   asm volatile("cp.async.commit_group;" ::: "memory");
   const unsigned long long now = *a.clock + 1ull;
@@ -574,13 +574,13 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     return;
   }
 
-  // policy 1: token by token every score x0.9, then each pick +1 (fp64, no
-  // fused operations: the same bits as any plain evaluation of the rule)
+  // policy 1: token by token every score x0.9, then each pick +1 (fp32, each
+  // operation rounded, none fused: the same bits as any plain evaluation)
   if (a.policy == 1) {
     for (int t = 0; t < T; ++t) {
-      for (int i = lane; i < E; i += 32) s_score[i] = __dmul_rn(s_score[i], 0.9);
+      for (int i = lane; i < E; i += 32) s_score[i] = __fmul_rn(s_score[i], 0.9f);
       __syncwarp();
-      if (lane < k) s_score[s_ids[t * k + lane]] = __dadd_rn(s_score[s_ids[t * k + lane]], 1.0);
+      if (lane < k) s_score[s_ids[t * k + lane]] = __fadd_rn(s_score[s_ids[t * k + lane]], 1.0f);
       __syncwarp();
     }
     for (int i = lane; i < E; i += 32) a.score[i] = s_score[i];
@@ -655,11 +655,11 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     bool pend = miss;
     int remaining = a.admit_budget > 0 ? a.admit_budget : S + 1, used_free = 0;
     for (int r = 0; r < nM; ++r) {
-      double bs = pend ? s_score[e] : -1.0;
+      float bs = pend ? s_score[e] : -1.f;
       int bi = pend ? e : 0x7fffffff;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const double os = __shfl_xor_sync(F, bs, o);
+        const float os = __shfl_xor_sync(F, bs, o);
         const int oi = __shfl_xor_sync(F, bi, o);
         if (os > bs || (os == bs && oi < bi)) { bs = os; bi = oi; }
       }
@@ -668,17 +668,17 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
         if (used_free < nf) {
           slot = s_fr[used_free++];
         } else {
-          double ws = __longlong_as_double(0x7ff0000000000000ll);  // +inf
+          float ws = __int_as_float(0x7f800000);  // +inf
           int wsl = 0x7fffffff;
           for (int c = 0; c < kpl; ++c)
             if ((evbits >> c) & 1u) {
               const int sl = c * 32 + lane;
-              const double sc = s_score[s_se[sl]];
+              const float sc = s_score[s_se[sl]];
               if (sc < ws || (sc == ws && sl < wsl)) { ws = sc; wsl = sl; }
             }
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) {
-            const double os = __shfl_xor_sync(F, ws, o);
+            const float os = __shfl_xor_sync(F, ws, o);
             const int osl = __shfl_xor_sync(F, wsl, o);
             if (os < ws || (os == ws && osl < wsl)) { ws = os; wsl = osl; }
           }

@@ -6,7 +6,8 @@ expert, x0.9 per token; a missed expert that scores higher than the weakest
 slot is promoted, up to a budget of copies; every miss is still computed):
 
   * one clock tick per call; token by token every score is multiplied by 0.9
-    and each picked expert gains 1;
+    and each picked expert gains 1, in single precision (each operation
+    rounded to float32);
   * distinct picked experts U; hits keep their slots and get the tick; the call
     must fit one stage (|U| <= S);
   * misses are considered strongest first (score descending, then lower id);
@@ -18,6 +19,7 @@ slot is promoted, up to a budget of copies; every miss is still computed):
 
 Plain lists and dictionaries.
 """
+import numpy as np
 
 
 class BruteScore:
@@ -26,7 +28,7 @@ class BruteScore:
         self.holder = [None] * S
         self.used_at = [0] * S
         self.tick = 0
-        self.score = [0.0] * E
+        self.score = [np.float32(0.0)] * E
 
     def call(self, tokens):
         S = self.S
@@ -35,9 +37,9 @@ class BruteScore:
         self.tick += 1
         now = self.tick
         for tok in tokens:
-            self.score = [v * 0.9 for v in self.score]
+            self.score = [np.float32(v * np.float32(0.9)) for v in self.score]
             for e in tok:
-                self.score[e] = self.score[e] + 1.0
+                self.score[e] = np.float32(self.score[e] + np.float32(1.0))
         where = {e: s for s, e in enumerate(self.holder) if e is not None}
         hits = [e for e in wanted if e in where]
         misses = [e for e in wanted if e not in where]
