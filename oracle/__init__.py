@@ -78,6 +78,7 @@ def lib() -> ctypes.CDLL:
             L.orc_cache_lru.restype = vp
             L.orc_cache_lru.argtypes = [vp, i32]
             L.orc_cache_stats.argtypes = [vp, i32, vp]
+            L.orc_cache_preload.argtypes = [vp, vp]
             L.orc_layer_forward.restype = i32
             L.orc_layer_forward.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp,
                                             vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -220,6 +221,12 @@ class Cache:
 
     def lru(self, layer: int) -> LRU:
         return LRU._borrow(lib().orc_cache_lru(self._h, layer), self.S, self.E)
+
+    def preload(self, counts: np.ndarray):
+        """Warm start: per layer the S most-used experts (counts [L, E]) in slots 0, 1, ..."""
+        c = np.ascontiguousarray(counts, dtype=np.uint32)
+        assert c.shape == (self.L, self.E)
+        lib().orc_cache_preload(self._h, _p(c))
 
     def forward(self, layer: int, logits: np.ndarray, x: np.ndarray | None, compute: bool = True):
         lg = np.ascontiguousarray(logits, dtype=np.float32)

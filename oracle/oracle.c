@@ -549,6 +549,45 @@ void orc_cache_free(orc_cache *c) {
 
 orc_lru *orc_cache_lru(orc_cache *c, int layer) { return c->lru[layer]; }
 
+/*
+ * Warm start from a usage profile ("Persistent hot experts": each layer's
+ * most-used experts are preloaded before the first request).  counts[L][E]:
+ * usage per (layer, expert).  Per layer, the experts with a non-zero count,
+ * by (count descending, id ascending), the first S of them in slots 0, 1, ...;
+ * every other slot empty; stamps 0; the clock, scores and counters unchanged.
+ */
+void orc_cache_preload(orc_cache *c, const uint32_t *counts) {
+    for (int l = 0; l < c->L; ++l) {
+        orc_lru *st = c->lru[l];
+        const uint32_t *cnt = counts + (size_t)l * c->E;
+        int32_t *order = (int32_t *)malloc(sizeof(int32_t) * c->E);
+        int n = 0;
+        for (int e = 0; e < c->E; ++e)
+            if (cnt[e] > 0) order[n++] = e;
+        for (int i = 1; i < n; ++i) {      /* insertion sort by (count desc, id asc) */
+            int32_t x = order[i];
+            int j = i - 1;
+            while (j >= 0 && (cnt[x] > cnt[order[j]] || (cnt[x] == cnt[order[j]] && x < order[j]))) {
+                order[j + 1] = order[j];
+                --j;
+            }
+            order[j + 1] = x;
+        }
+        for (int e = 0; e < c->E; ++e) st->expert_slot[e] = -1;
+        for (int sl = 0; sl < c->S; ++sl) {
+            st->slot_expert[sl] = -1;
+            st->slot_stamp[sl] = 0;
+            c->slot_src[(size_t)l * c->S + sl] = NULL;
+        }
+        for (int i = 0; i < n && i < c->S; ++i) {
+            st->slot_expert[i] = order[i];
+            st->expert_slot[order[i]] = i;
+            c->slot_src[(size_t)l * c->S + i] = c->store + (size_t)l * c->layer_stride + (size_t)order[i] * c->expert_stride;
+        }
+        free(order);
+    }
+}
+
 void orc_cache_stats(const orc_cache *c, int layer, uint64_t *out) {
     memcpy(out, c->stats + (size_t)layer * ORC_NSTAT, sizeof(uint64_t) * ORC_NSTAT);
 }
