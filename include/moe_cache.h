@@ -190,6 +190,21 @@ int moe_layer_last_plan(const moe_cache *c, int32_t layer, int32_t *ids, float *
                         int32_t *n_miss, int32_t *n_stages);
 
 /*
+ * Warm start from a usage profile ("Persistent hot experts": each layer's
+ * most-used experts are preloaded before the first request).  counts: host
+ * array [n_layers][n_experts] of usage counts (e.g. saved from an earlier
+ * session).  Per layer, the experts with a non-zero count, by (count
+ * descending, id ascending), the first slots_per_layer of them are copied from
+ * the host store into slots 0, 1, ...; every other slot becomes empty; the
+ * layer's recency stamps become 0.  The call counter, the scores of
+ * MOE_POLICY_SCORE and the statistics do not change.  Stream-ordered on
+ * cuda_stream (between calls, not during one) and synchronises with it before
+ * returning.  NULL handle or counts: MOE_ERR_INVALID_ARG; a poisoned handle:
+ * MOE_ERR_POISONED; CUDA failures poison the handle (MOE_ERR_CUDA).
+ */
+int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream);
+
+/*
  * Test hook: fault injection without a GPU fault.  what = MOE_INJECT_DECODE_WAIT
  * makes the next call that runs the decode layer kernel (pull fill, one stage,
  * <= 8 tokens) wait, in its down items, for a gate value carrying a call number

@@ -35,7 +35,8 @@ MOE_POLICY_SCORE = 1
 
 # every symbol include/moe_cache.h declares
 EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_stats",
-           "moe_layer_last_plan", "moe_cache_inject", "moe_cache_set_timing", "moe_cache_timing",
+           "moe_layer_last_plan", "moe_cache_preload", "moe_cache_inject", "moe_cache_set_timing",
+           "moe_cache_timing",
            "moe_cache_probe_h2d", "moe_expert_bytes", "moe_cache_launch_count",
            "moe_cache_destroy", "moe_strerror", "moe_expert_ffn_static")
 
@@ -103,6 +104,8 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_timing.restype = ctypes.c_int
         L.moe_cache_timing.argtypes = [vp, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(u64),
                                        ctypes.POINTER(ctypes.c_double), i32, ctypes.POINTER(i32)]
+        L.moe_cache_preload.restype = ctypes.c_int
+        L.moe_cache_preload.argtypes = [vp, vp, vp]
         L.moe_cache_inject.restype = ctypes.c_int
         L.moe_cache_inject.argtypes = [vp, i32]
         L.moe_cache_probe_h2d.restype = ctypes.c_int
@@ -212,7 +215,7 @@ class MoECache:
         ls = n_experts * es if layer_stride is None else layer_stride
         self.store = MoeHostStore(addr, nbytes, ls, es)
         self.handle = moe_cache_init(self.cfg, self.store, stream)
-        self.k, self.E, self.H, self.F = top_k, n_experts, hidden, ffn
+        self.L, self.k, self.E, self.H, self.F = n_layers, top_k, n_experts, hidden, ffn
 
     def close(self):
         if getattr(self, "handle", None):
@@ -267,6 +270,18 @@ class MoECache:
                 "gpu_slot": gs.reshape(n_tokens, self.k), "stage": stg.reshape(n_tokens, self.k),
                 "miss_expert": me[:n].copy(), "miss_slot": ms[:n].copy(),
                 "miss_evicted": mv[:n].copy(), "miss_stage": mst[:n].copy(), "n_stages": ns.value}
+
+    def preload(self, counts, stream=None):
+        """Warm start: per layer the most-used experts of counts [L, E] (moe_cache_preload)."""
+        import numpy as np
+        c = np.ascontiguousarray(counts, dtype=np.uint32)
+        if c.shape != (self.L, self.E):
+            raise ValueError(f"counts must be [{self.L}, {self.E}]")
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        _check(lib().moe_cache_preload(self.handle, ctypes.c_void_p(c.ctypes.data), ctypes.c_void_p(stream)),
+               "moe_cache_preload")
 
     def inject(self, what: int):
         """Test hook: fault injection without a GPU fault (moe_cache_inject)."""

@@ -990,6 +990,99 @@ MOE_API int moe_cache_timing(moe_cache *c, const char **names, uint64_t *launche
   return MOE_OK;
 }
 
+MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream) {
+  if (!c || !counts) return MOE_ERR_INVALID_ARG;
+  if (c->poisoned) return MOE_ERR_POISONED;
+  const int L = c->cfg.n_layers, E = c->cfg.n_experts, S = c->cfg.slots_per_layer;
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  // the new state: per layer the S most-used experts, by (count desc, id asc)
+  std::vector<int32_t> se((size_t)L * S, -1), es((size_t)L * E, -1);
+  std::vector<std::vector<int32_t>> chosen(L);
+  for (int l = 0; l < L; ++l) {
+    const uint32_t *cnt = counts + (size_t)l * E;
+    std::vector<int32_t> order;
+    for (int e = 0; e < E; ++e)
+      if (cnt[e] > 0) order.push_back(e);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cnt[x] > cnt[y]; });
+    if ((int)order.size() > S) order.resize(S);
+    for (int i = 0; i < (int)order.size(); ++i) {
+      se[(size_t)l * S + i] = order[i];
+      es[(size_t)l * E + order[i]] = i;
+    }
+    chosen[l] = std::move(order);
+  }
+  // contents: the blocks copied from the host store into their slots by the
+  // fill kernel (one stage of "misses" per layer; through staging, a chunk at
+  // a time, when the store has no device mapping)
+  MissItem *d_list = nullptr;
+  PlanHdr *d_h = nullptr;
+  if (dalloc(&d_list, (size_t)S) != cudaSuccess || dalloc(&d_h, 1) != cudaSuccess) {
+    cudaFree(d_list);
+    return MOE_ERR_OOM;
+  }
+  int rc = MOE_OK;
+  const int chunk = c->host_dev ? S : std::max(1, c->staging_blocks);
+  std::vector<MissItem> items(S);
+  for (int l = 0; l < L && rc == MOE_OK; ++l) {
+    const int m = (int)chosen[l].size();
+    for (int lo = 0; lo < m && rc == MOE_OK; lo += chunk) {
+      const int n = std::min(chunk, m - lo);
+      PlanHdr h = {};
+      h.n_stages = 1;
+      h.n_stage0_miss = n;
+      h.n_miss = n;
+      for (int i = 0; i < n; ++i) items[i] = MissItem{chosen[l][lo + i], lo + i, -1, 0};
+      RepackArgs ra;
+      ra.slots = c->d_slots + (size_t)l * S * c->lay.stride;
+      ra.slot_stride = c->lay.stride;
+      ra.lay = c->lay;
+      ra.miss = d_list;
+      ra.hdr = d_h;
+      ra.stage = 0;
+      const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) + (size_t)l * c->store.layer_stride;
+      bool ok = cudaMemcpyAsync(d_list, items.data(), sizeof(MissItem) * n, cudaMemcpyHostToDevice, st) ==
+                    cudaSuccess &&
+                cudaMemcpyAsync(d_h, &h, sizeof(PlanHdr), cudaMemcpyHostToDevice, st) == cudaSuccess;
+      if (c->host_dev) {
+        ra.src_base = c->host_dev;
+        ra.src_layer_off = (uint64_t)l * c->store.layer_stride;
+        ra.src_expert_stride = c->store.expert_stride;
+        ra.src_slot_stride = 0;
+        ra.by_expert = 1;
+      } else {
+        for (int i = 0; ok && i < n; ++i)
+          ok = cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
+                               lbase + (size_t)items[i].expert * c->store.expert_stride, c->expert_bytes,
+                               cudaMemcpyHostToDevice, st) == cudaSuccess;
+        ra.src_base = c->d_staging;
+        ra.src_layer_off = 0;
+        ra.src_expert_stride = 0;
+        ra.src_slot_stride = c->expert_bytes;
+        ra.by_expert = 0;
+      }
+      ok = ok && launch_repack(ra, S, n, st) == cudaSuccess;
+      // the host copies of this chunk's lists are reused by the next one
+      ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+      if (!ok) rc = MOE_ERR_CUDA;
+    }
+  }
+  if (rc == MOE_OK &&
+      (cudaMemcpyAsync(c->d_slot_expert, se.data(), sizeof(int32_t) * se.size(), cudaMemcpyHostToDevice, st) !=
+           cudaSuccess ||
+       cudaMemcpyAsync(c->d_expert_slot, es.data(), sizeof(int32_t) * es.size(), cudaMemcpyHostToDevice, st) !=
+           cudaSuccess ||
+       cudaMemsetAsync(c->d_slot_stamp, 0, sizeof(uint64_t) * (size_t)L * S, st) != cudaSuccess ||
+       cudaStreamSynchronize(st) != cudaSuccess))
+    rc = MOE_ERR_CUDA;
+  cudaFree(d_list);
+  cudaFree(d_h);
+  if (rc != MOE_OK) {
+    cudaGetLastError();
+    return poison(c, rc);
+  }
+  return MOE_OK;
+}
+
 MOE_API int moe_cache_inject(moe_cache *c, int32_t what) {
   if (!c || (what != 0 && what != MOE_INJECT_DECODE_WAIT)) return MOE_ERR_INVALID_ARG;
   c->inject = what;
