@@ -34,6 +34,7 @@ import synth  # noqa: E402
 
 METRIC = "MoE-layer tokens/s on 1 GB300; achieved HBM GB/s vs roofline; cache hit rate"
 UNIT = "tokens/s"
+PROFILE_STREAM = 777   # token stream that the warm-start profile is counted over (the timed one is 0)
 
 
 
@@ -98,6 +99,9 @@ def parse():
                     help="slot replacement: LRU, or the decayed-score admission policy (decode workload)")
     ap.add_argument("--admit-budget", type=int, default=0,
                     help="score policy: admissions per call (0 = no limit)")
+    ap.add_argument("--preload-profile", type=int, default=0,
+                    help="warm start: before the first step, preload each layer's most-used experts, "
+                         "counted over this many tokens of another token stream with the same routing")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--cpu-sample-steps", type=int, default=96)  # ~14 s of oracle work on 16 cores
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -407,6 +411,18 @@ def main():
     cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
                          slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=fill,
                          timeout_us=30_000_000, policy=policy, admit_budget=args.admit_budget)
+    preload = None
+    if args.preload_profile:
+        # usage counts from another token stream (same routing: same seed and layer)
+        counts = np.zeros((sh.L, sh.E), np.uint32)
+        for l in range(sh.L):
+            pp = synth.trace(args.preload_profile, sh.E, sh.k, sh.zipf, sh.sticky, rank, l, PROFILE_STREAM)
+            np.add.at(counts[l], pp.reshape(-1), 1)
+        t0 = time.time()
+        cache.preload(counts)
+        preload = {"profile_tokens": args.preload_profile, "stream": PROFILE_STREAM,
+                   "experts": int(np.minimum((counts > 0).sum(1), sh.S).sum()),
+                   "s": time.time() - t0}
     setup_s = time.time() - t_setup
     h2d_gbps = cache.probe_h2d(24)
     L = moe.lib()
@@ -636,7 +652,8 @@ def main():
                      "evictions_per_call": d["evictions"] / max(1, d["calls"]),
                      "bypassed_per_call": d["bypassed"] / max(1, d["calls"])},
         "cold_start": {"steps": W, "tokens_per_s": W / (cold_ms * 1e-3),
-                       "pick_hit_rate": cold["pick_hits"] / max(1, cold["pick_hits"] + cold["pick_misses"])},
+                       "pick_hit_rate": cold["pick_hits"] / max(1, cold["pick_hits"] + cold["pick_misses"]),
+                       "preload": preload},
         "achieved_hbm_gbs_step": (d["unique_hits"] + d["unique_misses"]) * sh.expert_bytes / (dev_ms * 1e-3) / 1e9,
         "roofline": roofline,
         "roofline_hbm": roofline_hbm,

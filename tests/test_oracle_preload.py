@@ -61,3 +61,20 @@ def test_outputs_do_not_depend_on_the_preload():
         x = rng.standard_normal((2, sh.H)).astype(np.float32)
         assert np.array_equal(a.forward(0, lg, x)["out"], b.forward(0, lg, x)["out"])
     assert b.stats(0)["unique_hits"] > a.stats(0)["unique_hits"]
+
+
+def test_preloaded_slots_are_evicted_in_slot_order():
+    # all preloaded slots carry stamp 0: the least recently used is the lowest
+    # slot index, and a slot used since is younger than every untouched one
+    c, _ = _cache(S=4)
+    c.preload(np.array([[0, 5, 5, 1, 0, 9, 2, 0]], dtype=np.uint32))   # slots: 5 1 2 6
+    lg = np.full((1, 8), -3.0, np.float32)
+    lg[0, 5], lg[0, 7] = 2.0, 1.0                                 # 5 hits (slot 0), 7 misses
+    r = c.forward(0, lg, None, compute=False)
+    assert r["miss_expert"].tolist() == [7]
+    assert r["miss_slot"].tolist() == [1] and r["miss_evicted"].tolist() == [1]
+    lg = np.full((1, 8), -3.0, np.float32)
+    lg[0, 0], lg[0, 4] = 2.0, 1.0                                 # two misses
+    r = c.forward(0, lg, None, compute=False)
+    assert sorted(r["miss_slot"].tolist()) == [2, 3]
+    assert sorted(r["miss_evicted"].tolist()) == [2, 6]
