@@ -103,6 +103,11 @@ def parse():
                     help="warm start: before the first step, preload each layer's most-used experts, "
                          "counted over this many tokens of another token stream with the same routing")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
+    ap.add_argument("--tokens", type=int, default=512,
+                    help="prefill workload: tokens per batch (one call per layer and batch)")
+    ap.add_argument("--gemm-min-tokens", type=int, default=64,
+                    help="prefill workload: calls of at least this many tokens take the tensor-core "
+                         "grouped GEMM, shorter ones the GEMV kernels (0 = never the GEMM)")
     ap.add_argument("--cpu-sample-steps", type=int, default=96)  # ~14 s of oracle work on 16 cores
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -263,16 +268,17 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------ prefill
-def prefill_config(sh, fill):
+def prefill_config(sh, fill, T=512, gemm_min=64):
+    path = ("the tensor-core grouped GEMM" if gemm_min and T >= gemm_min else "the Q4_0 GEMV kernels")
     return {
         "workload": (f"prefill: {sh.L} MoE layers, {sh.E} experts/layer, top-{sh.k}, hidden {sh.H}, "
                      f"expert FFN {sh.F}, Q4_0 experts in host RAM (pinned and mapped by the library), "
                      f"{sh.S} slots/layer, "
-                     f"512 tokens per batch through the tensor-core grouped GEMM, Zipf({sh.zipf}) routing "
+                     f"{T} tokens per batch through {path}, Zipf({sh.zipf}) routing "
                      f"with {int(sh.sticky * 100)}% of picks copied from the previous token, bf16 "
                      f"activations N(0,1)"),
         "layers": sh.L, "experts": sh.E, "top_k": sh.k, "hidden": sh.H, "ffn": sh.F,
-        "slots_per_layer": sh.S, "tokens_per_step": 512, "fill_mode": fill,
+        "slots_per_layer": sh.S, "tokens_per_step": T, "gemm_min_tokens": gemm_min, "fill_mode": fill,
         "l2": "inputs larger than L2: each batch streams the stage-wise expert weights and activations "
               "(~1 GB per layer-batch) through HBM",
     }
@@ -286,7 +292,8 @@ def run_prefill(args):
     if args.layers:
         import dataclasses
         sh = dataclasses.replace(sh, L=min(sh.L, args.layers))
-    T = 512
+    T = args.tokens
+    assert T >= 1 and args.gemm_min_tokens >= 0
     W, K = max(3, args.warmup), args.steps
     torch.cuda.set_device(0)
     eb = sh.expert_bytes
@@ -300,7 +307,7 @@ def run_prefill(args):
     fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
     cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
                          slots_per_layer=sh.S, max_tokens=T, store=store, act_dtype="bf16",
-                         fill_mode=fill, gemm_min_tokens=64, timeout_us=60_000_000)
+                         fill_mode=fill, gemm_min_tokens=args.gemm_min_tokens, timeout_us=60_000_000)
     h2d_gbps = cache.probe_h2d(24)
     fwd = moe.lib().moe_layer_forward
     sh_ = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -351,7 +358,8 @@ def run_prefill(args):
     value = K * T / (ms * 1e-3)
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16", "data": "synthetic", "config": prefill_config(sh, args.fill),
+            "dtype": "bf16", "data": "synthetic",
+            "config": prefill_config(sh, args.fill, T, args.gemm_min_tokens),
             "hit_rate": {"pick": d["pick_hits"] / max(1, d["pick_hits"] + d["pick_misses"]),
                          "unique": d["unique_hits"] / max(1, d["unique_hits"] + d["unique_misses"])},
             "roofline": roof,

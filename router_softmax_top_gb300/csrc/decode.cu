@@ -756,16 +756,21 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   j.inject = inject;
   j.err = a.err;
   // single-token calls: two compute groups and four items in flight per CTA;
-  // otherwise one group, three items in flight when they fit, else two
+  // two tokens: two groups and three items when they fit (with more tokens the
+  // second group's registers spill and it loses); otherwise one group, three
+  // items in flight when they fit, else two
   const bool two = T == 1 && decode_smem(a.H, a.F, T, 4, 2) <= kDecodeSmemCap;
+  const bool two3 = !two && T == 2 && decode_smem(a.H, a.F, T, 3, 2) <= kDecodeSmemCap;
   const bool nb3 = decode_smem(a.H, a.F, T, 3, 1) <= kDecodeSmemCap;
-  const size_t smem = two ? decode_smem(a.H, a.F, T, 4, 2) : decode_smem(a.H, a.F, T, nb3 ? 3 : 2, 1);
+  const size_t smem = two    ? decode_smem(a.H, a.F, T, 4, 2)
+                      : two3 ? decode_smem(a.H, a.F, T, 3, 2)
+                             : decode_smem(a.H, a.F, T, nb3 ? 3 : 2, 1);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_sms);
-  cfg.blockDim = dim3(decode_threads(two ? 2 : 1));
+  cfg.blockDim = dim3(decode_threads(two || two3 ? 2 : 1));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
@@ -775,9 +780,11 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, j);
   };
-  static size_t c412 = 0, c311 = 0, c211 = 0, c381 = 0, c281 = 0;
+  static size_t c412 = 0, c322 = 0, c311 = 0, c211 = 0, c341 = 0, c381 = 0, c281 = 0;
   if (two) return go(decode_layer_kernel<4, 1, 2>, c412);
+  if (two3) return go(decode_layer_kernel<3, 2, 2>, c322);
   if (T == 1) return nb3 ? go(decode_layer_kernel<3, 1, 1>, c311) : go(decode_layer_kernel<2, 1, 1>, c211);
+  if (T <= 4 && nb3) return go(decode_layer_kernel<3, 4, 1>, c341);
   return nb3 ? go(decode_layer_kernel<3, kTokPerUnit, 1>, c381) : go(decode_layer_kernel<2, kTokPerUnit, 1>, c281);
 }
 
