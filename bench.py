@@ -105,7 +105,7 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--tokens", type=int, default=512,
                     help="prefill workload: tokens per batch (one call per layer and batch)")
-    ap.add_argument("--gemm-min-tokens", type=int, default=64,
+    ap.add_argument("--gemm-min-tokens", type=int, default=16,
                     help="prefill workload: calls of at least this many tokens take the tensor-core "
                          "grouped GEMM, shorter ones the GEMV kernels (0 = never the GEMM)")
     ap.add_argument("--cpu-sample-steps", type=int, default=96)  # ~14 s of oracle work on 16 cores
@@ -268,7 +268,7 @@ def run_reference(args):
 
 
 # ------------------------------------------------------------ prefill
-def prefill_config(sh, fill, T=512, gemm_min=64):
+def prefill_config(sh, fill, T=512, gemm_min=16):
     path = ("the tensor-core grouped GEMM" if gemm_min and T >= gemm_min else "the Q4_0 GEMV kernels")
     return {
         "workload": (f"prefill: {sh.L} MoE layers, {sh.E} experts/layer, top-{sh.k}, hidden {sh.H}, "

@@ -103,7 +103,11 @@ typedef struct {
     int32_t act_dtype;       /* 0: x is fp32 [T,H]; 1: x is bf16 [T,H]             */
     int32_t fill_mode;       /* MOE_FILL_MEMCPY or MOE_FILL_PULL                   */
     int32_t gemm_min_tokens; /* calls with n_tokens >= this use the tensor-core
-                                grouped GEMM (bf16 activations only); 0 = never    */
+                                grouped GEMM (bf16 activations only); 0 = never.
+                                Shorter calls take the GEMV kernels.  Measured
+                                on GB300 (hidden 2816, FFN 704, top-8, 32
+                                slots): GEMV ahead up to 8 tokens, even at
+                                12-16, GEMM ahead from 24; 16 is the switch   */
     int32_t policy;          /* slot replacement: MOE_POLICY_LRU (0) or
                                 MOE_POLICY_SCORE (1, see below)                   */
     int32_t admit_budget;    /* MOE_POLICY_SCORE: admissions per call, 0 = no limit */
