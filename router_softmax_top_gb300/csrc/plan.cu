@@ -508,6 +508,9 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
 constexpr int kSmallMaxSlots = 256;
 constexpr int kRouteGridMin = 64;  // calls with more tokens route in their own grid
 
+// POLICY: MOE_POLICY_LRU (0) or MOE_POLICY_SCORE (1); the LRU instance carries
+// none of the score code or its shared memory.
+template <int POLICY>
 __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const unsigned F = 0xffffffffu;
   const int E = a.E, S = a.S, k = a.k, T = a.T, P = T * k;
@@ -520,8 +523,8 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   __shared__ unsigned long long s_pack[kMaxExperts];
   __shared__ unsigned long long s_key[kSmallMaxSlots];
   __shared__ int32_t s_ids[32];  // the routed ids, pair order (P <= 32)
-  __shared__ float s_score[kMaxExperts];   // policy 1: the layer's decayed usage scores
-  __shared__ int s_fr[kSmallMaxSlots];     // policy 1: empty slots, ascending
+  __shared__ float s_score[POLICY == 1 ? kMaxExperts : 1];  // policy 1: the layer's decayed usage scores
+  __shared__ int s_fr[POLICY == 1 ? kSmallMaxSlots : 1];      // policy 1: empty slots, ascending
   // Launched as a programmatic dependent of the kernel before it: until
   // griddepcontrol.wait it reads only the layer's state and the handle's
   // counters, which only earlier plan kernels write (complete before that
@@ -536,7 +539,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   for (int i = lane; i < E; i += 32)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_es[i])), "l"(a.expert_slot + i)
                  : "memory");
-  if (a.policy == 1)
+  if constexpr (POLICY == 1)
     for (int i = lane; i < E; i += 32)
       asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(&s_score[i])), "l"(a.score + i)
                    : "memory");
@@ -576,7 +579,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
 
   // policy 1: token by token every score x0.9, then each pick +1 (fp32, each
   // operation rounded, none fused: the same bits as any plain evaluation)
-  if (a.policy == 1) {
+  if constexpr (POLICY == 1) {
     for (int t = 0; t < T; ++t) {
       for (int i = lane; i < E; i += 32) s_score[i] = __fmul_rn(s_score[i], 0.9f);
       __syncwarp();
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   const int hr = field(before, 0), mr = field(before, 1);
 
   int vslot = -1, evicted = -1;  // a miss leader's slot (-1: bypassed) and the expert it replaces
-  if (a.policy == 1) {
+  if constexpr (POLICY == 1) {
     // decayed score with admission: rounds over the misses, strongest first
     // (score descending, lower id); each takes the next empty slot, else the
     // weakest slot whose expert the call does not pick (score ascending, lower
@@ -869,7 +872,8 @@ cudaError_t launch_plan(const PlanArgs &a_in, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, plan_small_kernel, a_in);
+    return a_in.policy == 1 ? cudaLaunchKernelEx(&cfg, plan_small_kernel<1>, a_in)
+                            : cudaLaunchKernelEx(&cfg, plan_small_kernel<0>, a_in);
   }
   PlanArgs a = a_in;
   a.routed = 0;
