@@ -26,6 +26,7 @@ STAT_NAMES = ("calls", "pick_hits", "pick_misses", "unique_hits", "unique_misses
 
 POLICY_LRU = 0
 POLICY_SCORE = 1
+POLICY_ADOPT = 2   # LRU; a call of more than one stage ends holding its most-used experts
 
 
 class PlanInfo(ctypes.Structure):

@@ -148,7 +148,8 @@ typedef struct {
     int32_t *expert_slot;  /* [E]  slot of each expert, -1 = not cached        */
     uint64_t *slot_stamp;  /* [S]  call counter of the slot's last use         */
     uint64_t clock;        /* number of calls planned so far                   */
-    int policy;            /* 0: LRU; 1: decayed usage score with admission    */
+    int policy;            /* 0: LRU; 1: decayed usage score with admission;
+                              2: LRU, staged calls keep their most-used experts */
     int budget;            /* policy 1: admissions per call, 0 = unlimited     */
     float *score;          /* [E]  policy 1: decayed usage per expert (fp32)   */
 } orc_lru;
@@ -169,7 +170,8 @@ orc_lru *orc_lru_new(int S, int E) {
     return st;
 }
 
-/* Replacement policy of the state: 0 = LRU (default), 1 = decayed score. */
+/* Replacement policy of the state: 0 = LRU (default), 1 = decayed score,
+ * 2 = LRU with adopt (staged calls end holding their most-used experts). */
 void orc_lru_set_policy(orc_lru *st, int policy, int budget) {
     st->policy = policy;
     st->budget = budget;
@@ -242,7 +244,8 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
     const int S = st->S, E = st->E;
     memset(info, 0, sizeof(*info));
     unsigned char *used = (unsigned char *)calloc((size_t)E, 1);
-    for (long p = 0; p < (long)T * k; ++p) used[ids[p]] = 1;
+    int32_t *cnt = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (long p = 0; p < (long)T * k; ++p) { used[ids[p]] = 1; cnt[ids[p]] += 1; }
     int nU = 0;
     for (int e = 0; e < E; ++e) nU += used[e];
     if (nU > S) { free(used); return -2; }
@@ -359,7 +362,25 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
  *   by ascending (stamp, index).  The i-th miss of a stage takes its i-th
  *   victim; the victim's old expert is marked not cached; the slot gets the
  *   clock as stamp.
+ *
+ * Policy 2 (LRU with adopt; the prefill preheat of "llama.cpp: fork with multi
+ * gpu acceleration ...", section "Prefill preheat": a long prompt's most-used
+ * experts stay in the cache, in place of cached experts it used less).  Calls
+ * of one stage are planned exactly as LRU.  A call of more than one stage:
+ *   rank = (pick count in this call descending, expert id ascending).
+ *   Misses are taken lowest rank first (count ascending, id descending), so
+ *   that the most-used misses are streamed last; stage 0 as for LRU.
+ *   With m misses left after stage 0, G = ceil(m / S) later stages (as many as
+ *   LRU needs) stream them through C = ceil(m / G) slots: the S - C slots whose
+ *   stage-0 expert ranks highest keep it to the end; the other C slots, in
+ *   ascending index, take the i-th later miss at stage 1 + i / C, slot
+ *   number i mod C among them.
  */
+/* a ranks above b among the call's experts: more picks, then the lower id */
+static int adopt_above(const int32_t *cnt, int a, int b) {
+    return cnt[a] > cnt[b] || (cnt[a] == cnt[b] && a < b);
+}
+
 int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
                  int32_t *gpu_slot, int32_t *stage,
                  int32_t *miss_expert, int32_t *miss_slot, int32_t *miss_evicted,
@@ -372,7 +393,8 @@ int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
     const uint64_t now = st->clock;
 
     unsigned char *used = (unsigned char *)calloc((size_t)E, 1);
-    for (long p = 0; p < (long)T * k; ++p) used[ids[p]] = 1;
+    int32_t *cnt = (int32_t *)calloc((size_t)E, sizeof(int32_t));
+    for (long p = 0; p < (long)T * k; ++p) { used[ids[p]] = 1; cnt[ids[p]] += 1; }
 
     int32_t *U = (int32_t *)malloc(sizeof(int32_t) * E), nU = 0;
     int32_t *M = (int32_t *)malloc(sizeof(int32_t) * E), nM = 0;
@@ -408,6 +430,17 @@ int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
         in_call[s] = 1;
     }
 
+    const int adopt = st->policy == 2 && nU > S;
+    if (adopt) {
+        /* misses lowest rank first (insertion sort) */
+        for (int i = 1; i < nM; ++i) {
+            const int e = M[i];
+            int j = i - 1;
+            while (j >= 0 && adopt_above(cnt, M[j], e)) { M[j + 1] = M[j]; --j; }
+            M[j + 1] = e;
+        }
+    }
+
     int n_stage0_miss = (nU <= S) ? nM : (S - nH);
     int *cand = (int *)malloc(sizeof(int) * S);
     int n_cand = 0;
@@ -430,6 +463,42 @@ int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
         e_stage[e] = 0;
         e_slot[e] = s;
         miss_expert[mi] = e; miss_slot[mi] = s; miss_evicted[mi] = old; miss_stage[mi] = 0;
+    }
+    /* later stages, policy 2: the S - C slots holding the highest-ranked
+     * experts keep them; the others stream the misses left */
+    if (adopt && mi < nM) {
+        const int m = nM - mi;
+        const int G = (m + S - 1) / S, C = (m + G - 1) / G;
+        int *order = (int *)malloc(sizeof(int) * S); /* slots by their expert's rank */
+        for (int s2 = 0; s2 < S; ++s2) order[s2] = s2;
+        for (int i = 1; i < S; ++i) {
+            const int v = order[i];
+            int j = i - 1;
+            while (j >= 0 && adopt_above(cnt, st->slot_expert[v], st->slot_expert[order[j]])) {
+                order[j + 1] = order[j];
+                --j;
+            }
+            order[j + 1] = v;
+        }
+        unsigned char *kept = (unsigned char *)calloc((size_t)S, 1);
+        for (int i = 0; i < S - C; ++i) kept[order[i]] = 1;
+        int nq = 0;
+        for (int s2 = 0; s2 < S; ++s2)
+            if (!kept[s2]) cand[nq++] = s2;
+        for (int i = 0; mi < nM; ++i, ++mi) {
+            const int e = M[mi], s2 = cand[i % C], j = 1 + i / C;
+            const int old = st->slot_expert[s2];
+            if (old >= 0) { st->expert_slot[old] = -1; info->n_evict++; }
+            st->slot_expert[s2] = e;
+            st->expert_slot[e] = s2;
+            st->slot_stamp[s2] = now;
+            e_stage[e] = j;
+            e_slot[e] = s2;
+            miss_expert[mi] = e; miss_slot[mi] = s2; miss_evicted[mi] = old; miss_stage[mi] = j;
+            if (j + 1 > n_stages) n_stages = j + 1;
+        }
+        free(order);
+        free(kept);
     }
     /* later stages */
     for (int j = 1; mi < nM; ++j) {
@@ -458,7 +527,7 @@ int orc_slot_map(orc_lru *st, const int32_t *ids, int T, int k,
         gpu_slot[p] = e_slot[ids[p]];
         stage[p] = e_stage[ids[p]];
     }
-    free(used); free(U); free(M); free(e_stage); free(e_slot); free(was_hit); free(in_call); free(cand);
+    free(used); free(cnt); free(U); free(M); free(e_stage); free(e_slot); free(was_hit); free(in_call); free(cand);
     return 0;
 }
 
