@@ -95,8 +95,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--fill", default="pull", choices=["memcpy", "pull"])
-    ap.add_argument("--policy", default="lru", choices=["lru", "score"],
-                    help="slot replacement: LRU, or the decayed-score admission policy (decode workload)")
+    ap.add_argument("--policy", default="lru", choices=["lru", "score", "adopt"],
+                    help="slot replacement: LRU, the decayed-score admission policy (decode workload), or "
+                         "LRU whose staged calls end holding their most-used experts (adopt)")
     ap.add_argument("--admit-budget", type=int, default=0,
                     help="score policy: admissions per call (0 = no limit)")
     ap.add_argument("--preload-profile", type=int, default=0,
@@ -105,6 +106,9 @@ def parse():
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--tokens", type=int, default=512,
                     help="prefill workload: tokens per batch (one call per layer and batch)")
+    ap.add_argument("--decode-after", type=int, default=0,
+                    help="prefill workload: after the timed batches, decode this many tokens per layer, "
+                         "continuing the last batch's token stream, and report their hit rate")
     ap.add_argument("--gemm-min-tokens", type=int, default=16,
                     help="prefill workload: calls of at least this many tokens take the tensor-core "
                          "grouped GEMM, shorter ones the GEMV kernels (0 = never the GEMM)")
@@ -294,6 +298,8 @@ def run_prefill(args):
         sh = dataclasses.replace(sh, L=min(sh.L, args.layers))
     T = args.tokens
     assert T >= 1 and args.gemm_min_tokens >= 0
+    if args.policy == "score":
+        raise SystemExit("the score policy plans single-stage calls only: not a prefill policy")
     W, K = max(3, args.warmup), args.steps
     torch.cuda.set_device(0)
     eb = sh.expert_bytes
@@ -307,7 +313,8 @@ def run_prefill(args):
     fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
     cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
                          slots_per_layer=sh.S, max_tokens=T, store=store, act_dtype="bf16",
-                         fill_mode=fill, gemm_min_tokens=args.gemm_min_tokens, timeout_us=60_000_000)
+                         fill_mode=fill, gemm_min_tokens=args.gemm_min_tokens, timeout_us=60_000_000,
+                         policy={"lru": moe.MOE_POLICY_LRU, "adopt": moe.MOE_POLICY_ADOPT}[args.policy])
     h2d_gbps = cache.probe_h2d(24)
     fwd = moe.lib().moe_layer_forward
     sh_ = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -339,6 +346,36 @@ def run_prefill(args):
     kt = cache.timing()
     cache.set_timing(False)
     st3 = cache.stats(-1)
+    after = None
+    if args.decode_after:
+        # single tokens after the last batch, continuing each layer's token
+        # stream of that batch (the same trace, longer): the cache as the
+        # prompt left it
+        D, bl = args.decode_after, nb - 1
+        lg2 = np.empty((D, sh.L, 1, sh.E), np.float32)
+        for l in range(sh.L):
+            full = synth.trace(T + D, sh.E, sh.k, sh.zipf, sh.sticky, 0, l, 10000 + bl)
+            lg2[:, l, 0] = synth.logits_from_picks(full[T:], sh.E, 0, l, 10000 + bl, 2)
+        x2 = synth.normal_bf16_bits(D * sh.L * sh.H, 0, synth.PURPOSE_X, 77, D).reshape(D, sh.L, 1, sh.H)
+        lg2_d = torch.from_numpy(lg2).cuda()
+        x2_d = torch.from_numpy(x2.view(np.int16)).cuda().view(torch.bfloat16)
+        o2 = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        sa = cache.stats(-1)
+        e0.record()
+        for t in range(D):
+            for l in range(sh.L):
+                rc = fwd(cache.handle, l, ctypes.c_void_p(lg2_d[t, l].data_ptr()),
+                         ctypes.c_void_p(x2_d[t, l].data_ptr()), 1, ctypes.c_void_p(o2[l].data_ptr()), sh_)
+                if rc != 0:
+                    raise moe.MoeError(rc, f"moe_layer_forward decode {t} layer {l}")
+        e1.record()
+        torch.cuda.synchronize()
+        sb = cache.stats(-1)
+        ph, pm = sb["pick_hits"] - sa["pick_hits"], sb["pick_misses"] - sa["pick_misses"]
+        after = {"decode_tokens": D, "pick_hit_rate": ph / max(1, ph + pm),
+                 "tokens_per_s": D / (e0.elapsed_time(e1) * 1e-3),
+                 "note": "single tokens continuing the last batch's token streams, eager calls"}
     hbm_peak, bf16_peak, peak_kind = measured_peaks()
     d = {k2: st2[k2] - st1[k2] for k2 in ("pick_hits", "pick_misses", "unique_hits", "unique_misses")}
     dk = {k2: st3[k2] - st2[k2] for k2 in ("pick_hits", "pick_misses", "unique_hits", "unique_misses")}
@@ -359,7 +396,7 @@ def run_prefill(args):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": K, "warmup": W,
             "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": prefill_config(sh, args.fill, T, args.gemm_min_tokens),
+            "config": dict(prefill_config(sh, args.fill, T, args.gemm_min_tokens), policy=args.policy),
             "hit_rate": {"pick": d["pick_hits"] / max(1, d["pick_hits"] + d["pick_misses"]),
                          "unique": d["unique_hits"] / max(1, d["unique_hits"] + d["unique_misses"])},
             "roofline": roof,
@@ -369,6 +406,8 @@ def run_prefill(args):
             "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kt.items()
                         if v["launches"]},
             "clocks": clk}
+    if after:
+        line["after_prompt"] = after
     cache.close()
     print(json.dumps(line), flush=True)
 
@@ -415,7 +454,7 @@ def main():
     x_d = torch.from_numpy(x_h).cuda()               # [steps, L, 1, H]
     out_d = torch.empty((sh.L, 1, sh.H), dtype=torch.float32, device="cuda")
     fill = moe.MOE_FILL_PULL if args.fill == "pull" else moe.MOE_FILL_MEMCPY
-    policy = moe.MOE_POLICY_SCORE if args.policy == "score" else moe.MOE_POLICY_LRU
+    policy = {"lru": moe.MOE_POLICY_LRU, "score": moe.MOE_POLICY_SCORE, "adopt": moe.MOE_POLICY_ADOPT}[args.policy]
     cache = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
                          slots_per_layer=sh.S, max_tokens=1, store=store, fill_mode=fill,
                          timeout_us=30_000_000, policy=policy, admit_budget=args.admit_budget)

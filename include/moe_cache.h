@@ -78,9 +78,19 @@ extern "C" {
  *   Needs every call to fit one stage and the decode layer kernel: max_tokens x
  *   top_k <= min(slots_per_layer, 32), max_tokens <= 8, no tensor-core GEMM
  *   (gemm_min_tokens 0 or > max_tokens), and the pull fill or the memcpy fill
- *   with stream memory writes; otherwise init returns MOE_ERR_UNSUPPORTED. */
+ *   with stream memory writes; otherwise init returns MOE_ERR_UNSUPPORTED.
+ * MOE_POLICY_ADOPT ("Prefill preheat": a long prompt's most-used experts stay
+ *   in the cache in place of cached experts it used less): LRU, except for
+ *   calls of more than one stage.  There rank = (picks in the call descending,
+ *   expert id ascending); misses are taken lowest rank first, so the most-used
+ *   ones stream last; stage 0 as LRU; with m misses after stage 0 and
+ *   G = ceil(m / S) later stages (as many as LRU), the S - C slots whose
+ *   stage-0 expert ranks highest (C = ceil(m / G)) keep it, and the other C
+ *   slots, in ascending index, take the later misses in turn.  Same uploads,
+ *   stages and outputs as LRU; the call ends holding higher-ranked experts. */
 #define MOE_POLICY_LRU 0
 #define MOE_POLICY_SCORE 1
+#define MOE_POLICY_ADOPT 2
 
 /* How misses reach their slots. */
 #define MOE_FILL_MEMCPY 0  /* cudaMemcpyAsync per missed block on a side stream into a
@@ -108,8 +118,9 @@ typedef struct {
                                 on GB300 (hidden 2816, FFN 704, top-8, 32
                                 slots): GEMV ahead up to 8 tokens, even at
                                 12-16, GEMM ahead from 24; 16 is the switch   */
-    int32_t policy;          /* slot replacement: MOE_POLICY_LRU (0) or
-                                MOE_POLICY_SCORE (1, see below)                   */
+    int32_t policy;          /* slot replacement: MOE_POLICY_LRU (0),
+                                MOE_POLICY_SCORE (1) or MOE_POLICY_ADOPT (2),
+                                see above                                         */
     int32_t admit_budget;    /* MOE_POLICY_SCORE: admissions per call, 0 = no limit */
     int32_t reserved;        /* must be 0                                          */
     int64_t timeout_us;      /* limit of every bounded host wait, > 0; the decode

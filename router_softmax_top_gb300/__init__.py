@@ -32,6 +32,7 @@ MOE_INJECT_DECODE_WAIT = 1
 
 MOE_POLICY_LRU = 0
 MOE_POLICY_SCORE = 1
+MOE_POLICY_ADOPT = 2
 
 # every symbol include/moe_cache.h declares
 EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_stats",

@@ -36,11 +36,14 @@ struct PlanHdr {
   int32_t hit_units;  // GEMV units of the stage-0 hits: [0, hit_units)
   int32_t hit_gunits; // GEMM units of the stage-0 hits: [0, hit_gunits)
   uint32_t epoch;     // call number of the handle (1, 2, ...): tags the decode layer kernel's outputs
-  int32_t pad[3];
+  int32_t stage_cap;  // misses per stage after stage 0 (the last may hold fewer): S, or fewer
+                      // under the adopt policy
+  int32_t pad[2];
 };
 
 // A work item = one distinct expert of the call.  Items are ordered: stage-0
-// hits (ascending expert), then misses (ascending expert, which is stage order).
+// hits (ascending expert), then misses in stage order (ascending expert; under
+// the adopt policy a staged call's misses lowest rank first).
 struct WorkItem {
   int32_t expert;
   int32_t slot;

@@ -280,10 +280,15 @@ __global__ void __launch_bounds__(kThreads) fill_kernel(FillJob jb) {
   const RepackArgs &a = jb.a;
   const PlanHdr *h = a.hdr;
   if (h->error || a.stage >= h->n_stages) return;
-  const int n0 = h->n_stage0_miss, nM = h->n_miss, S = jb.S;
+  // stage 0 holds n0 misses, every later stage stage_cap (<= S; the last may hold fewer)
+  const int n0 = h->n_stage0_miss, nM = h->n_miss, C = h->stage_cap;
   int m_lo, m_hi;
   if (a.stage == 0) { m_lo = 0; m_hi = n0; }
-  else { m_lo = n0 + (a.stage - 1) * S; m_hi = min(nM, n0 + a.stage * S); }
+  else {
+    if (C < 1 || C > jb.S) return;
+    m_lo = n0 + (a.stage - 1) * C;
+    m_hi = min(nM, n0 + a.stage * C);
+  }
   const int tg = a.lay.gate.rows / 32, td = a.lay.down.rows / 32;
   const int tiles = 2 * tg + td;
   const int n_work = (m_hi - m_lo) * tiles;

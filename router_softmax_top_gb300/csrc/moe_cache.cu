@@ -54,6 +54,7 @@ struct moe_cache {
   // persistent device state
   uint8_t *d_slots = nullptr;
   uint8_t *d_stage_buf = nullptr;  // 2 x S blocks (slot layout): stages >= 1 of staged calls
+  std::vector<int> fin_src;         // [S] after a staged call: the stage holding each slot's final block
   cudaEvent_t ev_fin = nullptr;
   int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
   uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
@@ -280,7 +281,8 @@ int check_config(const moe_cache_config *g) {
   if (g->act_dtype != 0 && g->act_dtype != 1) return MOE_ERR_INVALID_ARG;
   if (g->fill_mode != MOE_FILL_MEMCPY && g->fill_mode != MOE_FILL_PULL) return MOE_ERR_INVALID_ARG;
   if (g->gemm_min_tokens < 0 || g->reserved != 0 || g->timeout_us <= 0) return MOE_ERR_INVALID_ARG;
-  if ((g->policy != MOE_POLICY_LRU && g->policy != MOE_POLICY_SCORE) || g->admit_budget < 0)
+  if ((g->policy != MOE_POLICY_LRU && g->policy != MOE_POLICY_SCORE && g->policy != MOE_POLICY_ADOPT) ||
+      g->admit_budget < 0)
     return MOE_ERR_INVALID_ARG;
   if (g->hidden < 64 || g->hidden % 64 || g->ffn < 64 || g->ffn % 64) return MOE_ERR_UNSUPPORTED;
   if (g->hidden > 16384 || g->ffn > 16384) return MOE_ERR_UNSUPPORTED;
@@ -374,8 +376,10 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   // staged calls (more distinct experts than slots) are possible: stages >= 1
   // alternate between two stage buffers, so that a stage's fill overlaps the
   // previous stage's compute
-  if (ok && std::min(E, cfg->max_tokens * cfg->top_k) > S)
+  if (ok && std::min(E, cfg->max_tokens * cfg->top_k) > S) {
     ok = cudaMalloc(&c->d_stage_buf, (size_t)2 * S * c->lay.stride) == cudaSuccess;
+    c->fin_src.assign(S, 0);
+  }
   ok = ok && dalloc(&c->d_slot_expert, (size_t)L * S) == cudaSuccess;
   ok = ok && dalloc(&c->d_expert_slot, (size_t)L * E) == cudaSuccess;
   ok = ok && dalloc(&c->d_slot_stamp, (size_t)L * S) == cudaSuccess;
@@ -662,22 +666,31 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     return MOE_OK;
   };
   // After a staged call: the blocks the final state maps live in the stage
-  // buffers for stages >= 1; copy them into their slots (slots [0, mL) from
-  // the last stage, [mL, S) from the one before when that one is >= 1), once
-  // stage 0's compute no longer reads the slots.  The main stream waits.
-  auto finalize_stages = [&](int n_st, int n0, int nM) -> int {
-    if (n_st < 2) return MOE_OK;
-    const int jL = n_st - 1, mL = std::min(nM, n0 + jL * S) - (n0 + (jL - 1) * S);
+  // buffers for stages >= 1.  Each slot's last miss (the miss list is in stage
+  // order) names the stage whose buffer holds its final block; runs of
+  // consecutive slots from the same buffer are copied into the layer's slots
+  // in one piece, once stage 0's compute no longer reads the slots.  The main
+  // stream waits.
+  auto finalize_stages = [&](int n_st, int nM) -> int {
+    if (n_st < 2 || !c->d_stage_buf) return MOE_OK;
+    std::vector<int> &fin_src = c->fin_src;  // sized S at init
+    std::fill(fin_src.begin(), fin_src.end(), 0);
+    for (int i = 0; i < nM; ++i) {
+      const MissItem m = c->h_mail_miss[i];
+      if (m.slot < 0 || m.slot >= S || m.stage < 0 || m.stage >= n_st) return MOE_ERR_CUDA;
+      fin_src[m.slot] = m.stage;
+    }
     if (cudaStreamWaitEvent(c->side, c->ev_done[0], 0) != cudaSuccess) return MOE_ERR_CUDA;
     const size_t stride = c->lay.stride;
-    if (mL > 0 &&
-        cudaMemcpyAsync(layer_slots, stage_base(jL), (size_t)mL * stride, cudaMemcpyDeviceToDevice, c->side) !=
-            cudaSuccess)
-      return MOE_ERR_CUDA;
-    if (jL - 1 >= 1 && mL < S &&
-        cudaMemcpyAsync(layer_slots + (size_t)mL * stride, stage_base(jL - 1) + (size_t)mL * stride,
-                        (size_t)(S - mL) * stride, cudaMemcpyDeviceToDevice, c->side) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    for (int s0 = 0; s0 < S;) {
+      int s1 = s0 + 1;
+      while (s1 < S && fin_src[s1] == fin_src[s0]) ++s1;
+      if (fin_src[s0] >= 1 &&
+          cudaMemcpyAsync(layer_slots + (size_t)s0 * stride, stage_base(fin_src[s0]) + (size_t)s0 * stride,
+                          (size_t)(s1 - s0) * stride, cudaMemcpyDeviceToDevice, c->side) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      s0 = s1;
+    }
     if (cudaEventRecord(c->ev_fin, c->side) != cudaSuccess || cudaStreamWaitEvent(st, c->ev_fin, 0) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
@@ -805,11 +818,12 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     if (rc != MOE_OK) return poison(c, rc);
     const PlanHdr hdr = c->h_mail->hdr;
     if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
-    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss;
-    if (n_st < 1 || n_st > c->maxStages - 1) return poison(c, MOE_ERR_CUDA);
+    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss, cap = hdr.stage_cap;
+    if (n_st < 1 || n_st > c->maxStages - 1 || cap < 1 || cap > S || n0 < 0 || n0 > nM || nM > c->maxU)
+      return poison(c, MOE_ERR_CUDA);
     for (int j = 0; j < n_st; ++j) {
-      const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
-      const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
+      const int mlo = j == 0 ? 0 : n0 + (j - 1) * cap;
+      const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * cap);
       if (mhi > mlo) {
         rc = fill_stage(j, mhi - mlo, c->ev_plan, stage_free(j), mlo, true);
         if (rc != MOE_OK) return poison(c, rc);
@@ -827,7 +841,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
                  launch_gemm_down(fj, c->h16_maps, rm, slot0, c->d_gunits, c->d_gunit_begin, 2, j, sg, st));
       if (cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
     }
-    rc = finalize_stages(n_st, n0, nM);
+    rc = finalize_stages(n_st, nM);
     if (rc != MOE_OK) return poison(c, rc);
     MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
   } else {
@@ -836,8 +850,9 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     if (rc != MOE_OK) return poison(c, rc);
     const PlanHdr hdr = c->h_mail->hdr;
     if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
-    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss;
-    if (n_st < 1 || n_st > c->maxStages - 1) return poison(c, MOE_ERR_CUDA);
+    const int n_st = hdr.n_stages, n0 = hdr.n_stage0_miss, nM = hdr.n_miss, cap = hdr.stage_cap;
+    if (n_st < 1 || n_st > c->maxStages - 1 || cap < 1 || cap > S || n0 < 0 || n0 > nM || nM > c->maxU)
+      return poison(c, MOE_ERR_CUDA);
     if (n_st == 1 && fused_ok) {
       if (nM > 0) {
         rc = fused_stage0(c->ev_plan, nM, true);
@@ -849,8 +864,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
     } else {
       for (int j = 0; j < n_st; ++j) {
-        const int mlo = j == 0 ? 0 : n0 + (j - 1) * S;
-        const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * S);
+        const int mlo = j == 0 ? 0 : n0 + (j - 1) * cap;
+        const int mhi = j == 0 ? n0 : std::min(nM, n0 + j * cap);
         if (mhi > mlo) {
           rc = fill_stage(j, mhi - mlo, c->ev_plan, stage_free(j), mlo, true);
           if (rc != MOE_OK) return poison(c, rc);
@@ -868,7 +883,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
           if (cudaEventRecord(c->ev_done[j], st) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
         }
       }
-      rc = finalize_stages(n_st, n0, nM);
+      rc = finalize_stages(n_st, nM);
       if (rc != MOE_OK) return poison(c, rc);
       if (n_st > 1 || !dc_ok)
         MOE_LAUNCH(K_COMBINE, launch_combine(c->d_y, c->d_w, c->d_hdr, T, k, g.hidden, d_out, st));
@@ -1031,6 +1046,7 @@ MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_s
       h.n_stages = 1;
       h.n_stage0_miss = n;
       h.n_miss = n;
+      h.stage_cap = S;
       for (int i = 0; i < n; ++i) items[i] = MissItem{chosen[l][lo + i], lo + i, -1, 0};
       RepackArgs ra;
       ra.slots = c->d_slots + (size_t)l * S * c->lay.stride;

@@ -177,9 +177,11 @@ __device__ void write_error(const PlanArgs &a) {
   }
 }
 
-__device__ __forceinline__ MissItem miss_record(int i, int n0, int S, const int *M,
-                                                const int *victim, const int *se0,
-                                                const int *occ0) {
+// Miss i of the call: stage 0 into its victim; after that C misses per stage,
+// the r-th later miss into later-stage slot qslot[r % C].
+__device__ __forceinline__ MissItem miss_record(int i, int n0, int C, const int *M,
+                                                const int *victim, const int *qslot,
+                                                const int *se0, const int *occ0) {
   MissItem m;
   m.expert = M[i];
   if (i < n0) {
@@ -188,9 +190,9 @@ __device__ __forceinline__ MissItem miss_record(int i, int n0, int S, const int 
     m.evicted = se0[m.slot];
   } else {
     const int r = i - n0;
-    m.stage = 1 + r / S;
-    m.slot = r % S;
-    m.evicted = (m.stage == 1) ? occ0[m.slot] : M[i - S];
+    m.stage = 1 + r / C;
+    m.slot = qslot[r % C];
+    m.evicted = (m.stage == 1) ? occ0[m.slot] : M[i - C];
   }
   return m;
 }
@@ -214,6 +216,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   int *cnt = take(E), *es0 = take(E), *code = take(E), *e_slot = take(E), *e_stage = take(E);
   int *M = take(E), *new_es = take(E), *item_of = take(E), *gitm = take(E + 1);
   int *se0 = take(S), *vpos = take(S), *occ0 = take(S), *touched = take(S), *victim = take(S);
+  int *qpos = take(S), *qslot = take(S);  // later-stage slots: position of a slot, slot of a position
   int *wcnt = take(NW * E);
   int *ws = take(NW + 2);
   int *scal = take(8);  // 0 bad, 1 pick hits, 2 evictions
@@ -276,11 +279,17 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   const int nH = tot & 0xFFFF, nM = tot >> 16, nU = nH + nM;
   const int n0 = (nU <= S) ? nM : (S - nH);
   const int n_later = nM - n0;
-  const int n_stages = n_later > 0 ? 1 + (n_later + S - 1) / S : 1;
+  // adopt (policy 2), a call of more than one stage: misses lowest rank first
+  // (rank: picks in this call descending, then expert id ascending), and the
+  // later stages stream through C slots, as many stages as LRU takes
+  const bool adopt = a.policy == 2 && n_later > 0;
+  const int G = (n_later + S - 1) / S;
+  const int C = adopt ? (n_later + G - 1) / G : S;
+  const int n_stages = n_later > 0 ? 1 + (n_later + C - 1) / C : 1;
 
-  // ---- D. hits keep their slot; misses in ascending order; stage-0 victim
-  // ranks: empty slots (by index) first, then slots whose expert the call does
-  // not pick, by (stamp, index)
+  // ---- D. hits keep their slot; misses in ascending order (adopt: lowest
+  // rank first); stage-0 victim ranks: empty slots (by index) first, then
+  // slots whose expert the call does not pick, by (stamp, index)
   for (int e = tid; e < E; e += NT) {
     if (cnt[e] == 0) { item_of[e] = -1; continue; }
     const int s0 = es0[e];
@@ -290,7 +299,12 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
       touched[s0] = 1;
       item_of[e] = code[e] & 0xFFFF;
     } else {
-      const int mr = code[e] >> 16;
+      int mr = code[e] >> 16;
+      if (adopt) {
+        mr = 0;
+        for (int f = 0; f < E; ++f)
+          mr += cnt[f] > 0 && es0[f] < 0 && (cnt[f] < cnt[e] || (cnt[f] == cnt[e] && f > e));
+      }
       M[mr] = e;
       item_of[e] = nH + mr;
     }
@@ -324,10 +338,41 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   }
   __syncthreads();
 
+  // ---- E2. slots of the later stages: LRU all S, slot i at position i; adopt
+  // keeps the S - C slots whose stage-0 expert ranks highest (after stage 0
+  // every slot holds an expert of the call), the others in ascending index
+  if (adopt) {
+    for (int i = tid; i < S; i += NT) {
+      const int ei = occ0[i];
+      int above = ei < 0 ? S : 0;  // (an empty slot cannot occur here; it would rank last)
+      for (int j2 = 0; j2 < S && ei >= 0; ++j2) {
+        const int ej = occ0[j2];
+        above += ej >= 0 && (cnt[ej] > cnt[ei] || (cnt[ej] == cnt[ei] && ej < ei));
+      }
+      vpos[i] = above < S - C ? 1 : 0;  // kept (vpos is free after E)
+    }
+    __syncthreads();
+    for (int i = tid; i < S; i += NT) {
+      int q = -1;
+      if (!vpos[i]) {
+        q = 0;
+        for (int j2 = 0; j2 < i; ++j2) q += vpos[j2] ? 0 : 1;
+        qslot[q] = i;
+      }
+      qpos[i] = q;
+    }
+  } else {
+    for (int i = tid; i < S; i += NT) {
+      qpos[i] = i;
+      qslot[i] = i;
+    }
+  }
+  __syncthreads();
+
   // ---- F. miss list, final slot contents and stamps
   int my_evict = 0;
   for (int i = tid; i < nM; i += NT) {
-    const MissItem m = miss_record(i, n0, S, M, victim, se0, occ0);
+    const MissItem m = miss_record(i, n0, C, M, victim, qslot, se0, occ0);
     e_slot[m.expert] = m.slot;
     e_stage[m.expert] = m.stage;
     my_evict += m.evicted >= 0;
@@ -338,7 +383,8 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   if (lane == 0 && my_evict) atomicAdd(&scal[2], my_evict);
   for (int i = tid; i < S; i += NT) {
     int f = occ0[i];
-    if (n_later > i) f = M[n0 + i + S * ((n_later - 1 - i) / S)];
+    const int q = qpos[i];
+    if (q >= 0 && n_later > q) f = M[n0 + q + C * ((n_later - 1 - q) / C)];
     a.slot_expert[i] = f;
     if (touched[i] || n_later > 0) a.slot_stamp[i] = now;
     if (f >= 0) new_es[f] = i;
@@ -403,7 +449,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     }
   }
   for (int j = tid; j <= n_stages; j += NT) {
-    const int first_item = (j == 0) ? 0 : min(nU, nH + n0 + (j - 1) * S);
+    const int first_item = (j == 0) ? 0 : min(nU, nH + n0 + (j - 1) * C);
     a.unit_begin[j] = (int)(itm[first_item] >> 32);
     a.gunit_begin[j] = gitm[first_item];
   }
@@ -466,6 +512,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     h.hit_units = hit_units;
     h.hit_gunits = hit_gunits;
     h.epoch = epoch;
+    h.stage_cap = C;
     *a.epoch = epoch;
     *a.hdr = h;
     *a.clock = now;
@@ -485,10 +532,10 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     int32_t *mub = reinterpret_cast<int32_t *>(a.mailbox + 1);
     MissItem *mm = reinterpret_cast<MissItem *>(mub + a.mailbox_stage_cap);
     for (int j = tid; j <= n_stages; j += NT) {
-      const int first_item = (j == 0) ? 0 : min(nU, nH + n0 + (j - 1) * S);
+      const int first_item = (j == 0) ? 0 : min(nU, nH + n0 + (j - 1) * C);
       mub[j] = (int)(itm[first_item] >> 32);
     }
-    for (int i = tid; i < nM; i += NT) mm[i] = miss_record(i, n0, S, M, victim, se0, occ0);
+    for (int i = tid; i < nM; i += NT) mm[i] = miss_record(i, n0, C, M, victim, qslot, se0, occ0);
     __threadfence_system();
     __syncthreads();
     if (tid == 0) {
@@ -808,6 +855,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     h.hit_units = tot_hit_units;
     h.hit_gunits = nH;
     h.epoch = epoch;
+    h.stage_cap = S;
     *a.epoch = epoch;
     *a.hdr = h;
     *a.clock = now;
@@ -849,7 +897,7 @@ size_t plan_smem_bytes(int E, int S) {
   auto r4 = [](size_t n) { return 4 * ((n + 3) / 4 * 4); };
   size_t b = r8(S) + r8(E + 1) + r8(NW + 2);
   b += 8 * r4(E) + r4(E + 1);
-  b += 5 * r4(S);
+  b += 7 * r4(S);
   b += r4((size_t)NW * E) + r4(NW + 2) + r4(8);
   return b + 64;
 }
