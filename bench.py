@@ -41,21 +41,65 @@ PROFILE_STREAM = 777   # token stream that the warm-start profile is counted ove
 _HOST_MAPS = []
 
 
-def host_store(nbytes: int):
+def host_store(nbytes: int, node: int = -1, strict: bool = False):
     """The expert store in ordinary anonymous memory (transparent huge pages
     requested, 512 MB-aligned), as a torch uint8 tensor; the library pins and
     maps it with cudaHostRegister.  On this Grace host such memory reads over
     the host link faster and more steadily than a cudaHostAlloc buffer for the
-    scattered expert blocks of the workload."""
+    scattered expert blocks of the workload.  node >= 0: its pages are taken
+    from that NUMA node (bound before the first touch; if the binding is
+    refused, first touch decides, unless strict)."""
     import torch
     align = 512 << 20
     mm = mmap.mmap(-1, nbytes + align, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
     if hasattr(mmap, "MADV_HUGEPAGE"):
         mm.madvise(mmap.MADV_HUGEPAGE)
     base = ctypes.addressof(ctypes.c_char.from_buffer(mm))
-    arr = np.frombuffer(mm, dtype=np.uint8, count=nbytes, offset=(-base) % align)
+    off = (-base) % align
+    if node >= 0 and not bind_to_node(base + off, nbytes, node) and strict:
+        raise SystemExit(f"could not bind the host store to NUMA node {node}")
+    arr = np.frombuffer(mm, dtype=np.uint8, count=nbytes, offset=off)
     _HOST_MAPS.append(mm)
     return torch.from_numpy(arr)
+
+
+def bind_to_node(addr: int, length: int, node: int) -> bool:
+    """mbind(addr, length, MPOL_BIND, {node}): pages of the range not yet
+    touched come from NUMA node `node` (a policy of this process's own
+    mapping; nothing else changes)."""
+    import platform
+    nr = {"aarch64": 235, "x86_64": 237}.get(platform.machine())
+    if nr is None or not 0 <= node < 1024:
+        return False
+    libc = ctypes.CDLL(None, use_errno=True)
+    mask = (ctypes.c_ulong * 16)()
+    mask[node // 64] = 1 << (node % 64)
+    MPOL_BIND = 2
+    r = libc.syscall(ctypes.c_long(nr), ctypes.c_void_p(addr), ctypes.c_ulong(length), ctypes.c_int(MPOL_BIND),
+                     mask, ctypes.c_ulong(16 * 64), ctypes.c_uint(0))
+    return r == 0
+
+
+def gpu_numa_node(dev: int = 0) -> int:
+    """NUMA node of the GPU's PCI function (sysfs), or -1 when unknown."""
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/numa_node" % (p.pci_domain_id, p.pci_bus_id,
+                                                                     p.pci_device_id)
+        with open(path) as f:
+            return int(f.read().strip())
+    except (AttributeError, OSError, ValueError):
+        return -1
+
+
+def store_node(args, dev: int = 0) -> int:
+    """The NUMA node the host store is bound to (-1: not bound)."""
+    if args.store_node == "none":
+        return -1
+    if args.store_node == "auto":
+        return gpu_numa_node(dev)
+    return int(args.store_node)
 
 
 def host_store_numa(t):
@@ -103,6 +147,9 @@ def parse():
     ap.add_argument("--preload-profile", type=int, default=0,
                     help="warm start: before the first step, preload each layer's most-used experts, "
                          "counted over this many tokens of another token stream with the same routing")
+    ap.add_argument("--store-node", default="auto",
+                    help="NUMA node of the host store's pages: auto (the GPU's node, from sysfs), "
+                         "none (first touch), or a node number")
     ap.add_argument("--workload", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--tokens", type=int, default=512,
                     help="prefill workload: tokens per batch (one call per layer and batch)")
@@ -303,7 +350,8 @@ def run_prefill(args):
     W, K = max(3, args.warmup), args.steps
     torch.cuda.set_device(0)
     eb = sh.expert_bytes
-    store = host_store(sh.L * sh.E * eb)
+    node = store_node(args, 0)
+    store = host_store(sh.L * sh.E * eb, node, strict=args.store_node not in ("auto", "none"))
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
     nb = W + 2 * K
     _, logits_h, x_h = synth.batch_inputs(sh, nb, T, seed=0, act="bf16")
@@ -405,7 +453,7 @@ def run_prefill(args):
                               "tflop_per_batch": flops / K / 1e12},
             "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 3)} for k2, v in kt.items()
                         if v["launches"]},
-            "clocks": clk}
+            "clocks": clk, "host_store_node": node, "host_store_numa_pages": host_store_numa(store)}
     if after:
         line["after_prompt"] = after
     cache.close()
@@ -445,7 +493,8 @@ def main():
     G0 = 2                        # graph warm-up steps (capture and first replays)
     nsteps = max(W + G0 + 3 * K, args.cpu_sample_steps)  # (the CPU baseline's sample too)
     eb = sh.expert_bytes
-    store = host_store(sh.L * sh.E * eb)
+    node = store_node(args, local)
+    store = host_store(sh.L * sh.E * eb, node, strict=args.store_node not in ("auto", "none"))
     synth.fill_store(store.data_ptr(), sh.L, sh.E, sh.H, sh.F, 0, args.threads)
     store_huge_kb = huge_page_kb()
     store_numa = host_store_numa(store)
@@ -713,6 +762,7 @@ def main():
         "host_store_huge_fraction": (None if store_huge_kb is None
                                      else min(1.0, store_huge_kb * 1024 / sh.store_bytes)),
         "host_store_numa_pages": store_numa,
+        "host_store_node": node,
         "clocks": clk,
         "e2e": e2e,
         "setup_s": setup_s,
