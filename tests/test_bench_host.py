@@ -1,0 +1,41 @@
+"""Host-side logic of bench.py (CPU only): the host store's NUMA binding and the
+option defaults the timed runs rely on."""
+import ctypes
+import mmap
+import sys
+
+import pytest
+
+import bench
+
+
+def test_store_bound_to_node_0_lands_there():
+    t = bench.host_store(64 << 20, node=0, strict=True)
+    t.numpy()[:] = 1                       # first touch after the binding
+    pages = bench.host_store_numa(t)
+    if pages is None:
+        pytest.skip("no /proc/self/numa_maps")
+    assert set(pages) == {"N0"} and pages["N0"] > 0
+
+
+def test_binding_to_an_absent_node_is_refused():
+    mm = mmap.mmap(-1, 1 << 21, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    base = ctypes.addressof(ctypes.c_char.from_buffer(mm))
+    assert not bench.bind_to_node(base, 1 << 21, 1000)
+    assert not bench.bind_to_node(base, 1 << 21, -1)
+    with pytest.raises(SystemExit):
+        bench.host_store(1 << 21, node=1000, strict=True)
+    bench.host_store(1 << 21, node=1000, strict=False)   # auto mode: first touch instead
+
+
+def test_defaults(monkeypatch):
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
+    assert (a.gpus, a.impl, a.workload, a.fill, a.policy) == (1, "ours", "decode", "pull", "lru")
+    assert a.warmup >= 3 and a.steps >= 1
+    assert a.store_node == "auto" and a.gemm_min_tokens == 16 and a.tokens == 512
+    assert a.preload_profile == 0 and a.decode_after == 0
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--store-node", "none"])
+    assert bench.store_node(bench.parse()) == -1
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--store-node", "3"])
+    assert bench.store_node(bench.parse()) == 3
