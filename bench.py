@@ -147,6 +147,9 @@ def parse():
     ap.add_argument("--preload-profile", type=int, default=0,
                     help="warm start: before the first step, preload each layer's most-used experts, "
                          "counted over this many tokens of another token stream with the same routing")
+    ap.add_argument("--slots", type=int, default=0,
+                    help="decode workload: slots per layer instead of 32 (up to the 128 experts: "
+                         "every expert resident once warm)")
     ap.add_argument("--store-node", default="auto",
                     help="NUMA node of the host store's pages: auto (the GPU's node, from sysfs), "
                          "none (first touch), or a node number")
@@ -487,6 +490,9 @@ def main():
     if args.layers:
         import dataclasses
         sh = dataclasses.replace(sh, L=min(sh.L, args.layers))
+    if args.slots:
+        import dataclasses
+        sh = dataclasses.replace(sh, S=min(sh.E, args.slots))
     W, K = args.warmup, args.steps
     assert W >= 3 and K >= 1
     t_setup = time.time()
