@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             L.orc_lru_free.argtypes = [vp]
             L.orc_lru_get.argtypes = [vp, vp, vp, vp, vp]
             L.orc_lru_set_policy.argtypes = [vp, i32, i32]
+            L.orc_lru_set_sticky.argtypes = [vp, i32]
+            L.orc_cache_set_sticky.argtypes = [vp, i32]
             L.orc_lru_scores.argtypes = [vp, vp]
             L.orc_slot_map.restype = i32
             L.orc_slot_map.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, ctypes.POINTER(PlanInfo)]
@@ -129,12 +131,14 @@ def router(logits: np.ndarray, k: int, weight_mode: int = 0):
 class LRU:
     """One layer's slot-map state (S slots, E experts)."""
 
-    def __init__(self, S: int, E: int, policy: int = POLICY_LRU, budget: int = 0):
+    def __init__(self, S: int, E: int, policy: int = POLICY_LRU, budget: int = 0, sticky: int = 0):
         self.S, self.E = S, E
         self._h = lib().orc_lru_new(S, E)
         self._own = True
         if policy != POLICY_LRU:
             lib().orc_lru_set_policy(self._h, policy, budget)
+        if sticky:
+            lib().orc_lru_set_sticky(self._h, sticky)
 
     @classmethod
     def _borrow(cls, handle, S, E):
@@ -200,7 +204,7 @@ class Cache:
     canonical Q4_0 expert blocks, [layer][expert] with the given strides."""
 
     def __init__(self, L, E, k, H, F, S, store, weight_mode=0, layer_stride=None,
-                 expert_stride=None, threads=0, policy=POLICY_LRU, admit_budget=0):
+                 expert_stride=None, threads=0, policy=POLICY_LRU, admit_budget=0, sticky=0):
         self.L, self.E, self.k, self.H, self.F, self.S = L, E, k, H, F, S
         eb = 3 * F * H // 32 * 18
         self.expert_stride = eb if expert_stride is None else expert_stride
@@ -214,6 +218,8 @@ class Cache:
         self._h = lib().orc_cache_new(L, E, k, H, F, S, weight_mode, ctypes.c_void_p(addr),
                                       self.layer_stride, self.expert_stride, threads, policy,
                                       admit_budget)
+        if sticky:
+            lib().orc_cache_set_sticky(self._h, sticky)
 
     def __del__(self):
         if getattr(self, "_h", None):

@@ -152,6 +152,8 @@ typedef struct {
                               2: LRU, staged calls keep their most-used experts */
     int budget;            /* policy 1: admissions per call, 0 = unlimited     */
     float *score;          /* [E]  policy 1: decayed usage per expert (fp32)   */
+    int sticky;            /* policy 1: per mille of the slots, highest scores
+                              first, that a call may not evict                */
 } orc_lru;
 
 orc_lru *orc_lru_new(int S, int E) {
@@ -176,6 +178,9 @@ void orc_lru_set_policy(orc_lru *st, int policy, int budget) {
     st->policy = policy;
     st->budget = budget;
 }
+
+/* Sticky share of policy 1, per mille of the slots (0 = none). */
+void orc_lru_set_sticky(orc_lru *st, int permille) { st->sticky = permille; }
 
 /* Copy of the decayed scores [E] (policy 1, fp32). */
 void orc_lru_scores(const orc_lru *st, float *out) { memcpy(out, st->score, sizeof(float) * st->E); }
@@ -237,6 +242,10 @@ static void sort_victims(const orc_lru *st, int *v, int n) {
  *   index ascending), if its own score is strictly higher; otherwise it is
  *   bypassed (slot -1, nothing evicted).  Every admission counts against the
  *   budget.  Miss list in ascending expert order, all in stage 0.
+ *   Sticky share (Fork A's option to never evict the most-used share of each
+ *   layer's slots): once the call's scores are updated, the
+ *   floor(sticky x S / 1000) occupied slots with the highest scores (ties to
+ *   the lower index) are not evictable in this call.
  */
 static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t *gpu_slot, int32_t *stage,
                           int32_t *miss_expert, int32_t *miss_slot, int32_t *miss_evicted, int32_t *miss_stage,
@@ -248,7 +257,7 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
     for (long p = 0; p < (long)T * k; ++p) { used[ids[p]] = 1; cnt[ids[p]] += 1; }
     int nU = 0;
     for (int e = 0; e < E; ++e) nU += used[e];
-    if (nU > S) { free(used); return -2; }
+    if (nU > S) { free(used); free(cnt); return -2; }
     st->clock += 1;
     const uint64_t now = st->clock;
     for (int t = 0; t < T; ++t) {
@@ -281,13 +290,26 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
         if (was_hit[ids[p]]) info->pick_hits++;
         else info->pick_misses++;
     }
-    /* empty slots ascending; slots of experts not picked, by (score, index) */
+    /* sticky: the n_sticky occupied slots of highest score are kept */
+    const int n_sticky = (int)((int64_t)st->sticky * S / 1000);
+    unsigned char *keep = (unsigned char *)calloc((size_t)S, 1);
+    for (int s = 0; s < S; ++s) {
+        const int e = st->slot_expert[s];
+        if (e < 0) continue;
+        int above = 0;
+        for (int s2 = 0; s2 < S; ++s2) {
+            const int e2 = st->slot_expert[s2];
+            if (e2 >= 0 && (st->score[e2] > st->score[e] || (st->score[e2] == st->score[e] && s2 < s))) ++above;
+        }
+        keep[s] = above < n_sticky;
+    }
+    /* empty slots ascending; slots of experts not picked and not kept, by (score, index) */
     int *fr = (int *)malloc(sizeof(int) * S), nf = 0;
     int *ev = (int *)malloc(sizeof(int) * S), nv = 0;
     for (int s = 0; s < S; ++s) {
         const int e = st->slot_expert[s];
         if (e < 0) fr[nf++] = s;
-        else if (!used[e]) ev[nv++] = s;
+        else if (!used[e] && !keep[s]) ev[nv++] = s;
     }
     for (int i = 1; i < nv; ++i) {         /* insertion sort by (score asc, index asc) */
         int x = ev[i], j = i - 1;
@@ -341,7 +363,8 @@ static int slot_map_score(orc_lru *st, const int32_t *ids, int T, int k, int32_t
         gpu_slot[p] = e_slot[ids[p]];
         stage[p] = 0;
     }
-    free(used); free(M); free(e_slot); free(d_old); free(was_hit); free(fr); free(ev); free(order);
+    free(used); free(cnt); free(keep); free(M); free(e_slot); free(d_old); free(was_hit); free(fr); free(ev);
+    free(order);
     return 0;
 }
 
@@ -625,6 +648,11 @@ orc_lru *orc_cache_lru(orc_cache *c, int layer) { return c->lru[layer]; }
  * by (count descending, id ascending), the first S of them in slots 0, 1, ...;
  * every other slot empty; stamps 0; the clock, scores and counters unchanged.
  */
+/* Sticky share of policy 1 on every layer, per mille of the slots. */
+void orc_cache_set_sticky(orc_cache *c, int permille) {
+    for (int l = 0; l < c->L; ++l) orc_lru_set_sticky(c->lru[l], permille);
+}
+
 void orc_cache_preload(orc_cache *c, const uint32_t *counts) {
     for (int l = 0; l < c->L; ++l) {
         orc_lru *st = c->lru[l];

@@ -15,7 +15,11 @@ slot is promoted, up to a budget of copies; every miss is still computed):
     index first) if there is one, else the weakest slot whose expert the call
     does not pick (score ascending, then lowest index) if its own score is
     strictly higher; otherwise it is bypassed (no slot, nothing evicted);
-  * every admission uses one unit of the budget.
+  * every admission uses one unit of the budget;
+  * sticky share (per mille, "never evict the most-used share of each layer's
+    slots"): after the scores of the call are updated, the floor(share x S /
+    1000) occupied slots with the highest scores (ties: lower index) are not
+    evictable in this call.
 
 Plain lists and dictionaries.
 """
@@ -23,8 +27,8 @@ import numpy as np
 
 
 class BruteScore:
-    def __init__(self, S, E, budget=0):
-        self.S, self.E, self.budget = S, E, budget
+    def __init__(self, S, E, budget=0, sticky=0):
+        self.S, self.E, self.budget, self.sticky = S, E, budget, sticky
         self.holder = [None] * S
         self.used_at = [0] * S
         self.tick = 0
@@ -46,7 +50,11 @@ class BruteScore:
         for e in hits:
             self.used_at[where[e]] = now
         empty = [s for s in range(S) if self.holder[s] is None]
-        weak = [s for s in range(S) if self.holder[s] is not None and self.holder[s] not in wanted]
+        occupied = sorted((s for s in range(S) if self.holder[s] is not None),
+                          key=lambda s: (-self.score[self.holder[s]], s))
+        protected = set(occupied[:self.sticky * S // 1000])
+        weak = [s for s in range(S) if self.holder[s] is not None and self.holder[s] not in wanted
+                and s not in protected]
         weak.sort(key=lambda s: (self.score[self.holder[s]], s))
         left = self.budget if self.budget > 0 else S + 1
         slot_of = {e: where[e] for e in hits}

@@ -12,9 +12,9 @@ import synth
 from tests.score_bruteforce import BruteScore
 
 
-def _compare(S, E, trace, budget=0):
-    o = oracle.LRU(S, E, policy=oracle.POLICY_SCORE, budget=budget)
-    b = BruteScore(S, E, budget)
+def _compare(S, E, trace, budget=0, sticky=0):
+    o = oracle.LRU(S, E, policy=oracle.POLICY_SCORE, budget=budget, sticky=sticky)
+    b = BruteScore(S, E, budget, sticky)
     for call in trace:
         po = o.plan(np.array(call, dtype=np.int32))
         pb = b.call([list(t) for t in call])
@@ -127,3 +127,63 @@ def test_outputs_do_not_depend_on_the_policy():
         bypassed += rb["info"]["n_bypass"]
     assert b.stats(0)["bypassed"] == bypassed > 0
     assert a.stats(0)["bypassed"] == 0
+
+
+@pytest.mark.parametrize("sticky", [500, 1000])
+@pytest.mark.parametrize("S,k,T,length", [(2, 1, 1, 6), (3, 1, 1, 5), (3, 1, 2, 3), (2, 2, 1, 4)])
+def test_exhaustive_small_sticky(S, k, T, length, sticky):
+    E = 4
+    calls = [c for c in itertools.product(_token_choices(E, k), repeat=T)
+             if len({e for tok in c for e in tok}) <= S]
+    for trace in itertools.product(calls, repeat=length):
+        _compare(S, E, [list(c) for c in trace], 0, sticky)
+
+
+@pytest.mark.parametrize("S,E,k,T,budget,sticky", [(8, 16, 4, 2, 0, 500), (32, 128, 8, 1, 0, 300),
+                                                   (32, 128, 8, 4, 2, 300), (7, 32, 2, 3, 0, 999)])
+def test_random_long_sticky(S, E, k, T, budget, sticky):
+    rng = random.Random(S * 11 + E + k + T + sticky)
+    zipf = np.array([1.0 / (r + 1) ** 1.1 for r in range(E)])
+    cdf = np.cumsum(zipf / zipf.sum())
+    trace = []
+    for _ in range(60):
+        call = []
+        for _t in range(T):
+            tok = []
+            while len(tok) < k:
+                e = int(np.searchsorted(cdf, rng.random()))
+                if e < E and e not in tok:
+                    tok.append(e)
+            call.append(tok)
+        if len({e for tok in call for e in tok}) <= S:
+            trace.append(call)
+    _compare(S, E, trace, budget, sticky)
+
+
+def test_full_sticky_share_never_evicts():
+    # every occupied slot protected: once the slots are full, misses are bypassed
+    o = oracle.LRU(4, 16, policy=oracle.POLICY_SCORE, sticky=1000)
+    rng = np.random.default_rng(2)
+    for i in range(50):
+        p = o.plan(rng.choice(16, (1, 2), replace=False).astype(np.int32))
+        assert p["info"]["n_evict"] == 0
+    assert (o.state()["slot_expert"] >= 0).all()
+
+
+def test_sticky_hand_worked():
+    # S = 2, E = 4.  Calls [0] x3, then [1]: slot 0 holds expert 0 (score
+    # 2.439), slot 1 expert 1 (1.0).  Then one call of four tokens 1, 2, 2, 2:
+    # after it expert 0 scores 1.6, expert 1 1.385, expert 2 2.71.  Expert 1
+    # is picked (pinned), so the only evictable slot is 0, whose 1.6 is below
+    # 2.71: without a sticky share, expert 2 replaces expert 0.  With a share
+    # of 500 (one slot) the highest-scoring occupied slot, slot 0, is kept, and
+    # expert 2 is computed without a slot (bypassed).
+    for sticky, slot, state in ((0, 0, [2, 1]), (500, -1, [0, 1])):
+        o = oracle.LRU(2, 4, policy=oracle.POLICY_SCORE, sticky=sticky)
+        for ids in ([[0]], [[0]], [[0]], [[1]]):
+            o.plan(np.array(ids, dtype=np.int32))
+        p = o.plan(np.array([[1], [2], [2], [2]], dtype=np.int32))
+        assert p["miss_expert"].tolist() == [2] and p["miss_slot"].tolist() == [slot], sticky
+        assert p["info"]["n_bypass"] == (1 if slot < 0 else 0)
+        assert o.state()["slot_expert"].tolist() == state, sticky
+        np.testing.assert_allclose(o.scores(), [1.6, 1.385, 2.71, 0.0], rtol=1e-6)
