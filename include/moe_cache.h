@@ -75,6 +75,10 @@ extern "C" {
  *   (score ascending, then lower index) if their score is strictly higher,
  *   while admit_budget lasts; other misses are bypassed: computed from the host
  *   store like any miss but not cached (miss_slot -1, counted in `bypassed`).
+ *   With sticky_permille p (Fork A's option to never evict the most-used share
+ *   of each layer's slots), once the call's scores are updated the
+ *   floor(p x slots_per_layer / 1000) occupied slots with the highest scores
+ *   (ties to the lower index) are not evictable in that call.
  *   Needs every call to fit one stage and the decode layer kernel: max_tokens x
  *   top_k <= min(slots_per_layer, 32), max_tokens <= 8, no tensor-core GEMM
  *   (gemm_min_tokens 0 or > max_tokens), and the pull fill or the memcpy fill
@@ -122,7 +126,9 @@ typedef struct {
                                 MOE_POLICY_SCORE (1) or MOE_POLICY_ADOPT (2),
                                 see above                                         */
     int32_t admit_budget;    /* MOE_POLICY_SCORE: admissions per call, 0 = no limit */
-    int32_t reserved;        /* must be 0                                          */
+    int32_t sticky_permille; /* MOE_POLICY_SCORE: per mille of the slots, highest
+                                scores first, that a call may not evict (0-1000;
+                                0 = none; must be 0 under the other policies)      */
     int64_t timeout_us;      /* limit of every bounded host wait, > 0; the decode
                                 layer kernel's device waits use a quarter of it,
                                 clamped to [1 ms, 2 s] (other kernels: 2 s)        */

@@ -49,7 +49,7 @@ class MoeCacheConfig(ctypes.Structure):
                 ("weight_mode", ctypes.c_int32), ("act_dtype", ctypes.c_int32),
                 ("fill_mode", ctypes.c_int32), ("gemm_min_tokens", ctypes.c_int32),
                 ("policy", ctypes.c_int32), ("admit_budget", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("timeout_us", ctypes.c_int64)]
+                ("sticky_permille", ctypes.c_int32), ("timeout_us", ctypes.c_int64)]
 
 
 class MoeHostStore(ctypes.Structure):
@@ -198,12 +198,13 @@ class MoECache:
     def __init__(self, *, n_layers, n_experts, top_k, hidden, ffn, slots_per_layer, max_tokens,
                  store, weight_mode=0, act_dtype="f32", fill_mode=MOE_FILL_MEMCPY,
                  gemm_min_tokens=0, timeout_us=10_000_000, layer_stride=None,
-                 expert_stride=None, stream=None, policy=MOE_POLICY_LRU, admit_budget=0):
+                 expert_stride=None, stream=None, policy=MOE_POLICY_LRU, admit_budget=0,
+                 sticky_permille=0):
         self.cfg = MoeCacheConfig(n_layers=n_layers, n_experts=n_experts, top_k=top_k, hidden=hidden,
                                   ffn=ffn, slots_per_layer=slots_per_layer, max_tokens=max_tokens,
                                   weight_mode=weight_mode, act_dtype=1 if act_dtype == "bf16" else 0,
                                   fill_mode=fill_mode, gemm_min_tokens=gemm_min_tokens, policy=policy,
-                                  admit_budget=admit_budget, reserved=0, timeout_us=timeout_us)
+                                  admit_budget=admit_budget, sticky_permille=sticky_permille, timeout_us=timeout_us)
         eb = moe_expert_bytes(hidden, ffn)
         self.expert_bytes = eb
         if isinstance(store, tuple):

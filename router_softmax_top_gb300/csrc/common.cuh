@@ -159,9 +159,11 @@ struct PlanArgs {
   int mailbox_stage_cap;  // capacity of the mailbox's unit_begin array
   uint32_t seq;
   uint32_t *epoch;    // the handle's call counter (device), advanced by every accepted call
-  int policy;         // 0 LRU, 1 decayed score with admission (plan_small_kernel only)
+  int policy;         // 0 LRU, 1 decayed score with admission (plan_small_kernel only),
+                      // 2 LRU whose staged calls keep their most-used experts (plan_kernel)
   int admit_budget;   // policy 1: admissions per call, 0 = no limit
   float *score;       // policy 1: the layer's decayed usage scores [E] (fp32)
+  int n_sticky;       // policy 1: occupied slots of highest score that may not be evicted
 };
 bool plan_small_ok(int T, int E, int k, int S);
 

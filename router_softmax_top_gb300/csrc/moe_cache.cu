@@ -280,7 +280,9 @@ int check_config(const moe_cache_config *g) {
   if (g->weight_mode != 0 && g->weight_mode != 1) return MOE_ERR_INVALID_ARG;
   if (g->act_dtype != 0 && g->act_dtype != 1) return MOE_ERR_INVALID_ARG;
   if (g->fill_mode != MOE_FILL_MEMCPY && g->fill_mode != MOE_FILL_PULL) return MOE_ERR_INVALID_ARG;
-  if (g->gemm_min_tokens < 0 || g->reserved != 0 || g->timeout_us <= 0) return MOE_ERR_INVALID_ARG;
+  if (g->gemm_min_tokens < 0 || g->timeout_us <= 0 || g->sticky_permille < 0 || g->sticky_permille > 1000 ||
+      (g->sticky_permille != 0 && g->policy != MOE_POLICY_SCORE))
+    return MOE_ERR_INVALID_ARG;
   if ((g->policy != MOE_POLICY_LRU && g->policy != MOE_POLICY_SCORE && g->policy != MOE_POLICY_ADOPT) ||
       g->admit_budget < 0)
     return MOE_ERR_INVALID_ARG;
@@ -562,6 +564,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.policy = g.policy;
   pa.admit_budget = g.admit_budget;
   pa.score = c->d_score + (size_t)layer * E;
+  pa.n_sticky = (int)((int64_t)g.sticky_permille * S / 1000);
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
   // memcpy fill, one stage guaranteed (distinct experts <= slots), few tokens:
   // the decode layer kernel too, its misses read from staging as they land

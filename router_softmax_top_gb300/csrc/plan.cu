@@ -699,7 +699,21 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
     uint32_t evbits = 0;  // this lane's evictable slots, bit c = slot c * 32 + lane
     for (int c = 0; c < kpl; ++c) {
       const int sl = c * 32 + lane;
-      if (sl < S && s_se[sl] >= 0 && !((s_pinned[c] >> lane) & 1u)) evbits |= 1u << c;
+      if (sl < S && s_se[sl] >= 0 && !((s_pinned[c] >> lane) & 1u)) {
+        // sticky share: a slot is kept when fewer than n_sticky occupied slots
+        // score higher (ties: lower index first)
+        bool kept = false;
+        if (a.n_sticky > 0) {
+          const float sc = s_score[s_se[sl]];
+          int above = 0;
+          for (int s2 = 0; s2 < S; ++s2) {
+            const int e2 = s_se[s2];
+            above += e2 >= 0 && (s_score[e2] > sc || (s_score[e2] == sc && s2 < sl));
+          }
+          kept = above < a.n_sticky;
+        }
+        if (!kept) evbits |= 1u << c;
+      }
     }
     __syncwarp();
     bool pend = miss;

@@ -34,7 +34,8 @@ class Pair:
     """A CUDA cache and an oracle cache over the same pinned host store."""
 
     def __init__(self, L, E, k, H, F, S, store, max_tokens, fill_mode=0, act="f32",
-                 weight_mode=0, gemm_min_tokens=0, timeout_us=20_000_000, policy=0, admit_budget=0):
+                 weight_mode=0, gemm_min_tokens=0, timeout_us=20_000_000, policy=0, admit_budget=0,
+                 sticky=0):
         import router_softmax_top_gb300 as moe
         self.moe = moe
         self.L, self.E, self.k, self.H, self.F, self.S = L, E, k, H, F, S
@@ -44,9 +45,9 @@ class Pair:
                                 slots_per_layer=S, max_tokens=max_tokens, store=store,
                                 weight_mode=weight_mode, act_dtype=act, fill_mode=fill_mode,
                                 gemm_min_tokens=gemm_min_tokens, timeout_us=timeout_us,
-                                policy=policy, admit_budget=admit_budget)
+                                policy=policy, admit_budget=admit_budget, sticky_permille=sticky)
         self.orc = oracle.Cache(L, E, k, H, F, S, store.numpy(), weight_mode=weight_mode, policy=policy,
-                                admit_budget=admit_budget)
+                                admit_budget=admit_budget, sticky=sticky)
 
     def close(self):
         self.gpu.close()

@@ -30,9 +30,16 @@ def test_binding_to_an_absent_node_is_refused():
 
 def test_defaults(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
-    a = bench.parse()
+    a = bench.resolve_defaults(bench.parse())
     assert (a.gpus, a.impl, a.workload, a.fill, a.policy) == (1, "ours", "decode", "pull", "lru")
-    assert a.warmup >= 3 and a.steps >= 1
+    assert a.warmup == bench.DECODE_WARMUP >= bench.COLD_STEPS >= 3 and a.steps >= 1
+    for extra in (["--workload", "prefill"], ["--impl", "reference"]):
+        monkeypatch.setattr(sys, "argv", ["bench.py"] + extra)
+        assert bench.resolve_defaults(bench.parse()).warmup == 64
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--warmup", "5"])
+    assert bench.resolve_defaults(bench.parse()).warmup == 5
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse()
     assert a.store_node == "auto" and a.gemm_min_tokens == 16 and a.tokens == 512
     assert a.preload_profile == 0 and a.decode_after == 0
     monkeypatch.setattr(sys, "argv", ["bench.py", "--store-node", "none"])

@@ -39,6 +39,30 @@ def test_score_policy_decode_shape(fill_mode, budget):
     p.close()
 
 
+@pytest.mark.parametrize("fill_mode,sticky", [(1, 300), (0, 300), (1, 1000)])
+def test_sticky_share(fill_mode, sticky):
+    # the highest-scoring share of occupied slots is never evicted: plans
+    # bit-exact against the oracle; a share of 1000 evicts nothing at all
+    sh = synth.DECODE
+    store = pinned_store(1, sh.E, sh.H, sh.F, seed=9)
+    steps = 60
+    _, logits, x = synth.decode_inputs(sh, steps, batch=1, seed=9, layers=[0])
+    p = Pair(1, sh.E, sh.k, sh.H, sh.F, sh.S, store, max_tokens=1, fill_mode=fill_mode, policy=1,
+             sticky=sticky)
+    for s in range(steps):
+        check = s in (0, 30, steps - 1)
+        g, plan, r = p.step(0, logits[s, 0], x[s, 0], compute_oracle=check)
+        assert_plan_equal(plan, r, f"step {s}")
+        if check:
+            assert row_rel_err(g, r["out"]).max() <= DECODE_TOL
+    assert_stats_equal(p.gpu.stats(0), p.orc.stats(0))
+    st = p.gpu.stats(0)
+    assert (st["evictions"] == 0) == (sticky == 1000)
+    if sticky == 1000:                             # full slots: every later miss is bypassed
+        assert st["bypassed"] > 0
+    p.close()
+
+
 def test_score_policy_four_token_calls():
     # 4 tokens x top-8 = 32 picks <= 32 slots: still one stage
     sh = synth.DECODE

@@ -64,6 +64,11 @@ def test_init_rejects_bad_config_before_any_cuda_call(lib):
     bad = moe.MoeCacheConfig(1, 8, 2, 250, 512, 4, 4, 0, 0, 0, 0, 0, 0, 0, 1000)  # H not a multiple of 64
     assert lib.moe_cache_init(ctypes.byref(bad), ctypes.byref(store), None, ctypes.byref(h)) \
         == moe.MOE_ERR_UNSUPPORTED
+    for policy, sticky in ((moe.MOE_POLICY_SCORE, 1001), (moe.MOE_POLICY_SCORE, -1),
+                           (moe.MOE_POLICY_LRU, 300), (moe.MOE_POLICY_ADOPT, 300), (3, 0)):
+        bad = moe.MoeCacheConfig(1, 8, 2, 256, 512, 4, 1, 0, 0, 1, 0, policy, 0, sticky, 1000)
+        assert lib.moe_cache_init(ctypes.byref(bad), ctypes.byref(store), None, ctypes.byref(h)) \
+            == moe.MOE_ERR_INVALID_ARG, (policy, sticky)
     good = moe.MoeCacheConfig(1, 8, 2, 256, 512, 4, 4, 0, 0, 0, 0, 0, 0, 0, 1000)
     assert lib.moe_cache_init(ctypes.byref(good), ctypes.byref(store), None, ctypes.byref(h)) \
         == moe.MOE_ERR_HOST_STORE   # null store
