@@ -32,10 +32,16 @@
  *  - Combine: "The idea: cache the hot experts on the GPU", step 4: partial
  *    results added, expert weights applied (weighted sum), here in ascending
  *    pick order.
+ *  - Replacement policies beside LRU: the decayed usage score with admission
+ *    ("llama.cpp + MoE expert cache", "Keeping the cache fresh") and its sticky
+ *    share; adopt, a staged call ending with its most-used experts ("llama.cpp:
+ *    fork with multi gpu acceleration ...", "Prefill preheat"); warm start from
+ *    usage counts (same page, "Persistent hot experts").
  *
  * Parity pins live in tests/test_oracle_*.py (hand-worked Q4_0 blocks, exact
- * integer GEMV cases, brute-force router, an independent brute-force LRU
- * simulator, exactly-once and budget-invariance checks).
+ * integer GEMV cases, brute-force router, independent brute-force simulators of
+ * LRU, the score policy and adopt, hand-worked warm starts, exactly-once and
+ * budget-invariance checks).
  */
 #include <math.h>
 #include <stdint.h>
