@@ -188,6 +188,22 @@ def resolve_defaults(args):
     return args
 
 
+def aggregate_over_ranks(dev_ms, e2e_ms_per_step, K, world, device):
+    """The slowest rank's timed region (and end-to-end step time), by a MAX
+    all-reduce when there are several ranks; whole-job tokens/s = world x K
+    steps (one token each) over that time.  Returns (max ms, tokens/s,
+    end-to-end tokens/s or None)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([dev_ms, e2e_ms_per_step if e2e_ms_per_step is not None else 0.0],
+                     dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev_max = float(t[0].item())
+    e2e_value = None if e2e_ms_per_step is None else world * 1e3 / float(t[1].item())
+    return dev_max, world * K / (dev_max * 1e-3), e2e_value
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -674,15 +690,10 @@ def main():
                "ms_per_step": 1e3 * e2e_s / K}
 
     # ---- aggregate over ranks
-    t_step = torch.tensor([dev_ms], dtype=torch.float64, device="cuda")
-    if world > 1:
-        dist.all_reduce(t_step, op=dist.ReduceOp.MAX)
-        if e2e is not None:
-            te = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device="cuda")
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-            e2e["value"] = world * 1e3 / float(te.item())
-    dev_ms_max = float(t_step.item())
-    value = world * K / (dev_ms_max * 1e-3)
+    dev_ms_max, value, e2e_value = aggregate_over_ranks(dev_ms, e2e["ms_per_step"] if e2e else None, K,
+                                                        world, "cuda")
+    if e2e is not None:
+        e2e["value"] = e2e_value
 
     # ---- roofline of the dominant kernel and of the whole step
     hbm_peak, _, peak_kind = measured_peaks()

@@ -46,3 +46,12 @@ def test_defaults(monkeypatch):
     assert bench.store_node(bench.parse()) == -1
     monkeypatch.setattr(sys, "argv", ["bench.py", "--store-node", "3"])
     assert bench.store_node(bench.parse()) == 3
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    # under torchrun only rank 0 times the oracle and prints; rank 1 returns at once
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference"])
+    assert bench.run_reference(bench.resolve_defaults(bench.parse())) is None
+    assert capsys.readouterr().out == ""
