@@ -13,7 +13,13 @@
 //
 // Stage-0 victims are ranked by (empty first, stamp, slot index); later stages
 // reuse all slots in ascending index (after stage 0 every slot holds an expert
-// of the call, all carrying the call's stamp).
+// of the call, all carrying the call's stamp).  Two other replacement policies:
+// the decayed usage score with admission ("llama.cpp + MoE expert cache",
+// "Keeping the cache fresh"; single-stage calls, plan_small_kernel<1>), and
+// adopt ("llama.cpp: fork with multi gpu acceleration ...", "Prefill preheat";
+// plan_kernel): a staged call takes its misses lowest rank first and streams
+// its later stages through the C slots that do not hold its highest-ranked
+// stage-0 experts, so that it ends holding its most-used experts.
 #include <math.h>
 
 #include "common.cuh"
