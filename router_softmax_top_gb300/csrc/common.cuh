@@ -2,6 +2,7 @@
 // of the C ABI).
 #pragma once
 
+#include <atomic>
 #include <cuda.h>  // CUtensorMap (types only; the encoder is fetched from the driver)
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -114,15 +115,32 @@ inline SlotLayout make_slot_layout(int H, int F) {
   return s;
 }
 
-// Raise a kernel's dynamic shared memory limit to `bytes` when needed (the
-// limit plus the kernel's static shared memory must stay within the opt-in
-// maximum, so it is raised to what a launch needs, not to the maximum).
+// The dynamic shared memory limit a kernel has been raised to, per device
+// (the attribute belongs to the kernel on each device).
+struct DynSmemLimit {
+  static constexpr int kDevices = 64;
+  std::atomic<size_t> bytes[kDevices] = {};
+};
+
+// Raise a kernel's dynamic shared memory limit on the current device to
+// `bytes` when needed (the limit plus the kernel's static shared memory must
+// stay within the opt-in maximum, so it is raised to what a launch needs, not
+// to the maximum).
 template <typename Kern>
-inline cudaError_t ensure_dyn_smem(Kern kernel, size_t bytes, size_t &current) {
-  if (bytes <= 48 * 1024 || bytes <= current) return cudaSuccess;
+inline cudaError_t ensure_dyn_smem(Kern kernel, size_t bytes, DynSmemLimit &limit) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = -1;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) return ge;
+  std::atomic<size_t> *cur = (dev >= 0 && dev < DynSmemLimit::kDevices) ? &limit.bytes[dev] : nullptr;
+  if (cur && bytes <= cur->load(std::memory_order_relaxed)) return cudaSuccess;
   const cudaError_t e =
       cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess) current = bytes;
+  if (e == cudaSuccess && cur) {
+    size_t seen = cur->load(std::memory_order_relaxed);
+    while (seen < bytes && !cur->compare_exchange_weak(seen, bytes, std::memory_order_relaxed)) {
+    }
+  }
   return e;
 }
 

@@ -775,12 +775,12 @@ cudaError_t launch_decode_layer(const FfnArgs &a, const uint8_t *host_layer, uin
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  auto go = [&](auto kern, size_t &cur) -> cudaError_t {
+  auto go = [&](auto kern, DynSmemLimit &cur) -> cudaError_t {
     const cudaError_t e = ensure_dyn_smem(kern, smem, cur);
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, j);
   };
-  static size_t c412 = 0, c322 = 0, c311 = 0, c211 = 0, c341 = 0, c381 = 0, c281 = 0;
+  static DynSmemLimit c412, c322, c311, c211, c341, c381, c281;
   if (two) return go(decode_layer_kernel<4, 1, 2>, c412);
   if (two3) return go(decode_layer_kernel<3, 2, 2>, c322);
   if (T == 1) return nb3 ? go(decode_layer_kernel<3, 1, 1>, c311) : go(decode_layer_kernel<2, 1, 1>, c211);

@@ -174,7 +174,7 @@ cudaError_t launch_tile(TileJob j, int max_units, cudaStream_t st) {
   j.G = G;
   const size_t smem = tile_smem(NMAT, j.nb, G);
   if (smem > budget) return cudaErrorInvalidValue;
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(q4_tile_gemv_kernel<NMAT>, smem, cur);
   if (e != cudaSuccess) return e;
   dim3 grid(j.R / 32, max_units);
@@ -617,7 +617,7 @@ cudaError_t launch_down_combine(const FfnArgs &a, const float *w, const int32_t 
   j.NS = dc_stages(a.F, a.k);
   j.err = a.err;
   const size_t smem = dc_smem(a.F / 32, a.k, j.NS);
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(down_combine_kernel, smem, cur);
   if (e != cudaSuccess) return e;
   dim3 grid(a.H / 32, T);
@@ -661,7 +661,7 @@ cudaError_t launch_fused_miss(const FfnArgs &a, const RepackArgs &r, int32_t *sy
   j.G = G;
   const size_t smem = fused_smem(a.H / 32, a.F / 32, G);
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(fused_miss_kernel, smem, cur);
   if (e != cudaSuccess) return e;
   fused_miss_kernel<<<grid, kThreads, smem, st>>>(j);
@@ -674,7 +674,7 @@ cudaError_t launch_repack(const RepackArgs &a, int S, int max_miss, cudaStream_t
   if (max_miss <= 0) return cudaSuccess;
   FillJob jb{a, S, a.lay.gate.nb > a.lay.down.nb ? a.lay.gate.nb : a.lay.down.nb};
   const size_t smem = 2 * (size_t)32 * jb.nb_max * 18;
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(fill_kernel, smem, cur);
   if (e != cudaSuccess) return e;
   const int tiles = 2 * a.lay.gate.rows / 32 + a.lay.down.rows / 32;

@@ -449,7 +449,7 @@ cudaError_t launch_gemm_t(const GemmMaps &maps, const RawMaps &raw, const GemmJo
   if (max_gunits <= 0) return cudaSuccess;
   if (j.nb % 2) return cudaErrorInvalidValue;
   const size_t smem = gemm_smem_bytes<NMAT>();
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT>, smem, cur);
   if (e != cudaSuccess) return e;
   dim3 grid((j.R + kGemmM - 1) / kGemmM, max_gunits);

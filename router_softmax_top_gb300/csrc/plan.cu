@@ -959,7 +959,7 @@ cudaError_t launch_plan(const PlanArgs &a_in, cudaStream_t st) {
     a.routed = 1;
   }
   const size_t smem = plan_smem_bytes(a.E, a.S);
-  static size_t cur = 0;
+  static DynSmemLimit cur;
   const cudaError_t e = ensure_dyn_smem(plan_kernel, smem, cur);
   if (e != cudaSuccess) return e;
   plan_kernel<<<1, NT, smem, st>>>(a);
