@@ -303,6 +303,28 @@ def profiled_traffic_ratio(kernel):
 
 
 # ------------------------------------------------------- oracle (baseline)
+def host_cpu_model() -> str:
+    """The host CPU's name from /proc/cpuinfo ("model name", else the Arm
+    implementer and part numbers) and the number of logical CPUs."""
+    name = impl = part = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key, val = key.strip(), val.strip()
+                if key == "model name" and not name:
+                    name = val
+                elif key == "CPU implementer" and not impl:
+                    impl = val
+                elif key == "CPU part" and not part:
+                    part = val
+    except OSError:
+        pass
+    if not name and (impl or part):
+        name = f"Arm implementer {impl} part {part}"
+    return f"{name or 'unknown'}, {os.cpu_count()} logical CPUs"
+
+
 def run_oracle_sample(sh, store_np, logits, x, n_steps, threads):
     """Time the CPU oracle over the first n_steps steps (all layers, outputs computed)."""
     import oracle
@@ -344,6 +366,7 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(sh, "oracle"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "cpu_model": host_cpu_model(),
                              "sample": f"{K} single-layer decode calls (layers in turn), outputs "
                                        f"computed; tokens/s = 1 / ({sh.L} x mean call time)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -807,9 +830,14 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n = max(1, min(args.cpu_sample_steps, logits_h.shape[0]))
         v, dt, cores = run_oracle_sample(sh, store.numpy(), logits_h, x_h, n, args.threads)
+        n1 = min(2, n)
+        v1, dt1, _ = run_oracle_sample(sh, store.numpy(), logits_h, x_h, n1, 1)
         result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                   "sample": f"first {n} decode steps (one token through all {sh.L} "
-                                            f"layers, outputs computed) from a cold cache; {dt:.1f} s"}
+                                            f"layers, outputs computed) from a cold cache; {dt:.1f} s",
+                                  "cpu_model": host_cpu_model(),
+                                  "value_1thread": v1,
+                                  "sample_1thread": f"first {n1} decode steps on one thread; {dt1:.1f} s"}
     cache.close()
     if rank == 0:
         print(json.dumps(result), flush=True)

@@ -55,3 +55,8 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference"])
     assert bench.run_reference(bench.resolve_defaults(bench.parse())) is None
     assert capsys.readouterr().out == ""
+
+
+def test_cpu_model_names_the_host():
+    m = bench.host_cpu_model()
+    assert m.endswith(f"{__import__('os').cpu_count()} logical CPUs") and not m.startswith("unknown,")
