@@ -159,7 +159,13 @@ typedef struct {
 } moe_cache_stats_t;
 
 /*
- * Create a cache.  cfg and store are read during the call only.
+ * Create a cache: per layer a fixed budget of slots_per_layer device slots,
+ * managed least-recently-used, for a model whose expert weights do not all fit
+ * ("Longhaul MoE loading", opening paragraph: a per-layer LRU cache of expert
+ * slots under a fixed budget), over a host-resident store of every expert
+ * ("llama.cpp + MoE expert cache", "The idea: cache the hot experts on the
+ * GPU": the full expert set stays in host RAM, a subset is cached on the GPU).
+ * cfg and store are read during the call only.
  * The host store must stay valid and unchanged until moe_cache_destroy.  If it
  * is not page-locked already, it is registered (cudaHostRegister, mapped) here
  * and unregistered at destroy; failure -> MOE_ERR_HOST_STORE.  Every (layer,
@@ -195,7 +201,11 @@ int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits, const 
 int moe_cache_sync(moe_cache *c, void *cuda_stream);
 
 /* Counters of one layer, or the sum over all layers for layer == -1 (host out;
- * synchronises with the device). */
+ * synchronises with the device).  The hit rate of the pages is the share of
+ * routed picks whose expert was already cached, pick_hits / (pick_hits +
+ * pick_misses) ("llama.cpp + MoE expert cache", "The idea: cache the hot
+ * experts on the GPU": 70-80% of a token's expert picks were cached ones);
+ * unique_* count distinct experts per call, unique_misses = uploads. */
 int moe_cache_stats(const moe_cache *c, int32_t layer, moe_cache_stats_t *out);
 
 /*
@@ -281,7 +291,17 @@ uint64_t moe_expert_bytes(int32_t hidden, int32_t ffn);
  * calls (the counters are cleared at the start of each call): calls that
  * overlap on the GPU race and must be serialised by the caller.  The first
  * call on each device looks up the array's device address (with that device
- * current); make that first call before any stream capture.
+ * current), and the first call in the process page-locks a 64 KiB status page
+ * compiled into the library (no allocation); make that first call before any
+ * stream capture.
+ * Failures on the device: each down tile waits, bounded (2 s), for the call's
+ * gate/up tiles.  If that wait gives up, the tile's rows of d_y become NaN for
+ * every token and the failure is recorded; the first call issued after the
+ * failed kernel has finished returns MOE_ERR_TIMEOUT without launching
+ * anything, and clears the record.
+ * Cost: when hidden or ffn is large (e.g. 4096 and 1536 at 8 tokens) the
+ * tokens' inputs are staged in groups that fit shared memory, and each group
+ * decodes the weight tiles again.
  */
 int moe_expert_ffn_static(const void *d_expert_block, int32_t hidden, int32_t ffn,
                           const float *d_x, int32_t n_tokens, float *d_y, void *cuda_stream);

@@ -240,7 +240,10 @@ static void sort_victims(const orc_lru *st, int *v, int n) {
  * higher than the weakest slot is promoted, up to a budget of copies).  Every
  * miss is still computed (from the host store); only admitted ones take a slot.
  *   clock += 1.  Token by token: every score *= 0.9, then each picked expert's
- *   score += 1, in fp32 (each operation rounded).  U, hits and misses as for LRU; the call must fit one stage
+ *   score += 1, in fp32 (each operation rounded).  The page gives the factor and
+ *   no precision; single precision is the reading taken, pinned by a trace on
+ *   which it decides an admission (a tie at exactly 1.0 that double precision
+ *   would not have).  U, hits and misses as for LRU; the call must fit one stage
  *   (|U| <= S), else -2.  Hits keep their slots (stamped).  Misses in order of
  *   (score descending, id ascending); each, while the budget lasts (0 =
  *   unlimited), takes the next empty slot (ascending index) if any, else the

@@ -21,9 +21,24 @@
 // address with cudaGetSymbolAddress (with that device current) and caches it,
 // so that first call should come before any stream capture.
 //
+// Failure reporting without allocation: a down tile waits (bounded, 2 s) for
+// the gate/up tiles of the call.  If that wait gives up, the tile writes NaN
+// into its 32 output rows of every token (so a failed call never leaves stale
+// values that look valid) and records the failure in a status word of a
+// 64 KiB page compiled into the library, which the first call in the process
+// page-locks and maps (cudaHostRegister of static memory; nothing is
+// allocated).  The first call issued after the failed kernel has finished
+// reads the record, clears it, launches nothing and returns MOE_ERR_TIMEOUT.
+//
+// Cost note: a down tile reads h of every token, but the shared memory holds
+// the inputs of at most G tokens at a time (G < T for large hidden or FFN
+// widths, e.g. hidden 4096 / FFN 1536 at 8 tokens); each group of G tokens
+// then decodes the tile's weights again, once per group.
+//
 // The arithmetic is that of the library's fused miss kernel: per 32-row tile,
 // lane = row, warp w of 8 sums the 32-blocks w, w+8, ... in ascending order,
 // the warp partial sums are added in warp order.
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -40,9 +55,18 @@ constexpr size_t kNaCounterBytes = 256;
 constexpr size_t kScratchBytes = kNaCounterBytes + sizeof(float) * kNaMaxTok * kNaMaxDim;  // 128.25 KiB
 constexpr int kNaWarps = 8, kNaThreads = 256;
 constexpr uint32_t kNaSpin = 1u << 26;
+constexpr uint64_t kNaWaitNs = 2000000000ull;       // limit of a down tile's wait
+constexpr uint64_t kNaInjectWaitNs = 20000000ull;   // ... under the test injection
+constexpr int kNaMaxDevices = 64;
+constexpr size_t kNaStatusPage = 65536;  // a whole page also where pages are 64 KiB
 
 // [0, 256): counters (queue head, finished gate/up tiles); then h [T][F] fp32.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+// Failure records, one int32 per device 64 bytes apart, in a static page that
+// is page-locked and mapped at set-up: the kernel sets its device's word when
+// a wait gives up; the host reads and clears it.
+alignas(kNaStatusPage) static int32_t g_na_status[kNaStatusPage / sizeof(int32_t)];
 
 __device__ __forceinline__ uint32_t na_smem(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -121,7 +145,16 @@ struct NaJob {
   const float *x;      // [T, H]
   float *y;            // [T, H]
   unsigned char *scratch;
+  int32_t *status;     // device alias of this device's failure record (mapped host word)
+  int inject;          // test hook: down tiles wait for a count that is never reached
+  uint64_t wait_ns;    // limit of a down tile's wait
 };
+
+__device__ __forceinline__ uint64_t na_now_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 size_t na_smem(int nbH, int nbF, int G) {
   const size_t canon = (size_t)32 * 18 * (2 * nbH > nbF ? 2 * nbH : nbF);
@@ -168,19 +201,36 @@ __global__ void __launch_bounds__(kNaThreads) expert_ffn_static_kernel(NaJob j) 
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (!gu) {
       if (tid == 0) {
+        // every gate/up tile has written h once counters[1] reaches tF (the
+        // injected fault waits for one more, which never comes)
+        const int need = j.inject ? tF + 1 : tF;
         int ok = 0;
+        uint64_t t0 = 0;
         for (uint32_t i = 0; i < kNaSpin; ++i) {
           int v;
           asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(&counters[1]) : "memory");
-          if (v >= tF) { ok = 1; break; }
+          if (v >= need) { ok = 1; break; }
+          if ((i & 63u) == 63u) {
+            const uint64_t now = na_now_ns();
+            if (t0 == 0) t0 = now;
+            else if (now - t0 > j.wait_ns) break;
+          }
           __nanosleep(64);
         }
         s_ok = ok;
       }
       __syncthreads();
-      if (!s_ok) {  // cannot happen while the gate/up tiles make progress; output left unwritten
+      if (!s_ok) {
+        // gave up: this tile's rows of y become NaN for every token and the
+        // failure is recorded for the host; no copy may still be landing
         asm volatile("cp.async.wait_all;" ::: "memory");
-        return;
+        for (int i = tid; i < T * 32; i += kNaThreads)
+          j.y[(size_t)(i >> 5) * j.H + t * 32 + (i & 31)] = __int_as_float(0x7fc00000);
+        if (tid == 0) {
+          asm volatile("st.relaxed.sys.global.b32 [%0], %1;" ::"l"(j.status), "r"(1) : "memory");
+          __threadfence_system();
+        }
+        continue;
       }
     }
     for (int g0 = 0; g0 < T; g0 += G) {
@@ -236,8 +286,18 @@ __global__ void __launch_bounds__(kNaThreads) expert_ffn_static_kernel(NaJob j) 
 }
 
 std::mutex g_na_mu;
-void *g_na_ptr[64] = {};  // device address of g_noalloc_scratch, per device
-size_t g_na_smem_set[64] = {};
+void *g_na_ptr[kNaMaxDevices] = {};       // device address of g_noalloc_scratch, per device
+int32_t *g_na_dstatus[kNaMaxDevices] = {};  // device alias of the device's failure record
+bool g_na_status_mapped = false;          // the status page is page-locked and mapped
+size_t g_na_smem_set[kNaMaxDevices] = {};
+
+// Test hook: MOE_STATIC_INJECT_WAIT=1 in the environment makes the down tiles
+// of a call wait for a gate/up count that is never reached, so that their
+// bounded wait gives up (after kNaInjectWaitNs) and the failure path runs.
+bool na_inject() {
+  const char *v = getenv("MOE_STATIC_INJECT_WAIT");
+  return v && v[0] == '1';
+}
 
 }  // namespace
 }  // namespace moe
@@ -254,36 +314,49 @@ MOE_API int moe_expert_ffn_static(const void *d_expert_block, int32_t hidden, in
   if ((uintptr_t)d_expert_block % 16 || (uintptr_t)d_x % 16 || (uintptr_t)d_y % 16)
     return MOE_ERR_INVALID_ARG;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  void *scratch = nullptr;
-  size_t smem_set = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_na_mu);
-    if (!g_na_ptr[dev]) {
-      void *p = nullptr;
-      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
-        cudaGetLastError();
-        return MOE_ERR_CUDA;
-      }
-      g_na_ptr[dev] = p;
-    }
-    scratch = g_na_ptr[dev];
-    smem_set = g_na_smem_set[dev];
-  }
-  cudaStream_t st = (cudaStream_t)cuda_stream;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNaMaxDevices) return MOE_ERR_CUDA;
   int G = n_tokens;
   while (G > 1 && na_smem(hidden / 32, ffn / 32, G) > 200 * 1024) --G;
   const size_t smem = na_smem(hidden / 32, ffn / 32, G);
   if (smem > 200 * 1024) return MOE_ERR_UNSUPPORTED;
-  if (smem > smem_set && smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(expert_ffn_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess) {
-      cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
+  void *scratch = nullptr;
+  int32_t *dstatus = nullptr;
+  {
+    // set-up, once per device (the status page once per process), and the
+    // kernel's shared-memory limit, which only ever grows
     std::lock_guard<std::mutex> lock(g_na_mu);
-    g_na_smem_set[dev] = smem;
+    if (!g_na_status_mapped) {
+      if (cudaHostRegister(g_na_status, sizeof(g_na_status), cudaHostRegisterMapped | cudaHostRegisterPortable) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      g_na_status_mapped = true;
+    }
+    if (!g_na_ptr[dev]) {
+      void *p = nullptr, *ps = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p ||
+          cudaHostGetDevicePointer(&ps, &g_na_status[dev * 16], 0) != cudaSuccess || !ps) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      g_na_dstatus[dev] = static_cast<int32_t *>(ps);
+      g_na_ptr[dev] = p;
+    }
+    if (smem > g_na_smem_set[dev] && smem > 48 * 1024) {
+      if (cudaFuncSetAttribute(expert_ffn_static_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      g_na_smem_set[dev] = smem;
+    }
+    scratch = g_na_ptr[dev];
+    dstatus = g_na_dstatus[dev];
   }
+  // a failure recorded by an earlier call that has finished on the GPU
+  if (__atomic_exchange_n(&g_na_status[dev * 16], 0, __ATOMIC_ACQ_REL) != 0) return MOE_ERR_TIMEOUT;
+  cudaStream_t st = (cudaStream_t)cuda_stream;
   if (cudaMemsetAsync(scratch, 0, kNaCounterBytes, st) != cudaSuccess) return MOE_ERR_CUDA;
   NaJob j;
   j.blk = static_cast<const uint8_t *>(d_expert_block);
@@ -294,6 +367,9 @@ MOE_API int moe_expert_ffn_static(const void *d_expert_block, int32_t hidden, in
   j.x = d_x;
   j.y = d_y;
   j.scratch = static_cast<unsigned char *>(scratch);
+  j.status = dstatus;
+  j.inject = na_inject() ? 1 : 0;
+  j.wait_ns = j.inject ? kNaInjectWaitNs : kNaWaitNs;
   const int items = ffn / 32 + hidden / 32;
   expert_ffn_static_kernel<<<items < 128 ? items : 128, kNaThreads, smem, st>>>(j);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;

@@ -187,3 +187,54 @@ def test_sticky_hand_worked():
         assert p["info"]["n_bypass"] == (1 if slot < 0 else 0)
         assert o.state()["slot_expert"].tolist() == state, sticky
         np.testing.assert_allclose(o.scores(), [1.6002, 1.3851, 2.71, 0.0], rtol=1e-4)
+
+
+def test_single_precision_reading_decides_an_admission():
+    """Hand-worked trace on which the precision of the score decides who is admitted.
+
+    "Keeping the cache fresh" gives the decay (x0.9 per token) but no arithmetic
+    precision; the reading taken is single precision, each operation rounded.
+    Two slots, experts A=0, B=1, C=2, D=3, one token per call, no budget limit:
+      * A and D fill the slots (calls [A], [D]) and are then picked alternately,
+        which keeps both scores near 4.3-5.3;
+      * B is picked once, 200 tokens before the last call, and C once, 190
+        tokens before it: both are bypassed (score 1 against slots above 4);
+      * the 189 calls before the last pick A only, so D's score decays to ~1e-8;
+      * the last call picks B and C together (k = 2).
+    In the last call B's score is 1 + 0.9^200 and C's is 1 + 0.9^190 in exact
+    arithmetic.  Both powers are below 2^-24, half a unit in the last place of
+    1.0 in single precision, so both scores round to exactly 1.0: a tie, which
+    goes to the lower id.  B is considered first, is stronger than the weakest
+    slot (D, ~1e-8), and takes D's slot 1; C then faces A (~9) and is bypassed.
+    A double-precision reading keeps 1 + 0.9^190 > 1 + 0.9^200 and would admit
+    C instead of B."""
+    from fractions import Fraction
+    # the two facts the expectation rests on, in exact rational arithmetic
+    assert Fraction(9, 10) ** 190 < Fraction(1, 2 ** 24)
+    assert Fraction(1) + Fraction(9, 10) ** 190 > Fraction(1) + Fraction(9, 10) ** 200
+    A, B, C, D = 0, 1, 2, 3
+    N = 600                                   # the last call is token N
+    o = oracle.LRU(2, 4, policy=oracle.POLICY_SCORE)
+    calls = [[[A]], [[D]]]
+    t = 3
+    while t < N - 200:
+        calls.append([[A]] if t % 2 else [[D]]); t += 1
+    calls.append([[B]]); t += 1               # token N - 200
+    while t < N - 190:
+        calls.append([[A]] if t % 2 else [[D]]); t += 1
+    calls.append([[C]]); t += 1               # token N - 190
+    while t < N:
+        calls.append([[A]]); t += 1
+    for c in calls:
+        p = o.plan(np.array(c, dtype=np.int32))
+        if c in ([[B]], [[C]]):
+            assert p["gpu_slot"].tolist() == [[-1]] and p["info"]["n_bypass"] == 1
+    assert o.state()["slot_expert"].tolist() == [A, D]
+    p = o.plan(np.array([[B, C]], dtype=np.int32))
+    assert p["gpu_slot"].tolist() == [[1, -1]]
+    assert list(zip(p["miss_expert"].tolist(), p["miss_slot"].tolist(), p["miss_evicted"].tolist())) == \
+        [(B, 1, D), (C, -1, -1)]
+    assert p["info"]["n_bypass"] == 1 and p["info"]["n_evict"] == 1
+    sc = o.scores()
+    assert sc[B] == np.float32(1.0) and sc[C] == np.float32(1.0)
+    assert o.state()["slot_expert"].tolist() == [A, B]
