@@ -62,6 +62,9 @@ extern "C" {
 #define MOE_ERR_HOST_STORE 5    /* host store invalid or could not be registered  */
 #define MOE_ERR_POISONED 6      /* an earlier call on this handle failed          */
 #define MOE_ERR_UNSUPPORTED 7   /* shape outside what the kernels implement       */
+#define MOE_ERR_CHECK 8         /* debug runs (MOE_CHECK_PLANS=1 at init): a
+                                   call's plan or the layer's slot table failed
+                                   the host-side consistency check               */
 
 /* Slot replacement policy.
  * MOE_POLICY_LRU: every miss takes a slot; victims are empty slots, then the
@@ -236,6 +239,14 @@ int moe_layer_last_plan(const moe_cache *c, int32_t layer, int32_t *ids, float *
 int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream);
 
 /*
+ * Debug runs: with MOE_CHECK_PLANS=1 in the environment when a handle is
+ * created, every forward call on it waits for its own completion (not while
+ * the stream is being captured) and checks on the host that its plan and the
+ * layer's slot table are consistent: ids in [0, E) and distinct per token,
+ * slots in [-1, S), stages and miss records in range, no expert in two slots,
+ * each pair's expert in the slot its plan names.  A failed check poisons the
+ * handle with MOE_ERR_CHECK.
+ *
  * Test hook: fault injection without a GPU fault.  what = MOE_INJECT_DECODE_WAIT
  * makes the next call that runs the decode layer kernel (pull fill, one stage,
  * <= 8 tokens) wait, in its down items, for a gate value carrying a call number
@@ -246,6 +257,13 @@ int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream);
  * MOE_ERR_INVALID_ARG for an unknown `what`.
  */
 #define MOE_INJECT_DECODE_WAIT 1
+/* what = MOE_INJECT_MEMCPY_FAIL | (n << 8), n >= 1 (0 reads as 1): the n-th next
+ * host-to-device copy of a missed block (memcpy fill, preload through staging)
+ * fails before it is issued, as a refused copy would.  The call that meets it
+ * returns MOE_ERR_CUDA and poisons the handle (stats stay readable, cuda_error
+ * reads cudaErrorUnknown); kernels of that call already launched finish, those
+ * waiting for the missing block by their bounded wait. */
+#define MOE_INJECT_MEMCPY_FAIL 2
 int moe_cache_inject(moe_cache *c, int32_t what);
 
 /*

@@ -24,11 +24,13 @@ MOE_ERR_TIMEOUT = 4
 MOE_ERR_HOST_STORE = 5
 MOE_ERR_POISONED = 6
 MOE_ERR_UNSUPPORTED = 7
+MOE_ERR_CHECK = 8
 
 MOE_FILL_MEMCPY = 0
 MOE_FILL_PULL = 1
 
 MOE_INJECT_DECODE_WAIT = 1
+MOE_INJECT_MEMCPY_FAIL = 2
 
 MOE_POLICY_LRU = 0
 MOE_POLICY_SCORE = 1

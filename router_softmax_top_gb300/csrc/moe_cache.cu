@@ -17,12 +17,14 @@
 #include <atomic>
 #include <chrono>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
 #include <vector>
 
 #include "common.cuh"
 #include "moe_cache.h"
+#include "plan_check.h"
 
 #define MOE_API extern "C" __attribute__((visibility("default")))
 
@@ -105,6 +107,8 @@ struct moe_cache {
 
   int poisoned = 0, last_error = MOE_OK, cuda_error = 0;
   int inject = 0;  // pending fault injection (moe_cache_inject)
+  int copy_fail_in = 0;  // > 0: the copy_fail_in-th next fill copy fails before it is issued
+  bool check_plans = false;  // MOE_CHECK_PLANS=1 at init: host check of every call's plan
   int last_layer = -1, last_T = 0;
   std::atomic<uint64_t> launches{0};
   TimingPool tp;
@@ -224,6 +228,17 @@ int wait_stream(cudaStream_t st, int64_t timeout_us) {
   }
 }
 
+// One host-to-device copy of a missed block (memcpy fill).  An injected
+// failure (MOE_INJECT_MEMCPY_FAIL) makes the n-th such copy fail before it is
+// issued, as a refused copy would.
+cudaError_t fill_copy(moe_cache *c, void *dst, const void *src, size_t bytes, cudaStream_t st) {
+  if (c->copy_fail_in > 0 && --c->copy_fail_in == 0) {
+    if (!c->cuda_error) c->cuda_error = (int)cudaErrorUnknown;
+    return cudaErrorUnknown;
+  }
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, st);
+}
+
 template <typename T>
 cudaError_t dalloc(T **p, size_t n) {
   return cudaMalloc(reinterpret_cast<void **>(p), sizeof(T) * (n ? n : 1));
@@ -310,6 +325,7 @@ MOE_API const char *moe_strerror(int code) {
     case MOE_ERR_HOST_STORE: return "host store invalid or not registrable";
     case MOE_ERR_POISONED: return "handle poisoned by an earlier failure";
     case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CHECK: return "a debug check of a call's plan failed";
     default: return "unknown error";
   }
 }
@@ -348,6 +364,10 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
     delete c;
     return code;
   };
+  {
+    const char *v = getenv("MOE_CHECK_PLANS");
+    c->check_plans = v && v[0] == '1';
+  }
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, c->device) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
@@ -640,9 +660,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
         for (int i = mlo; i < mlo + nmiss; ++i) {
           const MissItem m = c->h_mail_miss[i];
           if (!from_mailbox || m.expert < 0 || m.expert >= E) return MOE_ERR_CUDA;
-          if (cudaMemcpyAsync(c->d_staging + (size_t)(i - mlo) * c->expert_bytes,
-                              lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
-                              cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+          if (fill_copy(c, c->d_staging + (size_t)(i - mlo) * c->expert_bytes,
+                        lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes, c->side) != cudaSuccess)
             return MOE_ERR_CUDA;
         }
       }
@@ -718,9 +737,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
         for (int i = 0; i < nmiss_max; ++i) {
           const MissItem m = c->h_mail_miss[i];
           if (m.expert < 0 || m.expert >= E) return MOE_ERR_CUDA;
-          if (cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
-                              lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
-                              cudaMemcpyHostToDevice, c->side) != cudaSuccess)
+          if (fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
+                        lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes, c->side) != cudaSuccess)
             return MOE_ERR_CUDA;
         }
       }
@@ -781,9 +799,8 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
       for (int i = 0; i < hdr.n_miss; ++i) {
         const MissItem m = c->h_mail_miss[i];
         if (m.expert < 0 || m.expert >= E) return poison(c, MOE_ERR_CUDA);
-        if (cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
-                            lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes,
-                            cudaMemcpyHostToDevice, c->side) != cudaSuccess ||
+        if (fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
+                      lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes, c->side) != cudaSuccess ||
             c->write_value32(reinterpret_cast<CUstream>(c->side),
                              reinterpret_cast<CUdeviceptr>(c->d_miss_ready + i), hdr.epoch, 0) != CUDA_SUCCESS)
           return poison(c, MOE_ERR_CUDA);
@@ -895,6 +912,35 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
 #undef MOE_LAUNCH
   c->last_layer = layer;
   c->last_T = T;
+  if (c->check_plans) {
+    // debug runs: wait for the call, then check its plan and the layer's state
+    // on the host (skipped while the stream is being captured)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+    if (cs == cudaStreamCaptureStatusNone) {
+      int rc = wait_stream(st, g.timeout_us);
+      if (rc == MOE_OK) rc = wait_stream(c->side, g.timeout_us);
+      if (rc != MOE_OK) return poison(c, rc);
+      if (const int de = device_error_code(c)) return poison(c, de);
+      PlanHdr h;
+      std::vector<int32_t> ids(P), gs(P), sg(P), se(S), es(E);
+      std::vector<MissItem> mi(std::max(1, maxU));
+      bool ok = cudaMemcpy(&h, c->d_hdr, sizeof(h), cudaMemcpyDeviceToHost) == cudaSuccess &&
+                cudaMemcpy(ids.data(), c->d_ids, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess &&
+                cudaMemcpy(gs.data(), c->d_gpu_slot, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess &&
+                cudaMemcpy(sg.data(), c->d_stage, 4 * P, cudaMemcpyDeviceToHost) == cudaSuccess &&
+                cudaMemcpy(se.data(), pa.slot_expert, 4 * S, cudaMemcpyDeviceToHost) == cudaSuccess &&
+                cudaMemcpy(es.data(), pa.expert_slot, 4 * E, cudaMemcpyDeviceToHost) == cudaSuccess;
+      ok = ok && h.n_miss >= 0 && h.n_miss <= maxU &&
+           (h.n_miss == 0 ||
+            cudaMemcpy(mi.data(), c->d_miss, sizeof(MissItem) * h.n_miss, cudaMemcpyDeviceToHost) == cudaSuccess);
+      if (!ok) return poison(c, MOE_ERR_CUDA);
+      if (h.error) return poison(c, MOE_ERR_INVALID_ARG);
+      if (plan_check(T, k, E, S, h.n_stages, h.n_miss, ids.data(), gs.data(), sg.data(),
+                     reinterpret_cast<const int32_t *>(mi.data()), se.data(), es.data()) != 0)
+        return poison(c, MOE_ERR_CHECK);
+    }
+  }
   return MOE_OK;
 }
 
@@ -1070,9 +1116,8 @@ MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_s
         ra.by_expert = 1;
       } else {
         for (int i = 0; ok && i < n; ++i)
-          ok = cudaMemcpyAsync(c->d_staging + (size_t)i * c->expert_bytes,
-                               lbase + (size_t)items[i].expert * c->store.expert_stride, c->expert_bytes,
-                               cudaMemcpyHostToDevice, st) == cudaSuccess;
+          ok = fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
+                         lbase + (size_t)items[i].expert * c->store.expert_stride, c->expert_bytes, st) == cudaSuccess;
         ra.src_base = c->d_staging;
         ra.src_layer_off = 0;
         ra.src_expert_stride = 0;
@@ -1103,8 +1148,18 @@ MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_s
 }
 
 MOE_API int moe_cache_inject(moe_cache *c, int32_t what) {
-  if (!c || (what != 0 && what != MOE_INJECT_DECODE_WAIT)) return MOE_ERR_INVALID_ARG;
-  c->inject = what;
+  if (!c) return MOE_ERR_INVALID_ARG;
+  const int code = what & 0xFF, n = what >> 8;
+  if (what == 0) {
+    c->inject = 0;
+    c->copy_fail_in = 0;
+  } else if (what == MOE_INJECT_DECODE_WAIT) {
+    c->inject = what;
+  } else if (code == MOE_INJECT_MEMCPY_FAIL && n >= 0) {
+    c->copy_fail_in = n == 0 ? 1 : n;
+  } else {
+    return MOE_ERR_INVALID_ARG;
+  }
   return MOE_OK;
 }
 

@@ -83,3 +83,31 @@ def assert_stats_equal(gpu_stats, orc_stats):
     for key in ("calls", "pick_hits", "pick_misses", "unique_hits", "unique_misses", "evictions",
                 "bytes_uploaded", "stages", "staged_calls", "bypassed"):
         assert gpu_stats[key] == orc_stats[key], key
+
+
+def anonymous_store(nbytes: int):
+    """A host store in ordinary anonymous memory (transparent huge pages
+    requested), as a torch uint8 tensor; the library pins and maps it at init.
+    For stores too large for cudaHostAlloc to be quick (the large model's
+    130 GB)."""
+    import mmap
+    t = torch()
+    mm = mmap.mmap(-1, nbytes, flags=mmap.MAP_PRIVATE | mmap.MAP_ANONYMOUS)
+    if hasattr(mmap, "MADV_HUGEPAGE"):
+        mm.madvise(mmap.MADV_HUGEPAGE)
+    arr = np.frombuffer(mm, dtype=np.uint8, count=nbytes)
+    ten = t.from_numpy(arr)
+    ten._moe_mmap = mm          # keep the mapping alive with the tensor
+    return ten
+
+
+def mem_available_bytes():
+    """MemAvailable of the host (bytes), or None when unknown."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None

@@ -111,18 +111,51 @@ def test_non_finite_logit_large_call_poisons(store, fill_mode):
 
 
 def test_timeout_on_host_wait_poisons(store):
-    # a host wait limit shorter than any kernel launch: the mailbox wait gives up
+    # the stream is kept busy (~25 ms of device sleep) ahead of the call, so its
+    # plan cannot have written the mailbox when the host's wait (limit 1 ms)
+    # gives up: the call returns MOE_ERR_TIMEOUT every time
     import torch
-    c = _cache(store, timeout_us=1)
+    c = _cache(store, timeout_us=1000)           # memcpy fill, 4 tokens: the host reads the mailbox
     lg, x = _inputs(4)
     out = torch.empty((4, TINY.H), device="cuda")
-    rc = c.forward_rc(0, lg, x, out)
-    assert rc in (moe.MOE_ERR_TIMEOUT, moe.MOE_OK)
-    if rc == moe.MOE_ERR_TIMEOUT:
-        assert c.stats(-1)["poisoned"] == 1
-        assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
+    torch.cuda.synchronize()
+    torch.cuda._sleep(50_000_000)                  # ~25 ms at 2 GHz on the current stream
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_TIMEOUT
+    st = c.stats(-1)
+    assert st["poisoned"] == 1 and st["last_error"] == moe.MOE_ERR_TIMEOUT
+    assert c.forward_rc(0, lg, x, out) == moe.MOE_ERR_POISONED
     c.close()                                      # waits for the work in flight, frees all
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("T,S,n", [(1, 8, 1), (1, 8, 2), (4, 4, 2)])
+def test_failed_fill_copy_poisons(store, T, S, n):
+    # the n-th host-to-device copy of a missed block fails before it is issued
+    # (host-side injection): the call returns MOE_ERR_CUDA, the handle is
+    # poisoned, the statistics stay readable, and kernels of the call that wait
+    # for the missing block end by their bounded wait (timeout_us / 4 = 50 ms)
+    import torch
+    c = _cache(store, fill_mode=moe.MOE_FILL_MEMCPY, slots_per_layer=S, max_tokens=T, timeout_us=200_000)
+    lg, x = _inputs(4)
+    out = torch.empty((T, TINY.H), device="cuda")
+    c.inject(moe.MOE_INJECT_MEMCPY_FAIL | (n << 8))
+    rc = moe.MOE_OK
+    for t in range(4):                             # calls with misses until the n-th copy
+        s0 = t if T == 1 else 0
+        rc = c.forward_rc(0, lg[s0:s0 + T], x[s0:s0 + T], out)
+        if rc != moe.MOE_OK:
+            break
+    assert rc == moe.MOE_ERR_CUDA
+    st = c.stats(-1)
+    assert st["poisoned"] == 1 and st["last_error"] == moe.MOE_ERR_CUDA and st["cuda_error"] == 999
+    assert st["calls"] >= 1
+    assert c.forward_rc(0, lg[:T], x[:T], out) == moe.MOE_ERR_POISONED
+    c.close()
+    torch.cuda.synchronize()
+    c2 = _cache(store, fill_mode=moe.MOE_FILL_MEMCPY, slots_per_layer=S, max_tokens=T)
+    c2.forward(0, lg[:T], x[:T], out)
+    assert c2.sync() == moe.MOE_OK and torch.isfinite(out).all()
+    c2.close()
 
 
 def test_device_wait_limit_poisons(store):
@@ -157,7 +190,10 @@ def test_inject_rejects_unknown_code(store):
     c = _cache(store)
     with pytest.raises(moe.MoeError):
         c.inject(7)
-    c.inject(0)
+    with pytest.raises(moe.MoeError):
+        c.inject(moe.MOE_INJECT_MEMCPY_FAIL | (-1 << 8))
+    c.inject(moe.MOE_INJECT_MEMCPY_FAIL | (3 << 8))
+    c.inject(0)                                    # clears both kinds
     c.close()
 
 
