@@ -4,28 +4,37 @@
 // dense contraction (2 * 3 * H * F flops per routed pair, "Multi-GPU LLM
 // Calculator: VRAM Split and RAM Offload", "Decode and prefill").
 //
-// One CTA computes one output tile: 128 output features (rows of W) x up to
-// kGemmN routed pairs of one expert, looping over the input dimension in
-// chunks of 64.  The pairs' activations were copied beforehand into
-// pair-sorted order, so the tile's B operand is a contiguous row range that a
-// TMA tensor copy lands directly in the 128-byte-swizzled K-major layout.
-// Roles (11 warps):
-//   warp 9     brings each chunk's Q4_0 weights into a raw ring with two TMA
-//              tensor copies (nibbles, scales) over the slot planes viewed as
-//              [slot][matrix][tile][block][words] (one instruction per plane
-//              instead of one bulk copy per 1 KB run: issuing 16 bulk copies
-//              took as long as a whole chunk's dequantisation and MMAs);
-//   warp 10    brings each chunk's activation rows into a 6-deep ring with
-//              TMA tensor copies;
-//   warps 0-7  dequantise the raw chunk to bf16, w = (q - 8) * bf16(d) rounded
-//              to bf16, built with bf16x2 operations from the nibble bits, into
-//              the swizzled K-major layout the MMA reads;
-//   warp 8     one thread issues the MMAs (gate and up share the activations
-//              and accumulate into two TMEM regions) and commits each stage
-//              back to its producers;
-//   warps 0-7  finally read the accumulators from TMEM: gate/up -> h =
-//              silu(g) * u rounded to bf16 (pair-sorted rows); down -> y in
-//              fp32 (rows by pair).
+// Persistent kernel: one CTA per SM walks the call's output tiles, each
+// 128 output features (rows of W) x up to kGemmN routed pairs of one expert,
+// looping over the input dimension in chunks of 64; one pipeline runs on
+// across the CTA's tiles, so a tile's loads start while the previous tile is
+// still being multiplied and no tile pays for set-up.  The pairs' activations
+// were copied beforehand into pair-sorted order, so a tile's B operand is a
+// contiguous row range that a TMA tensor copy lands directly in the
+// 128-byte-swizzled K-major layout.  Roles:
+//   raw loader  brings each chunk's Q4_0 weights into a raw ring (10 deep for
+//               gate/up, 8 for down) with two TMA tensor copies (nibbles,
+//               scales) over the slot planes viewed as
+//               [slot][matrix][tile][block][words] (one instruction per plane:
+//               issuing one bulk copy per 1 KB run took as long as a whole
+//               chunk's dequantisation and MMAs);
+//   B loader    brings each chunk's activation rows into shared memory with a
+//               TMA tensor copy that completes on the stage's barrier;
+//   dequant     two groups of 8 warps take the chunks in turn and dequantise
+//               them to bf16, w = (q - 8) * bf16(d) rounded to bf16, built with
+//               bf16x2 operations from the nibble bits, straight into the
+//               stage's columns of tensor memory (tcgen05.st), so the weight
+//               operand never passes through shared memory;
+//   MMA         one thread waits for one barrier per chunk (the dequantised
+//               weights and the activations) and issues the MMAs -- A from
+//               tensor memory, B from shared memory; gate and up share the
+//               activations and accumulate into two TMEM regions -- then
+//               commits the stage back to both producers;
+//   epilogue    4 warps read the accumulators from TMEM: gate/up -> h =
+//               silu(g) * u rounded to bf16 (pair-sorted rows); down -> y in
+//               fp32 (rows by pair), while the next tile's chunks already load
+//               and dequantise (down: while the next tile accumulates into the
+//               second accumulator buffer).
 // Stages are guarded by mbarriers; every wait is bounded and gives up early
 // once another role has failed; on failure the CTA waits for its copies and
 // MMAs in flight, sets the handle's error word, frees TMEM and returns.
@@ -38,12 +47,8 @@ namespace {
 
 constexpr int kGemmM = 128;    // output features per tile
 constexpr int kGemmK = 64;     // input features per pipeline stage (128 bytes of bf16)
-constexpr int kAStages = 2;    // dequantised weight tiles
-constexpr int kBStages = 6;    // activation tiles
-constexpr int kRawStages = 4;  // raw Q4_0 chunks
-constexpr int kDqThreads = 256;
-constexpr int kMmaWarp = 8, kRawWarp = 9, kBWarp = 10;
-constexpr int kGemmThreads = 352;
+constexpr int kDqThreads = 256;  // one group of dequantising warps
+constexpr int kGemmDqg = 2;      // groups of dequantising warps
 constexpr uint32_t kGemmSpin = 1u << 26;
 constexpr uint64_t kGemmWaitNs = 2000000000ull;  // 2 s
 
@@ -69,10 +74,22 @@ __device__ __forceinline__ bool g_mbar_test(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool g_mbar_done(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(gsa(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase of `bar` with the given parity: gives up (false)
 // after kGemmWaitNs of wall time or kGemmSpin polls, or as soon as another role
-// of the CTA has failed (fail != nullptr).
+// of the CTA has failed (fail != nullptr).  A phase that has completed already
+// is seen by a non-blocking test first (a potentially suspending try_wait costs
+// a few hundred cycles even then, which the MMA issuer cannot afford per chunk).
 __device__ __forceinline__ bool g_mbar_wait(uint64_t *bar, uint32_t parity, const int *fail) {
+  if (g_mbar_done(bar, parity)) return true;
   uint64_t t0 = 0;
   for (uint32_t i = 0; i < kGemmSpin; ++i) {
     if (g_mbar_test(bar, parity)) return true;
@@ -84,6 +101,15 @@ __device__ __forceinline__ bool g_mbar_wait(uint64_t *bar, uint32_t parity, cons
     }
   }
   return false;
+}
+
+// The same wait by every lane of a warp, agreed by a vote: the lanes leave
+// their polling loops at different polls, and the warp-collective tcgen05
+// instructions that follow (.sync.aligned: ld, st, wait) need the warp
+// converged.  true only if every lane saw the phase complete.
+__device__ __forceinline__ bool g_mbar_wait_warp(uint64_t *bar, uint32_t parity, const int *fail) {
+  const bool ok = g_mbar_wait(bar, parity, fail);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -98,12 +124,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t idesc,
-                                     uint32_t accumulate) {
+// One MMA: D (tensor memory) += A x B, A in tensor memory (rows in lanes, K
+// along the columns, two bf16 per 32-bit column), B in shared memory.
+__device__ __forceinline__ void umma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t db, uint32_t idesc,
+                                        uint32_t accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
           tmem_d),
-      "l"(da), "l"(db), "r"(idesc), "r"(accumulate));
+      "r"(tmem_a), "l"(db), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(gsa(bar))
@@ -121,12 +149,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, float v[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
-// K-major tile (8-row groups of 1024 bytes).
-__device__ __forceinline__ uint32_t sw128_off(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+// The warp's 32 lanes x 16 consecutive 32-bit columns of tensor memory from
+// registers (each thread its lane).
+__device__ __forceinline__ void tmem_st16(uint32_t addr, const uint32_t v[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          addr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
 }
-
 
 // TMA tensor copy of one 2-D box (x = column, y = row) into shared memory,
 // completing on `bar` with the box's byte count.
@@ -183,23 +215,17 @@ __device__ __forceinline__ bool gunit_range(const PlanHdr *h, const int32_t *gb,
 }
 
 constexpr size_t kBTileBytes = (size_t)kGemmN * 128;  // one chunk of up to 128 activation rows
-template <int NMAT>
-constexpr size_t a_stage_bytes() { return (size_t)NMAT * kGemmM * 128; }
 // Q4_0 of one chunk (4 row tiles x 2 blocks per matrix), as the TMA boxes land:
 // nibbles [matrix][tile][block][512 B], then scales [matrix][tile][block][64 B]
 template <int NMAT>
 constexpr size_t raw_stage_bytes() { return (size_t)NMAT * (4 * 1024 + 4 * 128); }
-template <int NMAT>
-constexpr size_t gemm_smem_bytes() {
-  return kAStages * a_stage_bytes<NMAT>() + kBStages * kBTileBytes + kRawStages * raw_stage_bytes<NMAT>() + 1024;
-}
 
 // Dequantise block bi (32 inputs) of row r of one matrix from the raw chunk
 // (nib: the matrix's nibbles [tile][block][32 rows][16 B], sc: its scales
-// [tile][block][32 rows]) into the swizzled bf16 tile `a` (row r, 16-byte
-// chunks 4 bi .. 4 bi + 3).
-__device__ __forceinline__ void dequant_block(const unsigned char *nib, const unsigned char *sc, unsigned char *a,
-                                              int r, int bi, bool valid) {
+// [tile][block][32 rows]) into 16 bf16 pairs in input order: out[0..7] hold
+// values (0,1) .. (14,15) (low nibbles), out[8..15] values (16,17) .. (30,31).
+__device__ __forceinline__ void dequant_block(const unsigned char *nib, const unsigned char *sc, int r, int bi,
+                                              bool valid, uint32_t out[16]) {
   uint4 q = make_uint4(0x88888888u, 0x88888888u, 0x88888888u, 0x88888888u);
   float d = 0.f;
   if (valid) {
@@ -212,7 +238,6 @@ __device__ __forceinline__ void dequant_block(const unsigned char *nib, const un
   const __nv_bfloat162 d2 = __float2bfloat162_rn(d);
   const __nv_bfloat162 k136 = __float2bfloat162_rn(136.f);
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  uint32_t lo_pk[8], hi_pk[8];  // values 0..15 (low nibbles), 16..31 (high nibbles)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t p01 = __byte_perm(w[i], 0u, 0x4140u);  // bytes 4i, 4i+1 in the two halves
@@ -222,15 +247,11 @@ __device__ __forceinline__ void dequant_block(const unsigned char *nib, const un
     __nv_bfloat162 o[4];
 #pragma unroll
     for (int z = 0; z < 4; ++z) o[z] = __hmul2(__hsub2(*reinterpret_cast<const __nv_bfloat162 *>(&v[z]), k136), d2);
-    lo_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[0]);
-    lo_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[1]);
-    hi_pk[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[2]);
-    hi_pk[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[3]);
+    out[2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[0]);
+    out[2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[1]);
+    out[8 + 2 * i + 0] = *reinterpret_cast<const uint32_t *>(&o[2]);
+    out[8 + 2 * i + 1] = *reinterpret_cast<const uint32_t *>(&o[3]);
   }
-  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 0)) = make_uint4(lo_pk[0], lo_pk[1], lo_pk[2], lo_pk[3]);
-  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 1)) = make_uint4(lo_pk[4], lo_pk[5], lo_pk[6], lo_pk[7]);
-  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 2)) = make_uint4(hi_pk[0], hi_pk[1], hi_pk[2], hi_pk[3]);
-  *reinterpret_cast<uint4 *>(a + sw128_off(r, 4 * bi + 3)) = make_uint4(hi_pk[4], hi_pk[5], hi_pk[6], hi_pk[7]);
 }
 
 // Waits (bounded) until the last min(issued, stages) copies a loader issued
@@ -241,219 +262,338 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int stages, int issue
     (void)g_mbar_wait(&full[c % stages], (uint32_t)(c / stages) & 1u, nullptr);
 }
 
-template <int NMAT>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// Pipeline depths, tensor-memory layout and warp roles of the persistent
+// kernel.  Tensor memory (512 columns x 128 lanes of 32 bits): accumulators in
+// columns [0, 256) -- gate/up: one buffer, gate [0, 128) and up [128, 256);
+// down: two buffers of 128 -- and the dequantised weight stages in [256, 512),
+// each 64 inputs x 128 rows per matrix = 32 columns (two bf16 per column).
+// Keeping A in tensor memory takes its writes and the MMAs' reads of it off
+// shared memory, whose bandwidth otherwise bounds the chunk rate.
+template <int NMAT, int DQG>
+struct GemmCfg {
+  static constexpr int kAccBufs = NMAT == 2 ? 1 : 2;
+  static constexpr uint32_t kAccCols = NMAT == 2 ? 256 : 128;
+  static constexpr uint32_t kAStageCols = NMAT * 32;
+  // MMA stages: a dequantised weight stage in tensor memory and an activation
+  // stage in shared memory, completed together on one barrier (one wait per
+  // chunk for the MMA issuer)
+  static constexpr int kA = (int)(256 / kAStageCols);  // 4 (gate/up) or 8 (down)
+  static constexpr int kB = kA;
+  static constexpr int kRaw = NMAT == 2 ? 10 : 8;      // raw Q4_0 stages (bytes in flight from HBM)
+  static constexpr int kDqWarps = 8 * DQG;
+  static constexpr int kEpiWarp0 = kDqWarps;           // 4 epilogue warps; warp w reads TMEM lanes 32 (w % 4) ..
+  static constexpr int kMmaWarp = kDqWarps + 4, kRawWarp = kDqWarps + 5, kBWarp = kDqWarps + 6;
+  static constexpr int kThreads = 32 * (kDqWarps + 7);
+  static constexpr size_t kRawStage = raw_stage_bytes<NMAT>();
+  static constexpr size_t kSmem = kB * kBTileBytes + kRaw * kRawStage + 1024;
+  static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start at a multiple of 4");
+  static_assert(kSmem <= 227 * 1024, "shared memory");
+};
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemA0 = 256;  // first column of the weight stages
+
+// Persistent grouped GEMM: one CTA per SM walks the call's tiles (GEMM unit of
+// up to kGemmN pairs of one expert) x (128-row tile of the matrix), tile t =
+// blockIdx.x + i * gridDim.x, with one pipeline that runs on across tiles:
+// the loaders fetch chunk after chunk of tile after tile, the dequantising
+// warps and the MMA warp consume them in the same order, and the MMA warp
+// accumulates tile i into its TMEM buffer (i % 2 for down, the one buffer for
+// gate/up) once the epilogue warps have drained the tile that used it before.
+// Every role walks the same tile list; chunk g (counted over the CTA's tiles)
+// uses stage g % depth of each ring.
+template <int NMAT, int DQG>
+__global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
     umma_gemm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ RawMaps raw_maps,
                      const GemmJob j) {
+  using C = GemmCfg<NMAT, DQG>;
   int lo, hi;
   if (!gunit_range(j.hdr, j.gunit_begin, j.range_kind, j.stage, lo, hi)) return;
-  const int gu = lo + (int)blockIdx.y;
-  if (gu >= hi) return;
-  const WorkUnit wu = j.gunits[gu];
-  const WorkItem it = j.items[wu.item];
-  const int n = wu.pair_count;                 // 1..kGemmN
-  const int nr = (n + 15) & ~15;               // MMA N: pairs rounded up to 16
-  const int bsel = nr <= 16 ? 0 : nr <= 32 ? 1 : nr <= 64 ? 2 : 3;
-  const uint32_t b_bytes = (uint32_t)(16 << bsel) * 128u;  // activation box of 16 << bsel rows
-  const int m0 = blockIdx.x * kGemmM;
-  const int rt0 = m0 >> 5, n_rt = min(4, (j.R >> 5) - rt0);  // valid 32-row tiles
-  const int nb = j.nb, n_chunks = nb / 2;      // 64 inputs = 2 blocks per chunk
+  const int nM = (j.R + kGemmM - 1) / kGemmM;
+  const int nT = (hi - lo) * nM;
+  if ((int)blockIdx.x >= nT) return;
+  const int n_my = (nT - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;  // tiles of this CTA
+  const int n_chunks = j.nb / 2;                                      // 64 inputs = 2 blocks per chunk
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char *sm =
       reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~(uintptr_t)1023);
-  unsigned char *sa_base = sm;
-  unsigned char *sb_base = sa_base + kAStages * a_stage_bytes<NMAT>();
-  unsigned char *raw = sb_base + kBStages * kBTileBytes;
-  __shared__ __align__(8) uint64_t afull[kAStages], aempty[kAStages], bfull[kBStages], bempty[kBStages],
-      rfull[kRawStages], rempty[kRawStages], done;
+  unsigned char *sb_base = sm;
+  unsigned char *raw = sb_base + C::kB * kBTileBytes;
+  // full[s]: the dequantising warps' arrivals plus the activation copy's bytes;
+  // empty[s]: the MMAs that read stage s have completed
+  __shared__ __align__(8) uint64_t full[C::kA], empty[C::kA], rfull[C::kRaw], rempty[C::kRaw],
+      accfull[C::kAccBufs], accempty[C::kAccBufs], done;
   __shared__ uint32_t tmem_base;
-  __shared__ int s_rows[kGemmN];
   __shared__ int s_fail;
 
-  constexpr uint32_t kCols = NMAT == 2 ? 2 * kGemmN : kGemmN;  // TMEM columns (power of 2)
   if (tid == 0) {
-    for (int s = 0; s < kAStages; ++s) {
-      g_mbar_init(&afull[s], kDqThreads);
-      g_mbar_init(&aempty[s], 1);
+    for (int s = 0; s < C::kA; ++s) {
+      g_mbar_init(&full[s], kDqThreads + 1);
+      g_mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < kBStages; ++s) {
-      g_mbar_init(&bfull[s], 1);
-      g_mbar_init(&bempty[s], 1);
-    }
-    for (int s = 0; s < kRawStages; ++s) {
+    for (int s = 0; s < C::kRaw; ++s) {
       g_mbar_init(&rfull[s], 1);
       g_mbar_init(&rempty[s], kDqThreads);
+    }
+    for (int b = 0; b < C::kAccBufs; ++b) {
+      g_mbar_init(&accfull[b], 1);
+      g_mbar_init(&accempty[b], 128);
     }
     g_mbar_init(&done, 1);
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (tid < kGemmN) s_rows[tid] = tid < n ? j.perm[wu.pair_begin + tid] : -1;
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(gsa(&tmem_base)),
-                 "r"(kCols));
+                 "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = tmem_base;
-  const int slot_ix = j.slot0 + it.slot;
+  // tile i of this CTA: GEMM unit and 128-row tile
+  auto tile_unit = [&](int i, int &mt) -> int {
+    const int t = (int)blockIdx.x + i * (int)gridDim.x;
+    mt = t % nM;
+    return lo + t / nM;
+  };
 
-  if (warp == kRawWarp) {
-    // ---- raw Q4_0 loader: per chunk, blocks 2c, 2c+1 of row tiles rt0 .. rt0+3
-    // of each matrix: one tensor copy of the nibbles, one of the scales (the
-    // full boxes land, tiles past the matrix as zeros)
+  if (warp == C::kRawWarp) {
+    // ---- raw Q4_0 loader: per chunk, blocks 2c, 2c+1 of row tiles 4 mt .. 4 mt + 3
+    // of each matrix: one tensor copy of the nibbles, one of the scales (tiles
+    // past the matrix land as zeros)
     if (lane == 0) {
       const CUtensorMap *mn = NMAT == 2 ? &raw_maps.gu_nib : &raw_maps.dn_nib;
       const CUtensorMap *ms = NMAT == 2 ? &raw_maps.gu_sc : &raw_maps.dn_sc;
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mn)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(ms)) : "memory");
-      int c = 0;
-      for (; c < n_chunks; ++c) {
-        const int s = c % kRawStages;
-        if (c >= kRawStages && !g_mbar_wait(&rempty[s], (uint32_t)((c / kRawStages) - 1) & 1u, &s_fail)) {
-          s_fail = 1;
-          break;
-        }
-        unsigned char *rs = raw + (size_t)s * raw_stage_bytes<NMAT>();
-        expect_tx(&rfull[s], (uint32_t)raw_stage_bytes<NMAT>());
-        if (NMAT == 2) {
-          tma_load_5d(rs, mn, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
-          tma_load_5d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
-        } else {
-          tma_load_4d(rs, mn, 0, 2 * c, rt0, slot_ix, &rfull[s]);
-          tma_load_4d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, slot_ix, &rfull[s]);
+      int g = 0;
+      bool stop = false;
+      for (int i = 0; i < n_my && !stop; ++i) {
+        int mt;
+        const WorkUnit wu = j.gunits[tile_unit(i, mt)];
+        const int slot_ix = j.slot0 + j.items[wu.item].slot, rt0 = 4 * mt;
+        for (int c = 0; c < n_chunks; ++c, ++g) {
+          const int s = g % C::kRaw;
+          if (g >= C::kRaw && !g_mbar_wait(&rempty[s], (uint32_t)((g / C::kRaw) - 1) & 1u, &s_fail)) {
+            s_fail = 1;
+            stop = true;
+            break;
+          }
+          unsigned char *rs = raw + (size_t)s * C::kRawStage;
+          expect_tx(&rfull[s], (uint32_t)C::kRawStage);
+          if (NMAT == 2) {
+            tma_load_5d(rs, mn, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
+            tma_load_5d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, 0, slot_ix, &rfull[s]);
+          } else {
+            tma_load_4d(rs, mn, 0, 2 * c, rt0, slot_ix, &rfull[s]);
+            tma_load_4d(rs + NMAT * 4096, ms, 0, 2 * c, rt0, slot_ix, &rfull[s]);
+          }
         }
       }
-      drain_ring(rfull, kRawStages, c);
+      drain_ring(rfull, C::kRaw, g);
     }
-  } else if (warp == kBWarp) {
+  } else if (warp == C::kBWarp) {
     // ---- activation loader: rows [pair_begin, pair_begin + box) of the sorted
     // buffer, columns [64 c, 64 c + 64), one TMA tensor copy per chunk
     if (lane == 0) {
-      const CUtensorMap *map = &maps.box[bsel];
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-      int c = 0;
-      for (; c < n_chunks; ++c) {
-        const int s = c % kBStages;
-        if (c >= kBStages && !g_mbar_wait(&bempty[s], (uint32_t)((c / kBStages) - 1) & 1u, &s_fail)) {
-          s_fail = 1;
-          break;
+      for (int b = 0; b < 4; ++b)
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.box[b])) : "memory");
+      int g = 0;
+      bool stop = false;
+      for (int i = 0; i < n_my && !stop; ++i) {
+        int mt;
+        const WorkUnit wu = j.gunits[tile_unit(i, mt)];
+        const int nr = (wu.pair_count + 15) & ~15;
+        const int bsel = nr <= 16 ? 0 : nr <= 32 ? 1 : nr <= 64 ? 2 : 3;
+        const uint32_t b_bytes = (uint32_t)(16 << bsel) * 128u;
+        for (int c = 0; c < n_chunks; ++c, ++g) {
+          const int s = g % C::kB;
+          if (g >= C::kB && !g_mbar_wait(&empty[s], (uint32_t)((g / C::kB) - 1) & 1u, &s_fail)) {
+            s_fail = 1;
+            stop = true;
+            break;
+          }
+          expect_tx(&full[s], b_bytes);
+          tma_load_2d(sb_base + (size_t)s * kBTileBytes, &maps.box[bsel], c * kGemmK, wu.pair_begin, &full[s]);
         }
-        expect_tx(&bfull[s], b_bytes);
-        tma_load_2d(sb_base + (size_t)s * kBTileBytes, map, c * kGemmK, wu.pair_begin, &bfull[s]);
       }
-      drain_ring(bfull, kBStages, c);
+      // no copy may still be landing when the CTA leaves: the last stages'
+      // barriers complete once their bytes (and dequantised halves) are in
+      drain_ring(full, C::kB, g);
     }
-  } else if (warp == kMmaWarp) {
-    // ---- MMA issuer
+  } else if (warp == C::kMmaWarp) {
+    // ---- MMA issuer: tile i into accumulator buffer i % kAccBufs, once the
+    // epilogue has drained the tile that used it before (i - kAccBufs)
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kGemmM, nr);
-      for (int c = 0; c < n_chunks; ++c) {
-        const int sa = c % kAStages, sb = c % kBStages;
-        if (!g_mbar_wait(&afull[sa], (uint32_t)(c / kAStages) & 1u, &s_fail) ||
-            !g_mbar_wait(&bfull[sb], (uint32_t)(c / kBStages) & 1u, &s_fail)) {
+      int g = 0;
+      bool stop = false;
+      for (int i = 0; i < n_my && !stop; ++i) {
+        int mt;
+        const WorkUnit wu = j.gunits[tile_unit(i, mt)];
+        const int nr = (wu.pair_count + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(kGemmM, nr);
+        const int buf = i % C::kAccBufs, use = i / C::kAccBufs;
+        if (use >= 1 && !g_mbar_wait(&accempty[buf], (uint32_t)(use - 1) & 1u, &s_fail)) {
           s_fail = 1;
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t b_addr = gsa(sb_base + (size_t)sb * kBTileBytes);
-        const uint32_t a_base = gsa(sa_base + (size_t)sa * a_stage_bytes<NMAT>());
+        const uint32_t dcol = tmem + (uint32_t)buf * C::kAccCols;
+        for (int c = 0; c < n_chunks; ++c, ++g) {
+          const int sa = g % C::kA, sb = sa;
+          if (!g_mbar_wait(&full[sa], (uint32_t)(g / C::kA) & 1u, &s_fail)) {
+            s_fail = 1;
+            stop = true;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t b_addr = gsa(sb_base + (size_t)sb * kBTileBytes);
+          const uint32_t a_col = tmem + kTmemA0 + (uint32_t)sa * C::kAStageCols;
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) {
-          const uint32_t a_addr = a_base + (uint32_t)(m * kGemmM * 128);
+          for (int m = 0; m < NMAT; ++m) {
 #pragma unroll
-          for (int ks = 0; ks < kGemmK / 16; ++ks)
-            umma(tmem + (uint32_t)(m * kGemmN), sw128_desc(a_addr + ks * 32), sw128_desc(b_addr + ks * 32), idesc,
-                 (c > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < kGemmK / 16; ++ks)
+              umma_ts(dcol + (uint32_t)(m * kGemmN), a_col + (uint32_t)(m * 32 + ks * 8),
+                      sw128_desc(b_addr + ks * 32), idesc, (c > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty[sa]);
         }
-        umma_commit(&aempty[sa]);
-        umma_commit(&bempty[sb]);
+        if (!stop) umma_commit(&accfull[buf]);
       }
       umma_commit(&done);  // also on failure: `done` then tracks the MMAs in flight
     }
-  } else {
-    // ---- dequant (warps 0-7): gate/up: thread = (matrix, row), both blocks;
-    // down: thread = (block, row)
-    const int r = tid & 127, hi_half = tid >> 7;
-    const bool valid = (r >> 5) < n_rt;
-    for (int c = 0; c < n_chunks; ++c) {
-      const int sa = c % kAStages, rsi = c % kRawStages;
-      if (c >= kAStages && !g_mbar_wait(&aempty[sa], (uint32_t)((c / kAStages) - 1) & 1u, &s_fail)) {
+  } else if (warp >= C::kEpiWarp0) {
+    // ---- epilogue (4 warps): warp w reads TMEM lanes 32 (w % 4) .. + 31 (rows of
+    // the tile): gate/up -> h = silu(g) * u rounded to bf16 (pair-sorted rows);
+    // down -> y in fp32 (rows by pair).  The buffer is released once read.
+    const int q = warp & 3;
+    for (int i = 0; i < n_my; ++i) {
+      int mt;
+      const WorkUnit wu = j.gunits[tile_unit(i, mt)];
+      const int n = wu.pair_count, nr = (n + 15) & ~15, buf = i % C::kAccBufs;
+      if (!g_mbar_wait_warp(&accfull[buf], (uint32_t)(i / C::kAccBufs) & 1u, &s_fail)) {
         s_fail = 1;
         break;
       }
-      if (!g_mbar_wait(&rfull[rsi], (uint32_t)(c / kRawStages) & 1u, &s_fail)) {
-        s_fail = 1;
-        break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      const int row = mt * kGemmM + q * 32 + lane;
+      const uint32_t lane_addr = tmem + (uint32_t)buf * C::kAccCols + ((uint32_t)(q * 32) << 16);
+      // down: the tile's pairs (rows of y), lane l holding pairs l, l + 32, l + 64, l + 96
+      static_assert(kGemmN == 128, "four pair registers per lane");
+      int p0 = 0, p1 = 0, p2 = 0, p3 = 0;
+      if (NMAT == 1) {
+        const int32_t *pp = j.perm + wu.pair_begin;
+        p0 = lane < n ? pp[lane] : 0;
+        p1 = 32 + lane < n ? pp[32 + lane] : 0;
+        p2 = 64 + lane < n ? pp[64 + lane] : 0;
+        p3 = 96 + lane < n ? pp[96 + lane] : 0;
       }
-      const unsigned char *rs = raw + (size_t)rsi * raw_stage_bytes<NMAT>();
-      unsigned char *st = sa_base + (size_t)sa * a_stage_bytes<NMAT>();
-      if (NMAT == 2) {
-        const unsigned char *nib = rs + hi_half * 4096, *sc = rs + NMAT * 4096 + hi_half * 512;
-        unsigned char *a = st + (size_t)hi_half * kGemmM * 128;
-        dequant_block(nib, sc, a, r, 0, valid);
-        dequant_block(nib, sc, a, r, 1, valid);
-      } else {
-        dequant_block(rs, rs + NMAT * 4096, st, r, hi_half, valid);
-      }
-      g_mbar_arrive(&rempty[rsi]);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      g_mbar_arrive(&afull[sa]);
-    }
-  }
-
-  // ---- epilogue (warps 0-7): warp w reads TMEM lanes 32 (w % 4) .. + 31 (the
-  // tile's rows) and the 16-column groups of parity w / 4
-  const bool ok = warp < 8 && g_mbar_wait(&done, 0, &s_fail) && !s_fail;
-  if (warp < 8 && ok) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    const int q = warp & 3, half = warp >> 2;
-    const int row = m0 + q * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-    for (int c0 = half * 16; c0 < nr; c0 += 32) {
-      float g[16], u[16];
-      tmem_ld16(lane_addr + c0, g);
-      if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
-      if (row < j.R) {
+      for (int c0 = 0; c0 < nr; c0 += 16) {
+        float g[16], u[16];
+        __syncwarp();
+        tmem_ld16(lane_addr + c0, g);
+        if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
+        const int pr = c0 < 32 ? p0 : c0 < 64 ? p1 : c0 < 96 ? p2 : p3;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = c0 + i;
-          if (col < n) {
-            if (NMAT == 2)
-              j.h16s[(size_t)(wu.pair_begin + col) * j.R + row] = __float2bfloat16_rn(g[i] / (1.f + expf(-g[i])) * u[i]);
-            else
-              j.y[(size_t)s_rows[col] * j.R + row] = g[i];
+        for (int i2 = 0; i2 < 16; ++i2) {
+          const int col = c0 + i2;
+          if (NMAT == 2) {
+            if (col < n && row < j.R)
+              j.h16s[(size_t)(wu.pair_begin + col) * j.R + row] =
+                  __float2bfloat16_rn(g[i2] / (1.f + expf(-g[i2])) * u[i2]);
+          } else {
+            const int p = __shfl_sync(0xffffffffu, pr, (c0 & 31) + i2);
+            if (col < n && row < j.R) j.y[(size_t)p * j.R + row] = g[i2];
           }
         }
       }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      g_mbar_arrive(&accempty[buf]);
     }
-  } else if (warp < 8 && !ok) {
-    s_fail = 1;
+  } else {
+    // ---- dequant (DQG groups of 8 warps, chunks in turn) into the tensor-memory
+    // weight stage: gate/up: thread = (matrix, row), both blocks (32 columns);
+    // down: thread = (block, row) (16 columns).  Warp w writes TMEM lanes
+    // 32 (w % 4) .. + 31, the rows its threads dequantise.
+    const int grp = warp / 8, lt = tid & (kDqThreads - 1);
+    const int r = lt & 127, hi_half = lt >> 7;
+    const uint32_t lane_base = (uint32_t)((r & ~31) << 16);
+    int g = 0;
+    bool stop = false;
+    for (int i = 0; i < n_my && !stop; ++i) {
+      int mt;
+      (void)tile_unit(i, mt);
+      const int n_rt = min(4, (j.R >> 5) - 4 * mt);  // valid 32-row tiles
+      const bool valid = (r >> 5) < n_rt;
+      for (int c = 0; c < n_chunks; ++c, ++g) {
+        if (DQG > 1 && g % DQG != grp) continue;
+        const int sa = g % C::kA, rsi = g % C::kRaw;
+        if (!g_mbar_wait_warp(&rfull[rsi], (uint32_t)(g / C::kRaw) & 1u, &s_fail)) {
+          s_fail = 1;
+          stop = true;
+          break;
+        }
+        const unsigned char *rs = raw + (size_t)rsi * C::kRawStage;
+        uint32_t v0[16], v1[16];
+        if (NMAT == 2) {
+          const unsigned char *nib = rs + hi_half * 4096, *sc = rs + NMAT * 4096 + hi_half * 512;
+          dequant_block(nib, sc, r, 0, valid, v0);
+          dequant_block(nib, sc, r, 1, valid, v1);
+        } else {
+          dequant_block(rs, rs + NMAT * 4096, r, hi_half, valid, v0);
+        }
+        g_mbar_arrive(&rempty[rsi]);
+        // the stage's previous MMAs (chunk g - kA) must have read it
+        if (g >= C::kA && !g_mbar_wait_warp(&empty[sa], (uint32_t)((g / C::kA) - 1) & 1u, &s_fail)) {
+          s_fail = 1;
+          stop = true;
+          break;
+        }
+        __syncwarp();
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t a_col = tmem + lane_base + kTmemA0 + (uint32_t)sa * C::kAStageCols;
+        if (NMAT == 2) {
+          tmem_st16(a_col + (uint32_t)hi_half * 32, v0);
+          tmem_st16(a_col + (uint32_t)hi_half * 32 + 16, v1);
+        } else {
+          tmem_st16(a_col + (uint32_t)hi_half * 16, v0);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        g_mbar_arrive(&full[sa]);
+      }
+    }
   }
+
   // MMAs in flight must finish before TMEM is freed: `done` is committed on
   // every path of the issuer
-  if (s_fail && warp == 0) (void)g_mbar_wait(&done, 0, nullptr);
+  if (warp == C::kMmaWarp && lane == 0) (void)g_mbar_wait(&done, 0, nullptr);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (s_fail && tid == 0 && j.err) atomicExch(j.err, 4);
-  if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+  if (warp == C::kMmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
 }
 
-template <int NMAT>
+template <int NMAT, int DQG>
 cudaError_t launch_gemm_t(const GemmMaps &maps, const RawMaps &raw, const GemmJob &j, int max_gunits,
                           cudaStream_t st) {
+  using C = GemmCfg<NMAT, DQG>;
   if (max_gunits <= 0) return cudaSuccess;
   if (j.nb % 2) return cudaErrorInvalidValue;
-  const size_t smem = gemm_smem_bytes<NMAT>();
   static DynSmemLimit cur;
-  const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT>, smem, cur);
+  const cudaError_t e = ensure_dyn_smem(umma_gemm_kernel<NMAT, DQG>, C::kSmem, cur);
   if (e != cudaSuccess) return e;
-  dim3 grid((j.R + kGemmM - 1) / kGemmM, max_gunits);
-  umma_gemm_kernel<NMAT><<<grid, kGemmThreads, smem, st>>>(maps, raw, j);
+  int dev = 0, n_sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n_sms <= 0)
+    return cudaErrorInvalidValue;
+  const long tiles = (long)max_gunits * ((j.R + kGemmM - 1) / kGemmM);
+  const int grid = (int)std::min<long>(tiles, n_sms);
+  umma_gemm_kernel<NMAT, DQG><<<grid, C::kThreads, C::kSmem, st>>>(maps, raw, j);
   return cudaGetLastError();
 }
 
@@ -587,7 +727,7 @@ cudaError_t launch_gemm_gateup(const FfnArgs &a, const GemmMaps &xs_maps, const 
   j.R = a.F;
   j.nb = a.H / 32;
   j.h16s = h16s;
-  return launch_gemm_t<2>(xs_maps, raw, j, max_gunits, st);
+  return launch_gemm_t<2, kGemmDqg>(xs_maps, raw, j, max_gunits, st);
 }
 
 cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const RawMaps &raw, int slot0,
@@ -599,7 +739,7 @@ cudaError_t launch_gemm_down(const FfnArgs &a, const GemmMaps &h16s_maps, const 
   j.R = a.H;
   j.nb = a.F / 32;
   j.y = a.y;
-  return launch_gemm_t<1>(h16s_maps, raw, j, max_gunits, st);
+  return launch_gemm_t<1, kGemmDqg>(h16s_maps, raw, j, max_gunits, st);
 }
 
 }  // namespace moe
