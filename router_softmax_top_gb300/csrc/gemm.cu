@@ -283,7 +283,11 @@ struct GemmCfg {
   static constexpr int kDqWarps = 8 * DQG;
   static constexpr int kEpiWarp0 = kDqWarps;           // 4 epilogue warps; warp w reads TMEM lanes 32 (w % 4) ..
   static constexpr int kMmaWarp = kDqWarps + 4, kRawWarp = kDqWarps + 5, kBWarp = kDqWarps + 6;
-  static constexpr int kThreads = 32 * (kDqWarps + 7);
+  // one MMA-issuing thread per matrix: issuing a tcgen05.mma costs its thread
+  // ~85 cycles whatever N is, so gate and up are issued from two warps
+  static constexpr int kIssuers = NMAT;
+  static constexpr int kMmaWarp2 = kDqWarps + 7;       // issues the up matrix (gate/up only)
+  static constexpr int kThreads = 32 * (kDqWarps + 7 + (NMAT == 2 ? 1 : 0));
   static constexpr size_t kRawStage = raw_stage_bytes<NMAT>();
   static constexpr size_t kSmem = kB * kBTileBytes + kRaw * kRawStage + 1024;
   static_assert(kEpiWarp0 % 4 == 0, "epilogue warps must start at a multiple of 4");
@@ -330,17 +334,17 @@ __global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < C::kA; ++s) {
       g_mbar_init(&full[s], kDqThreads + 1);
-      g_mbar_init(&empty[s], 1);
+      g_mbar_init(&empty[s], C::kIssuers);
     }
     for (int s = 0; s < C::kRaw; ++s) {
       g_mbar_init(&rfull[s], 1);
       g_mbar_init(&rempty[s], kDqThreads);
     }
     for (int b = 0; b < C::kAccBufs; ++b) {
-      g_mbar_init(&accfull[b], 1);
+      g_mbar_init(&accfull[b], C::kIssuers);
       g_mbar_init(&accempty[b], 128);
     }
-    g_mbar_init(&done, 1);
+    g_mbar_init(&done, C::kIssuers);
     s_fail = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -424,10 +428,13 @@ __global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
       // barriers complete once their bytes (and dequantised halves) are in
       drain_ring(full, C::kB, g);
     }
-  } else if (warp == C::kMmaWarp) {
-    // ---- MMA issuer: tile i into accumulator buffer i % kAccBufs, once the
-    // epilogue has drained the tile that used it before (i - kAccBufs)
+  } else if (warp == C::kMmaWarp || (NMAT == 2 && warp == C::kMmaWarp2)) {
+    // ---- MMA issuers (gate/up: one per matrix): tile i into accumulator buffer
+    // i % kAccBufs, once the epilogue has drained the tile that used it before
+    // (i - kAccBufs); every issuer commits each stage and each tile, so the
+    // barriers complete once both matrices' MMAs have
     if (lane == 0) {
+      const int m = (NMAT == 2 && warp == C::kMmaWarp2) ? 1 : 0;
       int g = 0;
       bool stop = false;
       for (int i = 0; i < n_my && !stop; ++i) {
@@ -441,24 +448,20 @@ __global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t dcol = tmem + (uint32_t)buf * C::kAccCols;
+        const uint32_t dcol = tmem + (uint32_t)buf * C::kAccCols + (uint32_t)(m * kGemmN);
         for (int c = 0; c < n_chunks; ++c, ++g) {
-          const int sa = g % C::kA, sb = sa;
+          const int sa = g % C::kA;
           if (!g_mbar_wait(&full[sa], (uint32_t)(g / C::kA) & 1u, &s_fail)) {
             s_fail = 1;
             stop = true;
             break;
           }
           asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          const uint32_t b_addr = gsa(sb_base + (size_t)sb * kBTileBytes);
-          const uint32_t a_col = tmem + kTmemA0 + (uint32_t)sa * C::kAStageCols;
+          const uint64_t bd = sw128_desc(gsa(sb_base + (size_t)sa * kBTileBytes));
+          const uint32_t a_col = tmem + kTmemA0 + (uint32_t)sa * C::kAStageCols + (uint32_t)(m * 32);
 #pragma unroll
-          for (int m = 0; m < NMAT; ++m) {
-#pragma unroll
-            for (int ks = 0; ks < kGemmK / 16; ++ks)
-              umma_ts(dcol + (uint32_t)(m * kGemmN), a_col + (uint32_t)(m * 32 + ks * 8),
-                      sw128_desc(b_addr + ks * 32), idesc, (c > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < kGemmK / 16; ++ks)
+            umma_ts(dcol, a_col + (uint32_t)(ks * 8), bd + (uint64_t)(ks * 2), idesc, (c > 0 || ks > 0) ? 1u : 0u);
           umma_commit(&empty[sa]);
         }
         if (!stop) umma_commit(&accfull[buf]);
@@ -570,7 +573,8 @@ __global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
 
   // MMAs in flight must finish before TMEM is freed: `done` is committed on
   // every path of the issuer
-  if (warp == C::kMmaWarp && lane == 0) (void)g_mbar_wait(&done, 0, nullptr);
+  if ((warp == C::kMmaWarp || (NMAT == 2 && warp == C::kMmaWarp2)) && lane == 0)
+    (void)g_mbar_wait(&done, 0, nullptr);
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (s_fail && tid == 0 && j.err) atomicExch(j.err, 4);
