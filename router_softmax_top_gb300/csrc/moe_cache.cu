@@ -102,6 +102,7 @@ struct moe_cache {
   uint32_t seq = 0;
 
   cudaStream_t side = nullptr;
+  cudaStream_t side2 = nullptr;  // memcpy fill through the decode layer kernel: every second missed block
   cudaEvent_t ev_plan = nullptr;
   std::vector<cudaEvent_t> ev_up, ev_done;
 
@@ -280,6 +281,7 @@ void free_all(moe_cache *c) {
   if (c->h_mail_raw) cudaFreeHost(c->h_mail_raw);
   if (c->h_err) cudaFreeHost(c->h_err);
   if (c->side) cudaStreamDestroy(c->side);
+  if (c->side2) cudaStreamDestroy(c->side2);
   if (c->ev_plan) cudaEventDestroy(c->ev_plan);
   for (auto e : c->ev_up) cudaEventDestroy(e);
   for (auto e : c->ev_done) cudaEventDestroy(e);
@@ -498,6 +500,8 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   int prio_lo = 0, prio_hi = 0;
   if (cudaDeviceGetStreamPriorityRange(&prio_lo, &prio_hi) != cudaSuccess ||
       cudaStreamCreateWithPriority(&c->side, cudaStreamNonBlocking, prio_hi) != cudaSuccess ||
+      (cfg->fill_mode == MOE_FILL_MEMCPY &&
+       cudaStreamCreateWithPriority(&c->side2, cudaStreamNonBlocking, prio_hi) != cudaSuccess) ||
       cudaEventCreateWithFlags(&c->ev_fin, cudaEventDisableTiming) != cudaSuccess)
     return fail(MOE_ERR_CUDA);
   if (cudaEventCreateWithFlags(&c->ev_plan, cudaEventDisableTiming) != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -793,15 +797,20 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     if (hdr.error) return poison(c, MOE_ERR_INVALID_ARG);
     if (hdr.n_stages != 1 || hdr.n_miss > c->staging_blocks) return poison(c, MOE_ERR_CUDA);
     if (hdr.n_miss > 0) {
-      if (cudaStreamWaitEvent(c->side, c->ev_plan, 0) != cudaSuccess) return poison(c, MOE_ERR_CUDA);
+      // the missed blocks alternate between two side streams, so that a block's
+      // copy does not queue behind the previous block's ready-word write
+      if (cudaStreamWaitEvent(c->side, c->ev_plan, 0) != cudaSuccess ||
+          (hdr.n_miss > 1 && cudaStreamWaitEvent(c->side2, c->ev_plan, 0) != cudaSuccess))
+        return poison(c, MOE_ERR_CUDA);
       Launch l(c, K_MEMCPY, c->side);
       const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) + (size_t)layer * c->store.layer_stride;
       for (int i = 0; i < hdr.n_miss; ++i) {
         const MissItem m = c->h_mail_miss[i];
         if (m.expert < 0 || m.expert >= E) return poison(c, MOE_ERR_CUDA);
+        cudaStream_t cs = (i & 1) ? c->side2 : c->side;
         if (fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
-                      lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes, c->side) != cudaSuccess ||
-            c->write_value32(reinterpret_cast<CUstream>(c->side),
+                      lbase + (size_t)m.expert * c->store.expert_stride, c->expert_bytes, cs) != cudaSuccess ||
+            c->write_value32(reinterpret_cast<CUstream>(cs),
                              reinterpret_cast<CUdeviceptr>(c->d_miss_ready + i), hdr.epoch, 0) != CUDA_SUCCESS)
           return poison(c, MOE_ERR_CUDA);
       }
@@ -920,6 +929,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
     if (cs == cudaStreamCaptureStatusNone) {
       int rc = wait_stream(st, g.timeout_us);
       if (rc == MOE_OK) rc = wait_stream(c->side, g.timeout_us);
+      if (rc == MOE_OK && c->side2) rc = wait_stream(c->side2, g.timeout_us);
       if (rc != MOE_OK) return poison(c, rc);
       if (const int de = device_error_code(c)) return poison(c, de);
       PlanHdr h;
@@ -948,6 +958,7 @@ MOE_API int moe_cache_sync(moe_cache *c, void *cuda_stream) {
   if (!c) return MOE_ERR_INVALID_ARG;
   int rc = wait_stream((cudaStream_t)cuda_stream, c->cfg.timeout_us);
   if (rc == MOE_OK) rc = wait_stream(c->side, c->cfg.timeout_us);
+  if (rc == MOE_OK && c->side2) rc = wait_stream(c->side2, c->cfg.timeout_us);
   if (rc != MOE_OK) return poison(c, rc);
   if (const int de = device_error_code(c)) return poison(c, de);
   return c->poisoned ? c->last_error : MOE_OK;
