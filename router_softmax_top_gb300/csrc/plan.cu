@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int E = a.E, S = a.S, k = a.k, T = a.T;
   const int P = T * k;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
 
   // ---- shared memory carve-up (sizes mirrored in plan_smem_bytes)
   unsigned char *sp = smem_raw;
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   int *M = take(E), *new_es = take(E), *item_of = take(E), *gitm = take(E + 1);
   int *se0 = take(S), *vpos = take(S), *occ0 = take(S), *touched = take(S), *victim = take(S);
   int *qpos = take(S), *qslot = take(S);  // later-stage slots: position of a slot, slot of a position
-  int *wcnt = take(NW * E);
+  int *vclass = take(S);  // stage-0 victim class of a slot: -1 not a victim, 0 empty, 1 evictable
   int *ws = take(NW + 2);
   int *scal = take(8);  // 0 bad, 1 pick hits, 2 evictions
 
@@ -240,7 +240,6 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     e_slot[e] = -1;
     e_stage[e] = -1;
   }
-  for (int i = tid; i < NW * E; i += NT) wcnt[i] = 0;
   for (int i = tid; i < a.sync_n; i += NT) a.sync[i] = 0;
   if (tid < 8) scal[tid] = 0;
   const unsigned long long now = *a.clock + 1ull;
@@ -317,15 +316,18 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   }
   for (int i = tid; i < S; i += NT) {
     const int ei = se0[i];
+    vclass[i] = ei < 0 ? 0 : (cnt[ei] == 0 ? 1 : -1);
+  }
+  __syncthreads();
+  for (int i = tid; i < S; i += NT) {
+    const int cli = vclass[i];
     int rank = -1;
-    if (ei < 0 || cnt[ei] == 0) {
+    if (cli >= 0) {
       rank = 0;
-      const int cli = ei < 0 ? 0 : 1;
       const unsigned long long ti = cli ? stamp0[i] : 0ull;
       for (int j = 0; j < S; ++j) {
-        const int ej = se0[j];
-        if (j == i || !(ej < 0 || cnt[ej] == 0)) continue;
-        const int clj = ej < 0 ? 0 : 1;
+        const int clj = vclass[j];
+        if (clj < 0 || j == i) continue;
         const unsigned long long tj = clj ? stamp0[j] : 0ull;
         rank += (clj < cli) || (clj == cli && (tj < ti || (tj == ti && j < i)));
       }
@@ -399,10 +401,19 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
 
   // ---- G. per-pair slot/stage, new expert->slot table, item sizes
   for (int e = tid; e < E; e += NT) a.expert_slot[e] = new_es[e];
-  for (int p = tid; p < P; p += NT) {
-    const int e = a.ids[p];
-    a.gpu_slot[p] = e_slot[e];
-    a.stage[p] = e_stage[e];
+  // the pairs' ids loaded four at a time before their stores, so the loads
+  // are in flight together
+  for (int p0 = tid; p0 < P; p0 += 4 * NT) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ev[u] = p0 + u * NT < P ? a.ids[p0 + u * NT] : 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (p0 + u * NT < P) {
+        a.gpu_slot[p0 + u * NT] = e_slot[ev[u]];
+        a.stage[p0 + u * NT] = e_stage[ev[u]];
+      }
+    }
   }
   for (int e = tid; e < E; e += NT) {
     const int it = item_of[e];
@@ -422,7 +433,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   if (tid == 0) gitm[nU] = n_gunits;
   __syncthreads();
 
-  // ---- H. items, units, stage ranges; perm = stable counting sort by item
+  // ---- H. items, units, stage ranges; perm = the pairs grouped by item
   for (int e = tid; e < E; e += NT) {
     const int it = item_of[e];
     if (it < 0) continue;
@@ -462,44 +473,22 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
   const int hit_units = (int)(itm[nH] >> 32);
   const int hit_gunits = gitm[nH];
 
-  const int chunk = (P + NW - 1) / NW;
-  const int c0 = warp * chunk, c1 = min(P, c0 + chunk);
-  for (int base = c0; base < c1; base += 32) {
-    const int p = base + lane;
-    const bool act = p < c1;
-    const unsigned am = __ballot_sync(0xffffffffu, act);
-    if (act) {
-      const int e = a.ids[p];
-      const unsigned m = __match_any_sync(am, e);
-      if ((__ffs(m) - 1) == lane) wcnt[warp * E + e] += __popc(m);
-    }
-    __syncwarp();
-  }
-  __syncthreads();
+  // perm: each item's pairs in its range [pair_begin, pair_begin + count), in
+  // an unspecified order (shared-memory counters): a pair's arithmetic does
+  // not depend on its position among its item's pairs, so no stable sort is
+  // needed (the outputs are the same bits in any order)
   for (int e = tid; e < E; e += NT) {
     const int it = item_of[e];
-    if (it < 0) continue;
-    int run = (int)(itm[it] & 0xFFFFFFFFll);
-    for (int w2 = 0; w2 < NW; ++w2) {
-      const int c = wcnt[w2 * E + e];
-      wcnt[w2 * E + e] = run;
-      run += c;
-    }
+    if (it >= 0) cnt[e] = (int)(itm[it] & 0xFFFFFFFFll);  // cnt is free after H: the fill position
   }
   __syncthreads();
-  for (int base = c0; base < c1; base += 32) {
-    const int p = base + lane;
-    const bool act = p < c1;
-    const unsigned am = __ballot_sync(0xffffffffu, act);
-    if (act) {
-      const int e = a.ids[p];
-      const unsigned m = __match_any_sync(am, e);
-      const int rank = __popc(m & ((1u << lane) - 1u));
-      a.perm[wcnt[warp * E + e] + rank] = p;
-      __syncwarp(m);
-      if ((__ffs(m) - 1) == lane) wcnt[warp * E + e] += __popc(m);
-    }
-    __syncwarp();
+  for (int p0 = tid; p0 < P; p0 += 4 * NT) {
+    int ev[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) ev[u] = p0 + u * NT < P ? a.ids[p0 + u * NT] : 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (p0 + u * NT < P) a.perm[atomicAdd(&cnt[ev[u]], 1)] = p0 + u * NT;
   }
 
   // ---- I. header, stats, clock, mailbox
@@ -559,7 +548,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
 // code: this kernel runs once per layer call, mostly from a cold instruction
 // cache).
 constexpr int kSmallMaxSlots = 256;
-constexpr int kRouteGridMin = 64;  // calls with more tokens route in their own grid
+constexpr int kRouteGridMin = 8;  // calls with more tokens route in their own grid (one warp per token)
 
 // POLICY: MOE_POLICY_LRU (0) or MOE_POLICY_SCORE (1); the LRU instance carries
 // none of the score code or its shared memory.
@@ -917,8 +906,8 @@ size_t plan_smem_bytes(int E, int S) {
   auto r4 = [](size_t n) { return 4 * ((n + 3) / 4 * 4); };
   size_t b = r8(S) + r8(E + 1) + r8(NW + 2);
   b += 8 * r4(E) + r4(E + 1);
-  b += 7 * r4(S);
-  b += r4((size_t)NW * E) + r4(NW + 2) + r4(8);
+  b += 8 * r4(S);
+  b += r4(NW + 2) + r4(8);
   return b + 64;
 }
 
