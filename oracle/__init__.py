@@ -82,6 +82,9 @@ def lib() -> ctypes.CDLL:
             L.orc_cache_lru.argtypes = [vp, i32]
             L.orc_cache_stats.argtypes = [vp, i32, vp]
             L.orc_cache_preload.argtypes = [vp, vp]
+            L.orc_cache_usage.argtypes = [vp, vp]
+            L.orc_cache_set_state.restype = i32
+            L.orc_cache_set_state.argtypes = [vp, i32, vp, vp, u64, vp, vp]
             L.orc_layer_forward.restype = i32
             L.orc_layer_forward.argtypes = [vp, i32, vp, vp, i32, i32, i32, vp,
                                             vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -234,6 +237,27 @@ class Cache:
         c = np.ascontiguousarray(counts, dtype=np.uint32)
         assert c.shape == (self.L, self.E)
         lib().orc_cache_preload(self._h, _p(c))
+
+    def usage(self) -> np.ndarray:
+        """Lifetime activation counts [L, E] (u32): one per routed (token, pick) of every accepted call."""
+        out = np.empty((self.L, self.E), np.uint32)
+        lib().orc_cache_usage(self._h, _p(out))
+        return out
+
+    def state(self, layer: int) -> dict:
+        """One layer's resumable state: slot_expert, slot_stamp, clock, score (fp32), usage (u32)."""
+        st = self.lru(layer).state()
+        return {"slot_expert": st["slot_expert"], "slot_stamp": st["slot_stamp"], "clock": st["clock"],
+                "score": self.lru(layer).scores(), "usage": self.usage()[layer].copy()}
+
+    def set_state(self, layer: int, slot_expert, slot_stamp, clock: int, score, usage) -> bool:
+        """Resume one layer from a saved state; False (state untouched) when the tables are invalid."""
+        se = np.ascontiguousarray(slot_expert, dtype=np.int32)
+        ss = np.ascontiguousarray(slot_stamp, dtype=np.uint64)
+        sc = np.ascontiguousarray(score, dtype=np.float32)
+        us = np.ascontiguousarray(usage, dtype=np.uint32)
+        assert se.shape == (self.S,) and ss.shape == (self.S,) and sc.shape == (self.E,) and us.shape == (self.E,)
+        return lib().orc_cache_set_state(self._h, layer, _p(se), _p(ss), int(clock), _p(sc), _p(us)) == 0
 
     def forward(self, layer: int, logits: np.ndarray, x: np.ndarray | None, compute: bool = True):
         lg = np.ascontiguousarray(logits, dtype=np.float32)

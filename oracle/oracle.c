@@ -36,7 +36,8 @@
  *    ("llama.cpp + MoE expert cache", "Keeping the cache fresh") and its sticky
  *    share; adopt, a staged call ending with its most-used experts ("llama.cpp:
  *    fork with multi gpu acceleration ...", "Prefill preheat"); warm start from
- *    usage counts (same page, "Persistent hot experts").
+ *    usage counts (same page, "Persistent hot experts"), the lifetime activation
+ *    counts such a profile holds, and resuming a saved slot-table state.
  *
  * Parity pins live in tests/test_oracle_*.py (hand-worked Q4_0 blocks, exact
  * integer GEMV cases, brute-force router, independent brute-force simulators of
@@ -616,6 +617,7 @@ typedef struct {
     orc_lru **lru;                 /* [L] */
     const uint8_t **slot_src;      /* [L*S] the store block each simulated slot holds */
     uint64_t *stats;               /* [L*ORC_NSTAT] */
+    uint32_t *usage;               /* [L*E] lifetime activation counts */
     int n_threads;
 } orc_cache;
 
@@ -635,6 +637,7 @@ orc_cache *orc_cache_new(int L, int E, int k, int H, int F, int S, int weight_mo
     }
     c->slot_src = (const uint8_t **)calloc((size_t)L * S, sizeof(uint8_t *));
     c->stats = (uint64_t *)calloc((size_t)L * ORC_NSTAT, sizeof(uint64_t));
+    c->usage = (uint32_t *)calloc((size_t)L * E, sizeof(uint32_t));
     c->n_threads = n_threads;
     return c;
 }
@@ -645,6 +648,7 @@ void orc_cache_free(orc_cache *c) {
     free(c->lru);
     free(c->slot_src);
     free(c->stats);
+    free(c->usage);
     free(c);
 }
 
@@ -692,6 +696,56 @@ void orc_cache_preload(orc_cache *c, const uint32_t *counts) {
         }
         free(order);
     }
+}
+
+/*
+ * Lifetime activation counts ("Persistent hot experts": the cache keeps how
+ * often each expert was used, n_layer x n_expert u32, and saves them at
+ * shutdown for the next start's preload).  Reading taken: one count per routed
+ * (token, pick) pair of every accepted call, whatever its slot outcome (hit,
+ * miss, bypass), added when the call is planned; a rejected call (non-finite
+ * logit, policy 1 over one stage) counts nothing; u32 arithmetic wraps.
+ * out[L][E].
+ */
+void orc_cache_usage(const orc_cache *c, uint32_t *out) {
+    memcpy(out, c->usage, sizeof(uint32_t) * (size_t)c->L * c->E);
+}
+
+/*
+ * Resume from a saved state (the page saves usage counts only; restoring the
+ * slot tables themselves is this library's addition): layer `layer` takes
+ * slot_expert[S] (-1 = empty), slot_stamp[S], clock, score[E] (policy 1) and
+ * usage[E]; expert_slot is derived and each occupied slot holds its expert's
+ * block of the store.  Returns -1, state untouched, when an expert id is out of
+ * [-1, E), an expert sits in two slots, an occupied slot's stamp is above the
+ * clock, or a score is negative or not finite; else 0.
+ */
+int orc_cache_set_state(orc_cache *c, int layer, const int32_t *slot_expert, const uint64_t *slot_stamp,
+                        uint64_t clock, const float *score, const uint32_t *usage) {
+    const int S = c->S, E = c->E;
+    orc_lru *st = c->lru[layer];
+    for (int sl = 0; sl < S; ++sl) {
+        int32_t e = slot_expert[sl];
+        if (e < -1 || e >= E) return -1;
+        if (e >= 0 && slot_stamp[sl] > clock) return -1;
+        for (int s2 = 0; s2 < sl; ++s2)
+            if (e >= 0 && slot_expert[s2] == e) return -1;
+    }
+    for (int e = 0; e < E; ++e)
+        if (!(score[e] >= 0.0f) || isinf(score[e])) return -1;
+    for (int e = 0; e < E; ++e) st->expert_slot[e] = -1;
+    for (int sl = 0; sl < S; ++sl) {
+        int32_t e = slot_expert[sl];
+        st->slot_expert[sl] = e;
+        st->slot_stamp[sl] = slot_stamp[sl];
+        if (e >= 0) st->expert_slot[e] = sl;
+        c->slot_src[(size_t)layer * S + sl] =
+            e >= 0 ? c->store + (size_t)layer * c->layer_stride + (size_t)e * c->expert_stride : NULL;
+    }
+    st->clock = clock;
+    memcpy(st->score, score, sizeof(float) * E);
+    memcpy(c->usage + (size_t)layer * E, usage, sizeof(uint32_t) * E);
+    return 0;
 }
 
 void orc_cache_stats(const orc_cache *c, int layer, uint64_t *out) {
@@ -746,6 +800,7 @@ int orc_layer_forward(orc_cache *c, int layer, const float *logits, const void *
     st[ORC_STAT_STAGES] += (uint64_t)info.n_stages;
     st[ORC_STAT_STAGED_CALLS] += info.n_stages > 1 ? 1u : 0u;
     st[ORC_STAT_BYPASSED] += (uint64_t)info.n_bypass;
+    for (long p = 0; p < P; ++p) c->usage[(size_t)layer * E + ids[p]] += 1u;
 
     int32_t *visits = (int32_t *)calloc((size_t)P, sizeof(int32_t));
     const uint8_t **slot_src = c->slot_src + (size_t)layer * S;
