@@ -239,6 +239,72 @@ int moe_layer_last_plan(const moe_cache *c, int32_t layer, int32_t *ids, float *
 int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream);
 
 /*
+ * Lifetime activation counts ("llama.cpp: fork with multi gpu acceleration
+ * ...", "Persistent hot experts": the cache keeps how often each expert was
+ * used, an n_layer x n_expert u32 array, saves it at shutdown and preloads the
+ * most-used experts at the next start).  counts: host array
+ * [n_layers][n_experts]; counts[l][e] = routed (token, pick) pairs of expert e
+ * in layer l over every accepted forward call since init (or since the state
+ * the handle was loaded from), whatever their slot outcome (hit, miss,
+ * bypass); u32, wrapping.  The array is a valid `counts` for
+ * moe_cache_preload.  Synchronises with the device; readable on a poisoned
+ * handle.  NULL handle or counts: MOE_ERR_INVALID_ARG.
+ */
+int moe_cache_usage(const moe_cache *c, uint32_t *counts);
+
+/*
+ * Saved cache state.  The pages persist usage counts only; resuming the slot
+ * tables themselves has no counterpart there: a handle that loads a state
+ * plans its next calls exactly as the saved handle would have.  Layout, host
+ * byte order, L = n_layers, S = slots_per_layer, E = n_experts:
+ *   moe_cache_state_header          48 bytes
+ *   uint64_t clock[L]               calls planned per layer
+ *   uint64_t slot_stamp[L][S]       each slot's last use, a value of its clock
+ *   int32_t  slot_expert[L][S]      expert held by each slot, -1 = empty
+ *   float    score[L][E]            decayed usage scores (MOE_POLICY_SCORE)
+ *   uint32_t usage[L][E]            lifetime activation counts
+ * Slot contents are not saved: loading copies each held expert's block from
+ * the handle's host store into its slot.
+ */
+#define MOE_STATE_MAGIC 0x53454F4Du /* "MOES" */
+#define MOE_STATE_VERSION 1u
+typedef struct {
+  uint32_t magic, version;
+  int32_t n_layers, n_experts, slots_per_layer;
+  int32_t policy;         /* the saving handle's policy (not checked on load) */
+  uint64_t expert_bytes;  /* bytes of one expert block (checked on load) */
+  uint64_t total_bytes;   /* header + arrays */
+  uint64_t reserved;      /* 0 */
+} moe_cache_state_header;
+
+/* Bytes of this handle's saved state.  NULL argument: MOE_ERR_INVALID_ARG. */
+int moe_cache_state_size(const moe_cache *c, uint64_t *bytes);
+
+/*
+ * Writes the state into buf (host, cap bytes).  Includes every call issued
+ * before it (synchronises with the device).  cap below moe_cache_state_size:
+ * MOE_ERR_INVALID_ARG, nothing written; a poisoned handle: MOE_ERR_POISONED
+ * (a failed call may have left the tables half-updated).
+ */
+int moe_cache_save_state(const moe_cache *c, void *buf, uint64_t cap);
+
+/*
+ * Replaces every layer's slot table, stamps, clock, scores and usage counts by
+ * a saved state (host buf, size bytes) and fills the held slots from the host
+ * store.  Stream-ordered on cuda_stream, between calls as for
+ * moe_cache_preload, and synchronises with it before returning; statistics
+ * and the call counter do not change.  Rejected with MOE_ERR_INVALID_ARG, the
+ * handle unchanged: wrong magic, version or size; another shape (layers,
+ * experts, slots, expert bytes); an expert id outside [-1, E) or one expert in
+ * two slots of a layer; an occupied slot stamped after its layer's clock; a
+ * clock of 2^48 or more (the decode plan orders slots by stamps packed below
+ * 2^51; a handle reaches such a clock only after 2^48 calls of one layer); a
+ * negative or non-finite score.  A poisoned handle: MOE_ERR_POISONED.  CUDA
+ * failures while filling poison the handle (MOE_ERR_CUDA).
+ */
+int moe_cache_load_state(moe_cache *c, const void *buf, uint64_t size, void *cuda_stream);
+
+/*
  * Debug runs: with MOE_CHECK_PLANS=1 in the environment when a handle is
  * created, every forward call on it waits for its own completion (not while
  * the stream is being captured) and checks on the host that its plan and the

@@ -41,7 +41,11 @@ EXPORTS = ("moe_cache_init", "moe_layer_forward", "moe_cache_sync", "moe_cache_s
            "moe_layer_last_plan", "moe_cache_preload", "moe_cache_inject", "moe_cache_set_timing",
            "moe_cache_timing",
            "moe_cache_probe_h2d", "moe_expert_bytes", "moe_cache_launch_count",
-           "moe_cache_destroy", "moe_strerror", "moe_expert_ffn_static")
+           "moe_cache_destroy", "moe_strerror", "moe_expert_ffn_static", "moe_cache_usage",
+           "moe_cache_state_size", "moe_cache_save_state", "moe_cache_load_state")
+
+MOE_STATE_MAGIC = 0x53454F4D
+MOE_STATE_VERSION = 1
 
 
 class MoeCacheConfig(ctypes.Structure):
@@ -71,6 +75,14 @@ class MoeCacheStats(ctypes.Structure):
 
     def as_dict(self):
         return {f: int(getattr(self, f)) for f, _ in self._fields_}
+
+
+class MoeStateHeader(ctypes.Structure):
+    """moe_cache_state_header: the first 48 bytes of a saved state."""
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("n_layers", ctypes.c_int32),
+                ("n_experts", ctypes.c_int32), ("slots_per_layer", ctypes.c_int32), ("policy", ctypes.c_int32),
+                ("expert_bytes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
+                ("reserved", ctypes.c_uint64)]
 
 
 class MoeError(RuntimeError):
@@ -111,6 +123,10 @@ def lib() -> ctypes.CDLL:
         L.moe_cache_preload.argtypes = [vp, vp, vp]
         L.moe_cache_inject.restype = ctypes.c_int
         L.moe_cache_inject.argtypes = [vp, i32]
+        L.moe_cache_usage.argtypes = [vp, vp]
+        L.moe_cache_state_size.argtypes = [vp, ctypes.POINTER(u64)]
+        L.moe_cache_save_state.argtypes = [vp, vp, u64]
+        L.moe_cache_load_state.argtypes = [vp, vp, u64, vp]
         L.moe_cache_probe_h2d.restype = ctypes.c_int
         L.moe_cache_probe_h2d.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_double)]
         L.moe_expert_bytes.restype = u64
@@ -286,6 +302,33 @@ class MoECache:
             stream = torch.cuda.current_stream().cuda_stream
         _check(lib().moe_cache_preload(self.handle, ctypes.c_void_p(c.ctypes.data), ctypes.c_void_p(stream)),
                "moe_cache_preload")
+
+    def usage(self):
+        """Lifetime activation counts [L, E] u32 (moe_cache_usage)."""
+        import numpy as np
+        out = np.empty((self.L, self.E), np.uint32)
+        _check(lib().moe_cache_usage(self.handle, ctypes.c_void_p(out.ctypes.data)), "moe_cache_usage")
+        return out
+
+    def save_state(self) -> bytes:
+        """The handle's slot tables, stamps, clocks, scores and usage (moe_cache_save_state)."""
+        n = ctypes.c_uint64(0)
+        _check(lib().moe_cache_state_size(self.handle, ctypes.byref(n)), "moe_cache_state_size")
+        buf = ctypes.create_string_buffer(n.value)
+        _check(lib().moe_cache_save_state(self.handle, buf, n.value), "moe_cache_save_state")
+        return buf.raw
+
+    def load_state_rc(self, state: bytes, stream=None) -> int:
+        """moe_cache_load_state; returns its code."""
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream().cuda_stream
+        buf = ctypes.create_string_buffer(bytes(state), len(state))
+        return lib().moe_cache_load_state(self.handle, buf, len(state), ctypes.c_void_p(stream))
+
+    def load_state(self, state: bytes, stream=None):
+        """Resume a saved state (moe_cache_load_state)."""
+        _check(self.load_state_rc(state, stream), "moe_cache_load_state")
 
     def inject(self, what: int):
         """Test hook: fault injection without a GPU fault (moe_cache_inject)."""

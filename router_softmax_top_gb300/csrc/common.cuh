@@ -154,6 +154,7 @@ struct PlanArgs {
   uint64_t *slot_stamp;  // [S]
   uint64_t *clock;       // [1]
   uint64_t *stats;       // [kNStat]
+  uint32_t *usage;       // [E] lifetime activation counts: + picks per expert of every accepted call
   uint64_t expert_bytes;
   // per-call outputs
   int32_t *ids;       // [T*k]

@@ -18,6 +18,7 @@
 #include <chrono>
 #include <cstdio>
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -61,6 +62,7 @@ struct moe_cache {
   int32_t *d_slot_expert = nullptr, *d_expert_slot = nullptr;
   uint64_t *d_slot_stamp = nullptr, *d_clock = nullptr, *d_stats = nullptr;
   float *d_score = nullptr;  // MOE_POLICY_SCORE: decayed usage per (layer, expert), fp32
+  uint32_t *d_usage = nullptr;  // lifetime activation counts per (layer, expert)
 
   // per-call scratch
   int32_t *d_ids = nullptr, *d_gpu_slot = nullptr, *d_stage = nullptr, *d_perm = nullptr;
@@ -255,6 +257,7 @@ void free_all(moe_cache *c) {
   cudaFree(c->d_clock);
   cudaFree(c->d_stats);
   cudaFree(c->d_score);
+  cudaFree(c->d_usage);
   cudaFree(c->d_ids);
   cudaFree(c->d_gpu_slot);
   cudaFree(c->d_stage);
@@ -411,6 +414,8 @@ MOE_API int moe_cache_init(const moe_cache_config *cfg, const moe_host_store *st
   ok = ok && dalloc(&c->d_stats, (size_t)L * kNStat) == cudaSuccess;
   ok = ok && dalloc(&c->d_score, (size_t)L * E) == cudaSuccess &&
        cudaMemset(c->d_score, 0, sizeof(float) * L * E) == cudaSuccess;
+  ok = ok && dalloc(&c->d_usage, (size_t)L * E) == cudaSuccess &&
+       cudaMemset(c->d_usage, 0, sizeof(uint32_t) * L * E) == cudaSuccess;
   ok = ok && dalloc(&c->d_ids, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_gpu_slot, c->maxP) == cudaSuccess;
   ok = ok && dalloc(&c->d_stage, c->maxP) == cudaSuccess;
@@ -588,6 +593,7 @@ MOE_API int moe_layer_forward(moe_cache *c, int32_t layer, const float *d_logits
   pa.policy = g.policy;
   pa.admit_budget = g.admit_budget;
   pa.score = c->d_score + (size_t)layer * E;
+  pa.usage = c->d_usage + (size_t)layer * E;
   pa.n_sticky = (int)((int64_t)g.sticky_permille * S / 1000);
   const bool use_decode = !need_host && g.fill_mode == MOE_FILL_PULL && decode_layer_supported(g.hidden, g.ffn, T);
   // memcpy fill, one stage guaranteed (distinct experts <= slots), few tokens:
@@ -1065,81 +1071,100 @@ MOE_API int moe_cache_timing(moe_cache *c, const char **names, uint64_t *launche
   return MOE_OK;
 }
 
+namespace {
+
+// Copies the blocks named by items (expert, slot) of layer l from the host
+// store into their slots: the fill kernel reads the mapped store, or each chunk
+// goes through staging when the store has no device mapping.  d_list holds S
+// items, d_h one header.  Stream-ordered on st; waits for st after each chunk
+// (the host lists are reused).  Returns MOE_OK or MOE_ERR_CUDA.
+int fill_layer_slots(moe_cache *c, int l, const std::vector<MissItem> &items, MissItem *d_list, PlanHdr *d_h,
+                     cudaStream_t st) {
+  const int S = c->cfg.slots_per_layer;
+  const int chunk = c->host_dev ? S : std::max(1, c->staging_blocks);
+  const int m = (int)items.size();
+  const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) + (size_t)l * c->store.layer_stride;
+  for (int lo = 0; lo < m; lo += chunk) {
+    const int n = std::min(chunk, m - lo);
+    PlanHdr h = {};
+    h.n_stages = 1;
+    h.n_stage0_miss = n;
+    h.n_miss = n;
+    h.stage_cap = S;
+    RepackArgs ra;
+    ra.slots = c->d_slots + (size_t)l * S * c->lay.stride;
+    ra.slot_stride = c->lay.stride;
+    ra.lay = c->lay;
+    ra.miss = d_list;
+    ra.hdr = d_h;
+    ra.stage = 0;
+    bool ok = cudaMemcpyAsync(d_list, items.data() + lo, sizeof(MissItem) * n, cudaMemcpyHostToDevice, st) ==
+                  cudaSuccess &&
+              cudaMemcpyAsync(d_h, &h, sizeof(PlanHdr), cudaMemcpyHostToDevice, st) == cudaSuccess;
+    if (c->host_dev) {
+      ra.src_base = c->host_dev;
+      ra.src_layer_off = (uint64_t)l * c->store.layer_stride;
+      ra.src_expert_stride = c->store.expert_stride;
+      ra.src_slot_stride = 0;
+      ra.by_expert = 1;
+    } else {
+      // staging block i holds the chunk's i-th item (the repack reads its
+      // source by list position and writes the item's slot)
+      for (int i = 0; ok && i < n; ++i)
+        ok = fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
+                       lbase + (size_t)items[lo + i].expert * c->store.expert_stride, c->expert_bytes, st) ==
+             cudaSuccess;
+      ra.src_base = c->d_staging;
+      ra.src_layer_off = 0;
+      ra.src_expert_stride = 0;
+      ra.src_slot_stride = c->expert_bytes;
+      ra.by_expert = 0;
+    }
+    ok = ok && launch_repack(ra, S, n, st) == cudaSuccess;
+    ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+    if (!ok) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+// Device lists for fill_layer_slots, freed with the object.
+struct FillLists {
+  MissItem *list = nullptr;
+  PlanHdr *hdr = nullptr;
+  bool alloc(int S) { return dalloc(&list, (size_t)S) == cudaSuccess && dalloc(&hdr, 1) == cudaSuccess; }
+  ~FillLists() {
+    cudaFree(list);
+    cudaFree(hdr);
+  }
+};
+
+}  // namespace
+
 MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_stream) {
   if (!c || !counts) return MOE_ERR_INVALID_ARG;
   if (c->poisoned) return MOE_ERR_POISONED;
   const int L = c->cfg.n_layers, E = c->cfg.n_experts, S = c->cfg.slots_per_layer;
   cudaStream_t st = (cudaStream_t)cuda_stream;
-  // the new state: per layer the S most-used experts, by (count desc, id asc)
+  // the new state: per layer the S most-used experts, by (count desc, id asc),
+  // in slots 0, 1, ...
   std::vector<int32_t> se((size_t)L * S, -1), es((size_t)L * E, -1);
-  std::vector<std::vector<int32_t>> chosen(L);
-  for (int l = 0; l < L; ++l) {
+  FillLists fl;
+  if (!fl.alloc(S)) return MOE_ERR_OOM;
+  int rc = MOE_OK;
+  for (int l = 0; l < L && rc == MOE_OK; ++l) {
     const uint32_t *cnt = counts + (size_t)l * E;
     std::vector<int32_t> order;
     for (int e = 0; e < E; ++e)
       if (cnt[e] > 0) order.push_back(e);
     std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cnt[x] > cnt[y]; });
     if ((int)order.size() > S) order.resize(S);
+    std::vector<MissItem> items;
     for (int i = 0; i < (int)order.size(); ++i) {
       se[(size_t)l * S + i] = order[i];
       es[(size_t)l * E + order[i]] = i;
+      items.push_back(MissItem{order[i], i, -1, 0});
     }
-    chosen[l] = std::move(order);
-  }
-  // contents: the blocks copied from the host store into their slots by the
-  // fill kernel (one stage of "misses" per layer; through staging, a chunk at
-  // a time, when the store has no device mapping)
-  MissItem *d_list = nullptr;
-  PlanHdr *d_h = nullptr;
-  if (dalloc(&d_list, (size_t)S) != cudaSuccess || dalloc(&d_h, 1) != cudaSuccess) {
-    cudaFree(d_list);
-    return MOE_ERR_OOM;
-  }
-  int rc = MOE_OK;
-  const int chunk = c->host_dev ? S : std::max(1, c->staging_blocks);
-  std::vector<MissItem> items(S);
-  for (int l = 0; l < L && rc == MOE_OK; ++l) {
-    const int m = (int)chosen[l].size();
-    for (int lo = 0; lo < m && rc == MOE_OK; lo += chunk) {
-      const int n = std::min(chunk, m - lo);
-      PlanHdr h = {};
-      h.n_stages = 1;
-      h.n_stage0_miss = n;
-      h.n_miss = n;
-      h.stage_cap = S;
-      for (int i = 0; i < n; ++i) items[i] = MissItem{chosen[l][lo + i], lo + i, -1, 0};
-      RepackArgs ra;
-      ra.slots = c->d_slots + (size_t)l * S * c->lay.stride;
-      ra.slot_stride = c->lay.stride;
-      ra.lay = c->lay;
-      ra.miss = d_list;
-      ra.hdr = d_h;
-      ra.stage = 0;
-      const uint8_t *lbase = static_cast<const uint8_t *>(c->store.base) + (size_t)l * c->store.layer_stride;
-      bool ok = cudaMemcpyAsync(d_list, items.data(), sizeof(MissItem) * n, cudaMemcpyHostToDevice, st) ==
-                    cudaSuccess &&
-                cudaMemcpyAsync(d_h, &h, sizeof(PlanHdr), cudaMemcpyHostToDevice, st) == cudaSuccess;
-      if (c->host_dev) {
-        ra.src_base = c->host_dev;
-        ra.src_layer_off = (uint64_t)l * c->store.layer_stride;
-        ra.src_expert_stride = c->store.expert_stride;
-        ra.src_slot_stride = 0;
-        ra.by_expert = 1;
-      } else {
-        for (int i = 0; ok && i < n; ++i)
-          ok = fill_copy(c, c->d_staging + (size_t)i * c->expert_bytes,
-                         lbase + (size_t)items[i].expert * c->store.expert_stride, c->expert_bytes, st) == cudaSuccess;
-        ra.src_base = c->d_staging;
-        ra.src_layer_off = 0;
-        ra.src_expert_stride = 0;
-        ra.src_slot_stride = c->expert_bytes;
-        ra.by_expert = 0;
-      }
-      ok = ok && launch_repack(ra, S, n, st) == cudaSuccess;
-      // the host copies of this chunk's lists are reused by the next one
-      ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
-      if (!ok) rc = MOE_ERR_CUDA;
-    }
+    rc = fill_layer_slots(c, l, items, fl.list, fl.hdr, st);
   }
   if (rc == MOE_OK &&
       (cudaMemcpyAsync(c->d_slot_expert, se.data(), sizeof(int32_t) * se.size(), cudaMemcpyHostToDevice, st) !=
@@ -1149,8 +1174,142 @@ MOE_API int moe_cache_preload(moe_cache *c, const uint32_t *counts, void *cuda_s
        cudaMemsetAsync(c->d_slot_stamp, 0, sizeof(uint64_t) * (size_t)L * S, st) != cudaSuccess ||
        cudaStreamSynchronize(st) != cudaSuccess))
     rc = MOE_ERR_CUDA;
-  cudaFree(d_list);
-  cudaFree(d_h);
+  if (rc != MOE_OK) {
+    cudaGetLastError();
+    return poison(c, rc);
+  }
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_usage(const moe_cache *cc, uint32_t *counts) {
+  moe_cache *c = const_cast<moe_cache *>(cc);
+  if (!c || !counts) return MOE_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    poison(c, MOE_ERR_CUDA);
+  }
+  if (cudaMemcpy(counts, c->d_usage, sizeof(uint32_t) * (size_t)c->cfg.n_layers * c->cfg.n_experts,
+                 cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  return MOE_OK;
+}
+
+namespace {
+
+// Byte offsets of the arrays of a saved state (see moe_cache_state_header).
+struct StateLayout {
+  uint64_t clock, stamp, expert, score, usage, total;
+  StateLayout(uint64_t L, uint64_t E, uint64_t S) {
+    clock = sizeof(moe_cache_state_header);
+    stamp = clock + 8 * L;
+    expert = stamp + 8 * L * S;
+    score = expert + 4 * L * S;
+    usage = score + 4 * L * E;
+    total = usage + 4 * L * E;
+  }
+};
+
+}  // namespace
+
+MOE_API int moe_cache_state_size(const moe_cache *c, uint64_t *bytes) {
+  if (!c || !bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = StateLayout(c->cfg.n_layers, c->cfg.n_experts, c->cfg.slots_per_layer).total;
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_save_state(const moe_cache *cc, void *buf, uint64_t cap) {
+  moe_cache *c = const_cast<moe_cache *>(cc);
+  if (!c || !buf) return MOE_ERR_INVALID_ARG;
+  const uint64_t L = c->cfg.n_layers, E = c->cfg.n_experts, S = c->cfg.slots_per_layer;
+  const StateLayout o(L, E, S);
+  if (cap < o.total) return MOE_ERR_INVALID_ARG;
+  if (c->poisoned) return MOE_ERR_POISONED;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  if (const int de = device_error_code(c)) return poison(c, de);
+  uint8_t *b = static_cast<uint8_t *>(buf);
+  moe_cache_state_header h = {};
+  h.magic = MOE_STATE_MAGIC;
+  h.version = MOE_STATE_VERSION;
+  h.n_layers = (int32_t)L;
+  h.n_experts = (int32_t)E;
+  h.slots_per_layer = (int32_t)S;
+  h.policy = c->cfg.policy;
+  h.expert_bytes = c->expert_bytes;
+  h.total_bytes = o.total;
+  std::memcpy(b, &h, sizeof(h));
+  const bool ok =
+      cudaMemcpy(b + o.clock, c->d_clock, 8 * L, cudaMemcpyDeviceToHost) == cudaSuccess &&
+      cudaMemcpy(b + o.stamp, c->d_slot_stamp, 8 * L * S, cudaMemcpyDeviceToHost) == cudaSuccess &&
+      cudaMemcpy(b + o.expert, c->d_slot_expert, 4 * L * S, cudaMemcpyDeviceToHost) == cudaSuccess &&
+      cudaMemcpy(b + o.score, c->d_score, 4 * L * E, cudaMemcpyDeviceToHost) == cudaSuccess &&
+      cudaMemcpy(b + o.usage, c->d_usage, 4 * L * E, cudaMemcpyDeviceToHost) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    return poison(c, MOE_ERR_CUDA);
+  }
+  return MOE_OK;
+}
+
+MOE_API int moe_cache_load_state(moe_cache *c, const void *buf, uint64_t size, void *cuda_stream) {
+  if (!c || !buf || size < sizeof(moe_cache_state_header)) return MOE_ERR_INVALID_ARG;
+  if (c->poisoned) return MOE_ERR_POISONED;
+  const int L = c->cfg.n_layers, E = c->cfg.n_experts, S = c->cfg.slots_per_layer;
+  const StateLayout o(L, E, S);
+  const uint8_t *b = static_cast<const uint8_t *>(buf);
+  moe_cache_state_header h;
+  std::memcpy(&h, b, sizeof(h));
+  if (h.magic != MOE_STATE_MAGIC || h.version != MOE_STATE_VERSION || h.n_layers != L || h.n_experts != E ||
+      h.slots_per_layer != S || h.expert_bytes != c->expert_bytes || h.total_bytes != o.total || size != o.total)
+    return MOE_ERR_INVALID_ARG;
+  // copies of the arrays (the buffer need not be aligned)
+  std::vector<uint64_t> clock(L), stamp((size_t)L * S);
+  std::vector<int32_t> se((size_t)L * S), es((size_t)L * E, -1);
+  std::vector<float> score((size_t)L * E);
+  std::vector<uint32_t> usage((size_t)L * E);
+  std::memcpy(clock.data(), b + o.clock, 8 * clock.size());
+  std::memcpy(stamp.data(), b + o.stamp, 8 * stamp.size());
+  std::memcpy(se.data(), b + o.expert, 4 * se.size());
+  std::memcpy(score.data(), b + o.score, 4 * score.size());
+  std::memcpy(usage.data(), b + o.usage, 4 * usage.size());
+  for (int l = 0; l < L; ++l) {
+    if (clock[l] >= (1ull << 48)) return MOE_ERR_INVALID_ARG;  // stamps are packed below 2^51 in the plan
+    for (int s = 0; s < S; ++s) {
+      const int32_t e = se[(size_t)l * S + s];
+      if (e < -1 || e >= E) return MOE_ERR_INVALID_ARG;
+      if (e < 0) continue;
+      if (es[(size_t)l * E + e] >= 0 || stamp[(size_t)l * S + s] > clock[l]) return MOE_ERR_INVALID_ARG;
+      es[(size_t)l * E + e] = s;
+    }
+    for (int e = 0; e < E; ++e) {
+      const float v = score[(size_t)l * E + e];
+      if (!(v >= 0.f) || std::isinf(v)) return MOE_ERR_INVALID_ARG;
+    }
+  }
+  cudaStream_t st = (cudaStream_t)cuda_stream;
+  FillLists fl;
+  if (!fl.alloc(S)) return MOE_ERR_OOM;
+  int rc = MOE_OK;
+  for (int l = 0; l < L && rc == MOE_OK; ++l) {
+    std::vector<MissItem> items;
+    for (int s = 0; s < S; ++s)
+      if (se[(size_t)l * S + s] >= 0) items.push_back(MissItem{se[(size_t)l * S + s], s, -1, 0});
+    rc = fill_layer_slots(c, l, items, fl.list, fl.hdr, st);
+  }
+  if (rc == MOE_OK &&
+      (cudaMemcpyAsync(c->d_slot_expert, se.data(), 4 * se.size(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaMemcpyAsync(c->d_expert_slot, es.data(), 4 * es.size(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaMemcpyAsync(c->d_slot_stamp, stamp.data(), 8 * stamp.size(), cudaMemcpyHostToDevice, st) !=
+           cudaSuccess ||
+       cudaMemcpyAsync(c->d_clock, clock.data(), 8 * clock.size(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaMemcpyAsync(c->d_score, score.data(), 4 * score.size(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaMemcpyAsync(c->d_usage, usage.data(), 4 * usage.size(), cudaMemcpyHostToDevice, st) != cudaSuccess ||
+       cudaStreamSynchronize(st) != cudaSuccess))
+    rc = MOE_ERR_CUDA;
   if (rc != MOE_OK) {
     cudaGetLastError();
     return poison(c, rc);

@@ -275,6 +275,7 @@ __global__ void __launch_bounds__(NT, 1) plan_kernel(PlanArgs a) {
     const bool miss = used && es0[e] < 0;
     code[e] = (hit ? 1 : 0) | (miss ? 1 << 16 : 0);
     if (hit) my_pick_hits += cnt[e];
+    if (used) a.usage[e] += (uint32_t)cnt[e];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) my_pick_hits += __shfl_xor_sync(0xffffffffu, my_pick_hits, o);
@@ -825,6 +826,7 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   }
   if (miss) a.miss[mr] = MissItem{e, vslot, evicted, 0};
   if (hit) a.slot_stamp[es0] = now;
+  if (lead) a.usage[e] += (uint32_t)cnt;
 
   // per-pair slot and stage
   const int pslot = __shfl_sync(F, my_slot, leader);

@@ -52,6 +52,12 @@ def test_host_only_calls(lib):
     assert lib.moe_layer_forward(None, 0, None, None, 1, None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_cache_sync(None, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_cache_launch_count(None) == 0
+    n = ctypes.c_uint64(0)
+    assert lib.moe_cache_state_size(None, ctypes.byref(n)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_cache_usage(None, None) == moe.MOE_ERR_INVALID_ARG
+    buf = ctypes.create_string_buffer(64)
+    assert lib.moe_cache_save_state(None, buf, 64) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_cache_load_state(None, buf, 64, None) == moe.MOE_ERR_INVALID_ARG
     lib.moe_cache_destroy(None)
 
 
@@ -86,14 +92,19 @@ int main(void) {
          sizeof(moe_host_store), sizeof(moe_cache_stats_t));
   printf("%zu %zu %zu\n", offsetof(moe_cache_stats_t, poisoned), offsetof(moe_cache_stats_t, last_error),
          offsetof(moe_cache_stats_t, cuda_error));
+  printf("%zu %zu %zu %u\n", sizeof(moe_cache_state_header), offsetof(moe_cache_state_header, expert_bytes),
+         offsetof(moe_cache_state_header, total_bytes), MOE_STATE_MAGIC);
   return 0;
 }''')
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
-    a, b = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines()
+    a, b, c = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines()
     a = [int(v) for v in a.split()]
     b = [int(v) for v in b.split()]
     assert a == [ctypes.sizeof(moe.MoeCacheConfig), moe.MoeCacheConfig.timeout_us.offset,
                  ctypes.sizeof(moe.MoeHostStore), ctypes.sizeof(moe.MoeCacheStats)]
     assert b == [moe.MoeCacheStats.poisoned.offset, moe.MoeCacheStats.last_error.offset,
                  moe.MoeCacheStats.cuda_error.offset]
+    assert [int(v) for v in c.split()] == [48, moe.MoeStateHeader.expert_bytes.offset,
+                                           moe.MoeStateHeader.total_bytes.offset, moe.MOE_STATE_MAGIC]
+    assert ctypes.sizeof(moe.MoeStateHeader) == 48
