@@ -293,6 +293,12 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
   float *gbase = xsum + (size_t)T * nbH;                        // per compute group, below
   __shared__ __align__(8) uint64_t full[NB], empty[NB], pub[kPubSlots], pubfree[kPubSlots];
   __shared__ int s_item[NB], s_pub[kPubSlots];
+  // each ring slot's work item and its pairs' rows (perm), written by the
+  // producer with the claim, and the same handed on to the publisher: no
+  // compute or combine step waits for a round trip to fetch them
+  __shared__ WorkItem s_work[NB];
+  __shared__ int s_prow[NB][TMAX], s_pub_n[kPubSlots], s_pub_prow[kPubSlots][TMAX];
+  __shared__ int s_grow[GROUPS][TMAX];  // the current item's pair rows, per compute group
   __shared__ int s_ok[GROUPS];  // decisions of a group's thread 0, read after a barrier
 
   auto mat_of = [&](int mat) -> const MatLayout & {
@@ -398,17 +404,23 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
             }
           }
           const uint32_t bytes = (uint32_t)(32 * nb * 18);
-          mbar_expect_tx(&full[s], bytes * wk.nt);
+          mbar_expect_tx_only(&full[s], bytes * wk.nt);
           bulk_g2s(dst, j.host + src * j.expert_stride + L.nib_off + (uint64_t)wk.tile * bytes, bytes * wk.nt,
                    &full[s]);
         } else {
           // tiled slot planes: nibbles [tiles][nb][32][16 B], then scales [tiles][nb][32]
           const uint8_t *slot = j.slots + (uint64_t)it.slot * j.slot_stride;
           const uint32_t bn = (uint32_t)nb * 512, bs = (uint32_t)nb * 64;
-          mbar_expect_tx(&full[s], (bn + bs) * wk.nt);
+          mbar_expect_tx_only(&full[s], (bn + bs) * wk.nt);
           bulk_g2s(dst, slot + L.nib_off + (uint64_t)wk.tile * bn, bn * wk.nt, &full[s]);
           bulk_g2s(dst + (size_t)bn * wk.nt, slot + L.sc_off + (uint64_t)wk.tile * bs, bs * wk.nt, &full[s]);
         }
+        // while the tiles are in flight: the item and its pairs' rows, then the
+        // arrival that (with the bytes) completes the slot's phase
+        s_work[s] = it;
+#pragma unroll
+        for (int q = 0; q < TMAX; ++q) s_prow[s][q] = q < it.pair_count ? j.perm[it.pair_begin + q] : 0;
+        mbar_arrive(&full[s]);
       }
     }
     return;
@@ -422,6 +434,10 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     qs.nH = hd->n_hits;
     qs.nM = hd->n_stage0_miss;
     const uint32_t ep = hd->epoch;
+    // lane q holds the router weight of pick q of token t in wreg[t] (k <= 32)
+    float wreg[TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) wreg[t] = (t < j.T && lane < j.k) ? j.w[t * j.k + lane] : 0.f;
     for (int c = 0;; ++c) {
       const int p = c % kPubSlots;
       int ok = 1;
@@ -433,27 +449,26 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
       }
       (void)mbar_try_wait(&pub[p], (uint32_t)(c / kPubSlots) & 1u);  // completed phase: acquire
       const int code = s_pub[p];
+      const int pc = s_pub_n[p];  // the item's pairs
+      const int prq = lane < TMAX ? s_pub_prow[p][lane] : 0;  // lane q: row of the item's pair q
       __syncwarp();
       if (lane == 0) mbar_arrive(&pubfree[p]);
       if (code < 0) break;
       const Work wk = decode_claim(code, qs);
-      const WorkItem it = j.items[wk.iu];
       if (wk.mat == 2) {
         // bit (tt * 8 + i): pick i of this item completed row tile tile + tt.
         // One counter per lane, all in flight together; meanwhile the first
         // two combinations' first 8 down rows are loaded on speculation (the
         // common single-token case: the tail of the call is then one round trip)
-        const int pc = it.pair_count, ncomb = wk.nt * pc;
+        const int ncomb = wk.nt * pc;
+        const int tl = __shfl_sync(0xffffffffu, prq, lane % pc) / j.k;
         int old = -1;
-        if (lane < ncomb) {
-          const int t = j.perm[it.pair_begin + lane % pc] / j.k;
-          old = atomicAdd(&j.sync[j.cbase + t * tH + wk.tile + lane / pc], 1);
-        }
+        if (lane < ncomb) old = atomicAdd(&j.sync[j.cbase + tl * tH + wk.tile + lane / pc], 1);
         uint64_t spec[2][8];
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2)
           if (c2 < ncomb) {
-            const int t = j.perm[it.pair_begin + c2 % pc] / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
+            const int t = __shfl_sync(0xffffffffu, prq, c2 % pc) / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
 #pragma unroll
             for (int i2 = 0; i2 < 8; ++i2)
               if (i2 < j.k) spec[c2][i2] = ld_tagged(j.y + ((size_t)t * j.k + i2) * j.H + r);
@@ -462,7 +477,11 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
         // weighted sum over the picks of each completed (token, row tile), ascending
         for (int c2 = 0; c2 < ncomb; ++c2) {
           if (!(last >> c2 & 1u)) continue;
-          const int t = j.perm[it.pair_begin + c2 % pc] / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
+          const int t = __shfl_sync(0xffffffffu, prq, c2 % pc) / j.k, r = (wk.tile + c2 / pc) * 32 + lane;
+          float wt = wreg[0];
+#pragma unroll
+          for (int tt = 1; tt < TMAX; ++tt)
+            if (t == tt) wt = wreg[tt];
           float o = 0.f;
           bool yok = true;
           // the k rows' words 8 at a time, all in flight together; one that does
@@ -478,10 +497,11 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
 #pragma unroll
             for (int i2 = 0; i2 < 8; ++i2)
               if (q0 + i2 < j.k) {
+                const float wq = __shfl_sync(0xffffffffu, wt, q0 + i2);
                 float yv = __uint_as_float((uint32_t)yw[i2]);
                 if ((uint32_t)(yw[i2] >> 32) != ep)
                   yok = wait_tagged(j.y + ((size_t)t * j.k + q0 + i2) * j.H + r, ep, j.sync + 2, yv, j.wait_ns) && yok;
-                o = fmaf(j.w[t * j.k + q0 + i2], yv, o);
+                o = fmaf(wq, yv, o);
               }
           }
           if (!yok) flag_error(j.err, 3);
@@ -548,18 +568,23 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     const int code = s_item[s];
     if (code < 0) break;
     const Work wk = decode_claim(code, qs);
-    const WorkItem it = j.items[wk.iu];
+    const int it_slot = s_work[s].slot, n = s_work[s].pair_count;
+    // the pairs' rows outlive the ring slot: kept for the group (read after its
+    // next barrier, rewritten only after the loop-top barrier of its next item)
+    if (gtid == 0)
+#pragma unroll
+      for (int q = 0; q < TMAX; ++q) s_grow[group][q] = s_prow[s][q];
     const MatLayout &L = mat_of(wk.mat);
     const bool is_down = wk.mat == 2;
-    const int nb = L.nb, K = 32 * nb, n = it.pair_count;
+    const int nb = L.nb, K = 32 * nb;
     const unsigned char *buf = ring + (size_t)s * slot_bytes;
-    uint8_t *slot = it.slot >= 0 ? j.slots + (uint64_t)it.slot * j.slot_stride : nullptr;
+    uint8_t *slot = it_slot >= 0 ? j.slots + (uint64_t)it_slot * j.slot_stride : nullptr;
 
     if (!is_down) {
       // ---- one 32-row tile of gate or up: inputs are the call's staged rows
       int qrow[TMAX];
 #pragma unroll
-      for (int q = 0; q < TMAX; ++q) qrow[q] = q < n ? j.perm[it.pair_begin + q] / j.k : 0;
+      for (int q = 0; q < TMAX; ++q) qrow[q] = q < n ? s_prow[s][q] / j.k : 0;
       const int row = lane;
       // blocks warp, warp + 8, ... in ascending order, two at a time; each is
       // added exactly as block_term adds it
@@ -598,7 +623,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
       for (int q = gwarp; q < n; q += kWarps) {
         float v = 0.f;
         for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
-        st_tagged(dst + (size_t)j.perm[it.pair_begin + q] * j.F + wk.tile * 32 + lane, v, ep);
+        st_tagged(dst + (size_t)s_grow[group][q] * j.F + wk.tile * 32 + lane, v, ep);
       }
     } else {
       // ---- up to kMaxDG 32-row tiles of down.  Each warp takes its blocks b
@@ -617,7 +642,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
       int prow[TMAX];
       uint64_t gw[TMAX], uw[TMAX];
 #pragma unroll
-      for (int q = 0; q < TMAX; ++q) prow[q] = q < n ? j.perm[it.pair_begin + q] : 0;
+      for (int q = 0; q < TMAX; ++q) prow[q] = q < n ? s_prow[s][q] : 0;
       auto fetch = [&](int b) {
 #pragma unroll
         for (int q = 0; q < TMAX; ++q)
@@ -692,7 +717,7 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
           for (int q = gwarp; q < n; q += kWarps) {
             float v = 0.f;
             for (int w2 = 0; w2 < kWarps; ++w2) v += red[(w2 * T + q) * 32 + lane];
-            st_tagged(j.y + (size_t)j.perm[it.pair_begin + q] * j.H + (wk.tile + tt) * 32 + lane, v, ep);
+            st_tagged(j.y + (size_t)s_grow[group][q] * j.H + (wk.tile + tt) * 32 + lane, v, ep);
           }
         }
       }
@@ -702,6 +727,9 @@ __global__ void __launch_bounds__(decode_threads(GROUPS), 1) decode_layer_kernel
     if (gtid == 0) {
       if (c >= kPubSlots && !ring_wait(&pubfree[p], (uint32_t)((c / kPubSlots) - 1) & 1u, j.wait_ns)) flag_error(j.err, 3);
       s_pub[p] = code;
+      s_pub_n[p] = n;
+#pragma unroll
+      for (int q = 0; q < TMAX; ++q) s_pub_prow[p][q] = s_grow[group][q];
     }
     mbar_arrive(&pub[p]);
   }
