@@ -137,14 +137,20 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(gsa(bar))
                : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, float v[16]) {
-  uint32_t r[16];
+// The warp's 32 lanes x 16 consecutive 32-bit columns of tensor memory into
+// registers; the values may be used only after tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t addr, uint32_t r[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(addr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, float v[16]) {
+  uint32_t r[16];
+  tmem_ld16_issue(addr, r);
+  tmem_ld_wait();
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -495,19 +501,35 @@ __global__ void __launch_bounds__(GemmCfg<NMAT, DQG>::kThreads, 1)
         p3 = 96 + lane < n ? pp[96 + lane] : 0;
       }
       for (int c0 = 0; c0 < nr; c0 += 16) {
-        float g[16], u[16];
         __syncwarp();
-        tmem_ld16(lane_addr + c0, g);
-        if (NMAT == 2) tmem_ld16(lane_addr + kGemmN + c0, u);
-        const int pr = c0 < 32 ? p0 : c0 < 64 ? p1 : c0 < 96 ? p2 : p3;
+        if (NMAT == 2) {
+          // gate and up columns loaded together; h = silu(g) * u for all 16, then
+          // the stores.  __expf and __fdividef err by a few fp32 ulps, far below
+          // the rounding of h to bf16 (an exponential that overflows gives h = 0,
+          // the value's limit)
+          uint32_t gr[16], ur[16];
+          tmem_ld16_issue(lane_addr + c0, gr);
+          tmem_ld16_issue(lane_addr + kGemmN + c0, ur);
+          tmem_ld_wait();
+          __nv_bfloat16 hb[16];
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) {
-          const int col = c0 + i2;
-          if (NMAT == 2) {
-            if (col < n && row < j.R)
-              j.h16s[(size_t)(wu.pair_begin + col) * j.R + row] =
-                  __float2bfloat16_rn(g[i2] / (1.f + expf(-g[i2])) * u[i2]);
-          } else {
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const float gv = __uint_as_float(gr[i2]), uv = __uint_as_float(ur[i2]);
+            hb[i2] = __float2bfloat16_rn(__fdividef(gv, 1.f + __expf(-gv)) * uv);
+          }
+          if (row < j.R) {
+            __nv_bfloat16 *dst = j.h16s + (size_t)(wu.pair_begin + c0) * j.R + row;
+#pragma unroll
+            for (int i2 = 0; i2 < 16; ++i2)
+              if (c0 + i2 < n) dst[(size_t)i2 * j.R] = hb[i2];
+          }
+        } else {
+          float g[16];
+          tmem_ld16(lane_addr + c0, g);
+          const int pr = c0 < 32 ? p0 : c0 < 64 ? p1 : c0 < 96 ? p2 : p3;
+#pragma unroll
+          for (int i2 = 0; i2 < 16; ++i2) {
+            const int col = c0 + i2;
             const int p = __shfl_sync(0xffffffffu, pr, (c0 & 31) + i2);
             if (col < n && row < j.R) j.y[(size_t)p * j.R + row] = g[i2];
           }
