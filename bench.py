@@ -341,9 +341,9 @@ def measured_peaks():
     return 6800.0, 1900.0, "fallback"
 
 
-def profiled_traffic_ratio(kernel):
-    """DRAM bytes per algorithmic byte of `kernel` from the committed ncu summary,
-    or None when the kernel's source changed since the capture."""
+def profiled_entry(kernel):
+    """The committed ncu figures of `kernel` (profiles/traffic.json), or None
+    when the kernel's source changed since the capture."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -358,7 +358,14 @@ def profiled_traffic_ratio(kernel):
         return None
     if hashlib.sha256(src[a:b].encode()).hexdigest() != d["source_sha256"]:
         return None
-    return float(d["dram_bytes_per_algorithmic_byte"])
+    return d
+
+
+def profiled_traffic_ratio(kernel):
+    """DRAM bytes per algorithmic byte of `kernel` from the committed ncu summary,
+    or None when the kernel's source changed since the capture."""
+    d = profiled_entry(kernel)
+    return float(d["dram_bytes_per_algorithmic_byte"]) if d else None
 
 
 def probe_h2d_sustained(store, block_bytes: int, n_blocks: int = 64, reps: int = 5):
@@ -999,6 +1006,7 @@ def main():
     # pull fill: the whole layer runs in the decode layer kernel, whose misses
     # cross the host link while its hits are read from HBM alongside
     dl = ktime.get("decode_layer", {"launches": 0, "ms": 0.0})
+    alu = None
     if dl["ms"] > 0:
         hit_b = dk["unique_hits"] * sh.expert_bytes
         per = 1.0 / max(1, dl["launches"])
@@ -1021,6 +1029,23 @@ def main():
                                 "their slots, activations and results; it overlaps the host-link reads. "
                                 "traffic: DRAM read + write per launch from the committed capture's DRAM "
                                 "bytes per hit-block byte (the slot writes stayed in L2 there)"}
+        # ALU budget: instructions per weight (the committed capture's count, spin
+        # waits included) x weights per second, against the issue rate of all SMs
+        ent = profiled_entry("decode_layer")
+        ipw = ent.get("warp_inst_per_weight") if ent else None
+        weights = (hit_b + miss_bytes_k) / sh.expert_bytes * 3 * sh.H * sh.F
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        mhz = (clk or {}).get("sm_mhz") or (clk or {}).get("sm_max_mhz")
+        alu_peak = sms * 4 * mhz * 1e6 / 1e9 if mhz else None
+        alu_ach = ipw * weights / (dl["ms"] * 1e-3) / 1e9 if ipw else None
+        alu = {"kernel": "decode_layer", "bound": "alu", "unit": "Gwarp-inst/s", "achieved": alu_ach,
+               "peak": alu_peak, "frac": alu_ach / alu_peak if alu_ach and alu_peak else None,
+               "warp_inst_per_weight": ipw, "weights_per_launch": weights * per,
+               "peak_source": f"{sms} SMs x 4 schedulers x 1 warp-instruction per cycle x the median SM "
+                              "clock sampled in the timed region",
+               "note": "instructions per weight: smsp__inst_executed.sum over the weights of the committed "
+                       "capture's launches (profiles/decode_layer_kernel.md), waits included; null once the "
+                       "kernel changed"}
     t_roof = (d["unique_hits"] * sh.expert_bytes / (hbm_peak * 1e9) +
               d["unique_misses"] * sh.expert_bytes / (h2d_peak * 1e9))
     t_roof_pb = (d["unique_hits"] * sh.expert_bytes / (hbm_peak * 1e9) +
@@ -1053,6 +1078,7 @@ def main():
         "achieved_hbm_gbs_step": (d["unique_hits"] + d["unique_misses"]) * sh.expert_bytes / (dev_ms * 1e-3) / 1e9,
         "roofline": roofline,
         "roofline_hbm": roofline_hbm,
+        "roofline_alu": alu,
         "step_roofline": step_roof,
         "steps_timed": stalls,
         "kernels": {k2: {"launches": v["launches"], "ms": round(v["ms"], 4)} for k2, v in ktime.items()
