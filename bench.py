@@ -834,8 +834,8 @@ def main():
                     raise moe.MoeError(rc, f"moe_layer_forward step {s} layer {l}")
 
     # ---- cold start: the first WC steps from an empty cache (the start of the
-    # warm-up; the rest of it runs below, untimed: on this pool a process's
-    # first seconds of host-link reads are sometimes much slower)
+    # warm-up; the rest of it runs below, untimed: on shared machines a
+    # process's first seconds of host-link reads are sometimes much slower)
     WC = min(COLD_STEPS, W)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -294,6 +294,9 @@ class Cache:
                 "visits": visits.reshape(T, k), "info": info.as_dict()}
 
     def stats(self, layer: int) -> dict:
+        """Counters of one layer (0 <= layer < L)."""
+        if not 0 <= layer < self.L:
+            raise IndexError(f"layer {layer} out of range [0, {self.L})")
         out = np.empty(NSTAT, np.uint64)
         lib().orc_cache_stats(self._h, layer, _p(out))
         return dict(zip(STAT_NAMES, (int(v) for v in out)))
