@@ -60,3 +60,33 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
 def test_cpu_model_names_the_host():
     m = bench.host_cpu_model()
     assert m.endswith(f"{__import__('os').cpu_count()} logical CPUs") and not m.startswith("unknown,")
+
+
+def test_profiled_figures_follow_the_kernel_source(tmp_path, monkeypatch):
+    # ncu figures (traffic ratio, instructions per weight) are used while the
+    # kernel's source text is the one captured, and dropped once it changes
+    import hashlib
+    import json
+    csrc = tmp_path / "router_softmax_top_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    src = "head\n<<kernel body>>\ntail\n"
+    (csrc / "k.cu").write_text(src)
+    body = src[src.find("<<"):src.find(">>")]
+    entry = {"file": "k.cu", "begin": "<<", "end": ">>",
+             "source_sha256": hashlib.sha256(body.encode()).hexdigest(),
+             "dram_bytes_per_algorithmic_byte": 1.01, "warp_inst_per_weight": 0.2}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"k": entry}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_entry("k")["warp_inst_per_weight"] == 0.2
+    assert bench.profiled_traffic_ratio("k") == 1.01
+    assert bench.profiled_entry("absent") is None
+    (csrc / "k.cu").write_text(src.replace("body", "b0dy"))
+    assert bench.profiled_entry("k") is None and bench.profiled_traffic_ratio("k") is None
+
+
+def test_committed_decode_figures_match_the_kernel():
+    # the committed capture is of the decode layer kernel as it stands
+    e = bench.profiled_entry("decode_layer")
+    assert e is not None, "decode_layer_kernel changed since profiles/traffic.json was captured"
+    assert 1.0 <= e["dram_bytes_per_algorithmic_byte"] < 1.05 and 0 < e["warp_inst_per_weight"] < 1
