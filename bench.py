@@ -1017,7 +1017,9 @@ def main():
                     "peak_source": peak_src,
                     "launches": dl["launches"], "avg_launch_us": 1e3 * dl["ms"] * per,
                     "alg_bytes_per_launch": miss_bytes_k * per,
-                    "note": "bytes of the missed expert blocks over the host link per launch / launch time"}
+                    "note": "bytes of the missed expert blocks over the host link per launch / launch time; "
+                            "traffic null: DRAM counters do not see the host link (the kernel's DRAM bytes, "
+                            "its hit blocks, are roofline_hbm.traffic)"}
         hbm_alg = hit_b + miss_bytes_k + picks_k * (2 * sh.H * 4 + 3 * sh.F * 4)
         roofline_hbm = {"kernel": "decode_layer", "bound": "hbm", "achieved": hbm_alg / (dl["ms"] * 1e-3) / 1e9,
                         "peak": hbm_peak, "unit": "GB/s",
