@@ -200,6 +200,10 @@ def parse():
     ap.add_argument("--preload-profile", type=int, default=0,
                     help="warm start: before the first step, preload each layer's most-used experts, "
                          "counted over this many tokens of another token stream with the same routing")
+    ap.add_argument("--preload-from-session", type=int, default=0,
+                    help="warm start from the library's own counts: a previous session (another handle "
+                         "over the same store) decodes this many tokens of another token stream with the "
+                         "same routing, its moe_cache_usage counts are read at its end and preloaded here")
     ap.add_argument("--slots", type=int, default=0,
                     help="decode and prefill workloads: slots per layer instead of the config's (up to "
                          "the number of experts: every expert resident once warm)")
@@ -812,6 +816,32 @@ def main():
         preload = {"profile_tokens": args.preload_profile, "stream": PROFILE_STREAM,
                    "experts": int(np.minimum((counts > 0).sum(1), sh.S).sum()),
                    "s": time.time() - t0}
+    elif args.preload_from_session:
+        # the previous session: its own handle, the other token stream, then
+        # its lifetime usage counts are what this session preloads
+        n = args.preload_from_session
+        if T != 1:
+            raise SystemExit("--preload-from-session: one token per step (decode workloads at batch 1)")
+        prev = moe.MoECache(n_layers=sh.L, n_experts=sh.E, top_k=sh.k, hidden=sh.H, ffn=sh.F,
+                            slots_per_layer=sh.S, max_tokens=T, store=store, fill_mode=fill,
+                            timeout_us=30_000_000)
+        lg_prev = torch.from_numpy(np.stack([synth.logits_from_picks(
+            synth.trace(n, sh.E, sh.k, sh.zipf, sh.sticky, rank, l, PROFILE_STREAM), sh.E, rank, l,
+            PROFILE_STREAM, 0) for l in range(sh.L)], axis=1)).cuda()          # [n, L, E]
+        x_prev = torch.zeros((sh.L, T, sh.H), dtype=torch.float32, device="cuda")
+        out_prev = torch.empty((T, sh.H), dtype=torch.float32, device="cuda")
+        for s_ in range(n):
+            for l in range(sh.L):
+                prev.forward(l, lg_prev[s_, l].view(T, sh.E), x_prev[l], out=out_prev)
+        counts = prev.usage()
+        prev_stats = prev.stats(-1)
+        prev.close()
+        t0 = time.time()
+        cache.preload(counts)
+        preload = {"session_tokens": n, "stream": PROFILE_STREAM, "counts_sum": int(counts.sum()),
+                   "session_pick_hit_rate": prev_stats["pick_hits"] / max(1, prev_stats["pick_hits"] +
+                                                                       prev_stats["pick_misses"]),
+                   "experts": int(np.minimum((counts > 0).sum(1), sh.S).sum()), "s": time.time() - t0}
     setup_s = time.time() - t_setup
     h2d_gbps = cache.probe_h2d(24)
     h2d_sus = probe_h2d_sustained(store, eb)
