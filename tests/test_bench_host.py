@@ -32,6 +32,7 @@ def test_defaults(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py"])
     a = bench.resolve_defaults(bench.parse())
     assert (a.gpus, a.impl, a.workload, a.fill, a.policy) == (1, "ours", "decode", "pull", "lru")
+    assert a.preload_profile == 0 and a.preload_from_session == 0   # cold start unless asked
     assert a.warmup == bench.DECODE_WARMUP >= bench.COLD_STEPS >= 3 and a.steps >= 1
     for extra in (["--workload", "prefill"], ["--impl", "reference"]):
         monkeypatch.setattr(sys, "argv", ["bench.py"] + extra)
