@@ -132,8 +132,9 @@ __device__ void route_values(const float v[VPL], int E, int k, int weight_mode, 
     my_p = expf(__uint_as_float(kb) - m) / z;
   }
   float sum = lane < k ? my_p : 0.f;
+  if (weight_mode == 1)  // the sum over the picks renormalises (mode 1 only)
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   if (lane < k) {
     ids[lane] = my_id;
     if (s_ids) s_ids[lane] = my_id;
@@ -652,26 +653,42 @@ __global__ void __launch_bounds__(32, 1) plan_small_kernel(PlanArgs a) {
   // ids gives every leader its item rank, pair offset and unit offset in the
   // item order (hits ascending, then misses ascending)
   const int ucount = (cnt + kTokPerUnit - 1) / kTokPerUnit;
-  const int csz = (E + 31) / 32;  // experts per lane in the scan
-  for (int i = lane; i < csz * 32; i += 32) s_pack[i] = 0ull;
-  __syncwarp();
-  if (lead)
-    s_pack[e] = hit ? (1ull | ((uint64_t)cnt << 16) | ((uint64_t)ucount << 32))
-                    : ((1ull << 8) | ((uint64_t)cnt << 24) | ((uint64_t)ucount << 40));
-  __syncwarp();
-  uint64_t part = 0;
-  for (int i = 0; i < csz; ++i) part += s_pack[lane * csz + i];
-  uint64_t incl = part;
+  uint64_t total, before;
+  if (T == 1) {
+    // one token: k distinct experts, one pair and one unit each, so an
+    // expert's prefix is the number of hit and of miss experts of lower id
+    // (the fields the scan below gives), from k shuffles
+    int bh = 0, bm = 0;
+    for (int jl = 0; jl < k; ++jl) {
+      const int ej = __shfl_sync(F, e, jl);
+      bh += ((hmask >> jl) & 1u) && ej < e;
+      bm += ((mmask >> jl) & 1u) && ej < e;
+    }
+    auto pack = [](uint64_t h, uint64_t m) { return h | (m << 8) | (h << 16) | (m << 24) | (h << 32) | (m << 40); };
+    total = pack((uint64_t)nH, (uint64_t)nM);
+    before = pack((uint64_t)bh, (uint64_t)bm);
+  } else {
+    const int csz = (E + 31) / 32;  // experts per lane in the scan
+    for (int i = lane; i < csz * 32; i += 32) s_pack[i] = 0ull;
+    __syncwarp();
+    if (lead)
+      s_pack[e] = hit ? (1ull | ((uint64_t)cnt << 16) | ((uint64_t)ucount << 32))
+                      : ((1ull << 8) | ((uint64_t)cnt << 24) | ((uint64_t)ucount << 40));
+    __syncwarp();
+    uint64_t part = 0;
+    for (int i = 0; i < csz; ++i) part += s_pack[lane * csz + i];
+    uint64_t incl = part;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint64_t y = __shfl_up_sync(F, incl, o);
-    if (lane >= o) incl += y;
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t y = __shfl_up_sync(F, incl, o);
+      if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(F, incl, 31);
+    const int src = lead ? e / csz : 0;
+    before = __shfl_sync(F, incl - part, src);  // exclusive prefix of my expert's chunk
+    if (lead)
+      for (int i = src * csz; i < e; ++i) before += s_pack[i];
   }
-  const uint64_t total = __shfl_sync(F, incl, 31);
-  const int src = lead ? e / csz : 0;
-  uint64_t before = __shfl_sync(F, incl - part, src);  // exclusive prefix of my expert's chunk
-  if (lead)
-    for (int i = src * csz; i < e; ++i) before += s_pack[i];
   auto field = [](uint64_t v, int f) { return (int)((v >> (8 * f)) & 0xffull); };
   const int tot_hit_pairs = field(total, 2), tot_hit_units = field(total, 4);
   const int hr = field(before, 0), mr = field(before, 1);
